@@ -1,0 +1,124 @@
+"""CPU float64 oracle for global attention with decomposed relative-position bias.
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline / reference arm of ``bench.py`` may import or call this module.  The
+product path (the CUDA library and its binding) never does, and this module
+imports nothing from the product.
+
+Source: vLLM PR #55629 page ("为 DeepEncoder 全局注意力融合相对位置偏置到 Triton 内核").
+
+* Section 关键源码片段 (key source excerpt): ``add_decomposed_rel_pos(q,
+  rel_pos_h, rel_pos_w, (H, W), (H, W))`` returns ``rel_h`` and ``rel_w``; the
+  fallback branch builds ``attn_bias = (rel_h + rel_w).view(B, heads, HW, H*W)``
+  and calls ``F.scaled_dot_product_attention(q, k, v, attn_mask=attn_bias)``.
+  That additive-mask call *defines* the result:
+  ``out = softmax(scale * q k^T + bias) v`` with ``scale = d**-0.5``.
+* The page does not print the body of ``add_decomposed_rel_pos``.  Reading
+  taken (SAM-style decomposed relative position, consistent with the table
+  lengths 2H-1 / 2W-1 and the ``.view`` above):
+  ``rel_h[n, kh] = q_n . rel_pos_h[qh(n) - kh + H - 1]`` and
+  ``rel_w[n, kw] = q_n . rel_pos_w[qw(n) - kw + W - 1]``, with row-major token
+  order ``n = qh*W + qw`` and key order ``m = kh*W + kw``; the projection uses
+  the unscaled q (it runs before SDPA applies the scale).
+* Section 风险与影响 (risks): the fast path accumulates in fp32; the oracle is
+  exact float64 softmax (a row-max shift is used only to avoid overflow).
+
+All functions take array-likes (converted to float64) shaped
+``q, k, v: [BH, N, d]``, ``rel_pos_h: [2H-1, d]``, ``rel_pos_w: [2W-1, d]``,
+``rel_h: [BH, N, H]``, ``rel_w: [BH, N, W]``.
+
+Pins: every function here is pinned in ``tests/test_oracle.py`` against
+brute force, the library SDPA routine, closed forms and hand-derived golden
+fixtures; none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def _f64(x) -> np.ndarray:
+    return np.asarray(x, dtype=np.float64)
+
+
+def rel_index(length: int) -> np.ndarray:
+    """Table row used for query coordinate a and key coordinate b: ``a - b + length - 1``."""
+    a = np.arange(length)[:, None]
+    b = np.arange(length)[None, :]
+    return a - b + length - 1
+
+
+def project(q, rel_pos_h, rel_pos_w, H: int, W: int):
+    """Decomposed rel-pos projection: ``(rel_h [BH,N,H], rel_w [BH,N,W])`` in float64."""
+    q = _f64(q)
+    th, tw = _f64(rel_pos_h), _f64(rel_pos_w)
+    BH, N, d = q.shape
+    if N != H * W:
+        raise ValueError("N must equal H*W")
+    if th.shape != (2 * H - 1, d) or tw.shape != (2 * W - 1, d):
+        raise ValueError("tables must be [2H-1, d] and [2W-1, d]")
+    qg = q.reshape(BH, H, W, d)                 # token n = qh*W + qw
+    Rh = th[rel_index(H)]                       # [qh, kh, d]
+    Rw = tw[rel_index(W)]                       # [qw, kw, d]
+    rel_h = np.einsum("bhwc,hkc->bhwk", qg, Rh, optimize=True).reshape(BH, N, H)
+    rel_w = np.einsum("bhwc,wkc->bhwk", qg, Rw, optimize=True).reshape(BH, N, W)
+    return rel_h, rel_w
+
+
+def project_rows(q_rows, rows, rel_pos_h, rel_pos_w, H: int, W: int):
+    """Projection for selected token rows only: ``q_rows [R, d]``, token indices ``rows [R]``."""
+    q_rows = _f64(q_rows)
+    rows = np.asarray(rows, dtype=np.int64)
+    th, tw = _f64(rel_pos_h), _f64(rel_pos_w)
+    qh, qw = rows // W, rows % W
+    Rh = th[qh[:, None] - np.arange(H)[None, :] + H - 1]      # [R, H, d]
+    Rw = tw[qw[:, None] - np.arange(W)[None, :] + W - 1]      # [R, W, d]
+    return np.einsum("rc,rkc->rk", q_rows, Rh), np.einsum("rc,rkc->rk", q_rows, Rw)
+
+
+def dense_bias(rel_h_b, rel_w_b, H: int, W: int) -> np.ndarray:
+    """The materialised bias of one (batch, head): ``Bias[n, kh*W + kw] = rel_h[n, kh] + rel_w[n, kw]``."""
+    rel_h_b, rel_w_b = _f64(rel_h_b), _f64(rel_w_b)
+    R = rel_h_b.shape[0]
+    return (rel_h_b[:, :, None] + rel_w_b[:, None, :]).reshape(R, H * W)
+
+
+def _softmax_rows(logits: np.ndarray) -> np.ndarray:
+    z = logits - logits.max(axis=-1, keepdims=True)
+    e = np.exp(z)
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def attention(q, k, v, rel_h, rel_w, H: int, W: int, scale: float) -> np.ndarray:
+    """``out[b] = softmax(scale * q[b] k[b]^T + Bias[b]) v[b]`` for every (batch, head) b."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    rel_h, rel_w = _f64(rel_h), _f64(rel_w)
+    BH, N, _ = q.shape
+    if N != H * W:
+        raise ValueError("N must equal H*W")
+    out = np.empty((BH, N, v.shape[2]), dtype=np.float64)
+    for b in range(BH):
+        logits = scale * (q[b] @ k[b].T) + dense_bias(rel_h[b], rel_w[b], H, W)
+        out[b] = _softmax_rows(logits) @ v[b]
+    return out
+
+
+def attention_rows(q, k, v, rel_h_rows, rel_w_rows, b: int, rows, H: int, W: int, scale: float) -> np.ndarray:
+    """Output rows ``rows`` of head ``b`` only; ``rel_*_rows`` hold the bias of those rows."""
+    rows = np.asarray(rows, dtype=np.int64)
+    qb = _f64(q[b])[rows]
+    kb, vb = _f64(k[b]), _f64(v[b])
+    logits = scale * (qb @ kb.T) + dense_bias(rel_h_rows, rel_w_rows, H, W)
+    return _softmax_rows(logits) @ vb
+
+
+def fused(q, k, v, rel_pos_h, rel_pos_w, H: int, W: int, scale: float) -> np.ndarray:
+    """Projection followed by attention, the whole path in float64."""
+    rel_h, rel_w = project(q, rel_pos_h, rel_pos_w, H, W)
+    return attention(q, k, v, rel_h, rel_w, H, W, scale)
+
+
+def fused_rows(q, k, v, rel_pos_h, rel_pos_w, b: int, rows, H: int, W: int, scale: float) -> np.ndarray:
+    """Selected output rows of head ``b`` of :func:`fused`."""
+    rows = np.asarray(rows, dtype=np.int64)
+    rh, rw = project_rows(_f64(q[b])[rows], rows, rel_pos_h, rel_pos_w, H, W)
+    return attention_rows(q, k, v, rh, rw, b, rows, H, W, scale)
