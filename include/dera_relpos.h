@@ -1,0 +1,149 @@
+/*
+ * dera_relpos — global self-attention with decomposed relative-position bias
+ * (the DeepEncoder / SAM-style "rel-pos" attention), on GB300 (sm_103a).
+ *
+ * Source of the operation: vLLM PR #55629 page ("为 DeepEncoder 全局注意力融合
+ * 相对位置偏置到 Triton 内核").
+ *   - Section 关键源码片段 (key source excerpt): RelPosAttention.forward calls
+ *     add_decomposed_rel_pos(q, rel_pos_h, rel_pos_w, (H,W), (H,W)) and then
+ *     either the fused launcher deepencoder_rel_pos_attention(q, k, v,
+ *     rel_h.squeeze(-1), rel_w.squeeze(-2), W, scale) or SDPA with the
+ *     materialised bias (rel_h + rel_w).view(B, heads, HW, H*W).  The SDPA
+ *     call defines the result:
+ *         out[n] = sum_m softmax_m(scale * q_n.k_m + rel_h[n, kh(m)] + rel_w[n, kw(m)]) v_m
+ *     with tokens n = qh*W + qw and keys m = kh*W + kw.
+ *   - The body of add_decomposed_rel_pos is not printed; this library takes
+ *     the SAM-style reading rel_h[n, kh] = q_n . rel_pos_h[qh - kh + H - 1] and
+ *     rel_w[n, kw] = q_n . rel_pos_w[qw - kw + W - 1] (unscaled q).
+ *   - Section 实现拆解 (implementation breakdown) item 1: the fused kernel
+ *     streams keys/values with an online softmax and adds the bias slice per
+ *     key block, never building the HW x HW bias.
+ *   - Section 风险与影响 (risks): fp32 accumulation, exp2; fast path only for
+ *     FP16/BF16 with head_dim 64.
+ *   - Section 评论区精华 (review discussion): all five launcher inputs must be
+ *     device tensors on the same device.
+ *
+ * Conventions shared by every entry point
+ *   - All pointers are DEVICE pointers on the current CUDA device, except
+ *     where an argument says otherwise.  The caller owns every buffer; the
+ *     library allocates nothing, never synchronises, and enqueues all work on
+ *     `stream` (a cudaStream_t passed as void*; NULL = legacy default stream).
+ *   - Layouts are contiguous, row-major:
+ *       q, k, v, out : [BH, N, head_dim], N = H*W, token n = qh*W + qw
+ *       rel_pos_h    : [2H-1, head_dim]      rel_pos_w : [2W-1, head_dim]
+ *       rel_h        : [BH, N, H]            rel_w     : [BH, N, W]
+ *   - head_dim must be 64.  q, k, v, tables share one dtype: DERA_F16 or
+ *     DERA_BF16.  1 <= H, W <= 64.  BH >= 0 (BH == 0 is a no-op).
+ *   - Every pointer must be 16-byte aligned (TMA operands).
+ *   - Argument errors are detected on the host before anything is enqueued
+ *     and returned as a status; nothing falls back to another backend.
+ *   - DERA_ERR_CUDA: a CUDA call made by the library failed (launch error,
+ *     invalid device pointer query).  The sticky CUDA error, if any, is left
+ *     for the caller to inspect.
+ *   - A kernel that exceeds its internal bounded-wait budget (about one
+ *     second per wait) stops early and records DERA_ERR_TIMEOUT in the
+ *     library's device status word; read it with dera_relpos_device_status().
+ *     Its output is then undefined.
+ *   - All entry points are stream-ordered and allocation-free, so they can be
+ *     captured in a CUDA graph.
+ */
+#ifndef DERA_RELPOS_H
+#define DERA_RELPOS_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DERA_RELPOS_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define DERA_API __attribute__((visibility("default")))
+#else
+#define DERA_API
+#endif
+
+typedef enum dera_status {
+  DERA_OK = 0,
+  DERA_ERR_NULL = 1,        /* a required pointer is NULL */
+  DERA_ERR_SHAPE = 2,       /* H, W, BH out of range, or N overflow */
+  DERA_ERR_DTYPE = 3,       /* dtype not supported for that argument */
+  DERA_ERR_HEAD_DIM = 4,    /* head_dim != 64 */
+  DERA_ERR_ALIGN = 5,       /* a pointer is not 16-byte aligned */
+  DERA_ERR_DEVICE = 6,      /* a pointer is not device memory of the current device */
+  DERA_ERR_TIMEOUT = 7,     /* (device status only) a bounded wait expired */
+  DERA_ERR_CUDA = 8         /* a CUDA runtime/driver call failed */
+} dera_status;
+
+typedef enum dera_dtype { DERA_F16 = 0, DERA_BF16 = 1, DERA_F32 = 2 } dera_dtype;
+
+/*
+ * A1 — decomposed rel-pos projection (add_decomposed_rel_pos; page section
+ * 关键源码片段, and the squeeze to the compact [.., HW, H] / [.., HW, W] form
+ * of section 实现拆解 item 2):
+ *     rel_h[b, n, kh] = sum_c q[b, n, c] * rel_pos_h[qh(n) - kh + H - 1, c]
+ *     rel_w[b, n, kw] = sum_c q[b, n, c] * rel_pos_w[qw(n) - kw + W - 1, c]
+ * in:  q [BH,N,64], rel_pos_h [2H-1,64], rel_pos_w [2W-1,64], all in_dtype
+ *      (DERA_F16 | DERA_BF16).
+ * out: rel_h [BH,N,H], rel_w [BH,N,W] in bias_dtype (DERA_F32, or
+ *      DERA_BF16/DERA_F16, rounded to nearest from the fp32 accumulator).
+ */
+DERA_API dera_status dera_relpos_project(const void* q, const void* rel_pos_h, const void* rel_pos_w, void* rel_h,
+                                void* rel_w, int BH, int H, int W, int head_dim, dera_dtype in_dtype,
+                                dera_dtype bias_dtype, void* stream);
+
+/*
+ * A2..A7 — attention with a compact bias (deepencoder_rel_pos_attention;
+ * page sections 关键源码片段 and 实现拆解 item 1):
+ *     out[b, n] = sum_m softmax_m(scale * q[b,n].k[b,m] + rel_h[b,n,kh(m)] + rel_w[b,n,kw(m)]) v[b,m]
+ * in:  q, k, v [BH,N,64] in_dtype (DERA_F16 | DERA_BF16);
+ *      rel_h [BH,N,H], rel_w [BH,N,W] in bias_dtype (DERA_F32 | DERA_BF16 | DERA_F16).
+ * out: out [BH,N,64] in out_dtype (DERA_F32, or in_dtype).
+ * Softmax runs in base 2 with fp32 accumulation; P is rounded to fp16 for the
+ * P.V product (for bf16 inputs, V tiles are converted to fp16 on chip, so
+ * |v| must stay below 65504).
+ */
+DERA_API dera_status dera_relpos_attention(const void* q, const void* k, const void* v, const void* rel_h,
+                                  const void* rel_w, void* out, int BH, int H, int W, int head_dim, float scale,
+                                  dera_dtype in_dtype, dera_dtype bias_dtype, dera_dtype out_dtype,
+                                  void* stream);
+
+/*
+ * A1..A7 fused — projection computed inside the attention kernel (tensor-core
+ * q.rel_pos^T products, skewed on chip), so neither the dense HW x HW bias
+ * nor the compact rel_h / rel_w ever reaches global memory.
+ * in:  q, k, v [BH,N,64], rel_pos_h [2H-1,64], rel_pos_w [2W-1,64], in_dtype.
+ * out: out [BH,N,64] in out_dtype (DERA_F32, or in_dtype).
+ */
+DERA_API dera_status dera_relpos_fused(const void* q, const void* k, const void* v, const void* rel_pos_h,
+                              const void* rel_pos_w, void* out, int BH, int H, int W, int head_dim, float scale,
+                              dera_dtype in_dtype, dera_dtype out_dtype, void* stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+DERA_API const char* dera_status_string(dera_status status);
+
+/*
+ * Reads the device status word of the current device into *status (host
+ * pointer) and, if reset != 0, clears it.  Synchronises the current device.
+ * Returns DERA_ERR_NULL for a NULL status pointer, DERA_ERR_CUDA if the copy
+ * fails.  *status is DERA_OK or DERA_ERR_TIMEOUT.
+ */
+DERA_API dera_status dera_relpos_device_status(int* status, int reset);
+
+/*
+ * Self-test of the bounded wait: launches one CTA that waits on an mbarrier
+ * that nothing ever arrives on, with a budget of `budget_cycles` SM cycles
+ * (clamped to [1e3, 4e9]).  The kernel gives up, writes DERA_ERR_TIMEOUT to
+ * the device status word and exits normally; the host reads it back with
+ * dera_relpos_device_status().  Used by tests to show that an expired wait
+ * ends in an error status rather than a hang.
+ */
+DERA_API dera_status dera_relpos_selftest_wait_timeout(long long budget_cycles, void* stream);
+
+/* Compile-time ABI version of the loaded library (DERA_RELPOS_ABI_VERSION). */
+DERA_API int dera_relpos_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DERA_RELPOS_H */

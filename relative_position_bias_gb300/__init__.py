@@ -1,0 +1,12 @@
+"""GB300-native global attention with decomposed relative-position bias.
+
+The computation lives in ``libdera_relpos.so`` (hand-written sm_103a CUDA
+behind a C ABI, declared in ``include/dera_relpos.h``); this package is its
+thin Python binding.  Entry points: :func:`project`, :func:`attention`,
+:func:`fused`.
+"""
+from .api import (DERA_BF16, DERA_F16, DERA_F32, DeraError, attention, declared_entry_points, device_status, fused,
+                  load_library, project, selftest_wait_timeout)
+
+__all__ = ["DERA_BF16", "DERA_F16", "DERA_F32", "DeraError", "attention", "declared_entry_points", "device_status",
+           "fused", "load_library", "project", "selftest_wait_timeout"]

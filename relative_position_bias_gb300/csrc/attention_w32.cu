@@ -1,0 +1,6 @@
+// Attention kernels for key tiles padded to 32 grid columns.
+#include "attention_inst.cuh"
+
+namespace dera {
+template cudaError_t launch_attention<32>(const AttnMaps&, const AttnArgs&, bool, cudaStream_t);
+}  // namespace dera

@@ -1,0 +1,326 @@
+// C-ABI of libdera_relpos: argument validation, TMA descriptors and kernel
+// dispatch for the decomposed rel-pos attention path.  Declarations and the
+// contract of every entry point are in include/dera_relpos.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <initializer_list>
+#include <mutex>
+
+#include "../../include/dera_relpos.h"
+#include "launch.cuh"
+#include "project.cuh"
+
+namespace dera {
+
+// Device status word: 0, or DERA_ERR_TIMEOUT once a bounded wait expired.
+__device__ int g_status_word = 0;
+
+cudaError_t launch_project(const CUtensorMap& q, const CUtensorMap& th, const CUtensorMap& tw,
+                           const ProjArgs& args, int in_fmt, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(relpos_project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       ProjSmem::kAlloc);
+  if (e != cudaSuccess) return e;
+  const int n_qtiles = (args.N + kBlockM - 1) / kBlockM;
+  const unsigned grid = static_cast<unsigned>(n_qtiles) * static_cast<unsigned>(args.BH);
+  relpos_project_kernel<<<grid, kProjThreads, ProjSmem::kAlloc, stream>>>(q, th, tw, args, in_fmt, n_qtiles);
+  return cudaGetLastError();
+}
+
+// One thread waits on an mbarrier that nothing arrives on; the bounded wait
+// gives up after `budget` cycles and records DERA_ERR_TIMEOUT.
+__global__ void wait_selftest_kernel(int* status, long long budget) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    if (!mbar_wait_budget(&bar, 0, budget)) atomicCAS(status, 0, DERA_ERR_TIMEOUT);
+  }
+}
+
+cudaError_t launch_wait_selftest(int* status, long long budget, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(status, budget);
+  return cudaGetLastError();
+}
+
+}  // namespace dera
+
+using namespace dera;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Device address of the status word on the current device (looked up once per device).
+int* status_ptr(int dev) {
+  static int* ptrs[kMaxDevices] = {};
+  static std::mutex mu;
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+bool is16(dera_dtype t) { return t == DERA_F16 || t == DERA_BF16; }
+bool is_float(dera_dtype t) { return t == DERA_F16 || t == DERA_BF16 || t == DERA_F32; }
+int fmt_of(dera_dtype t) { return t == DERA_F16 ? kF16 : (t == DERA_BF16 ? kBF16 : kF32); }
+
+dera_status check_shape(int BH, int H, int W, int head_dim) {
+  if (head_dim != kHeadDim) return DERA_ERR_HEAD_DIM;
+  if (BH < 0 || H < 1 || W < 1 || H > 64 || W > 64) return DERA_ERR_SHAPE;
+  // grid size: ceil(N/256) CTAs per head must fit 2^31 - 1 in total
+  const long long pairs = (static_cast<long long>(H) * W + 255) / 256;
+  if (pairs * BH > 0x7fffffffLL) return DERA_ERR_SHAPE;
+  return DERA_OK;
+}
+
+// Host-only checks: non-null and 16-byte aligned (TMA operands).
+dera_status check_host(std::initializer_list<const void*> ptrs) {
+  for (const void* p : ptrs)
+    if (!p) return DERA_ERR_NULL;
+  for (const void* p : ptrs)
+    if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return DERA_ERR_ALIGN;
+  return DERA_OK;
+}
+
+// Device memory of device `dev` (the launcher's same-device rule).
+dera_status check_ptr(const void* p, int dev) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return DERA_ERR_DEVICE;
+  }
+  if ((a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) || a.device != dev)
+    return DERA_ERR_DEVICE;
+  return DERA_OK;
+}
+
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int rank, const cuuint64_t* dims,
+              const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  std::memset(m, 0, sizeof(*m));
+  return fn(m, dt, rank, const_cast<void*>(base), dims, strides_bytes, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+CUtensorMapDataType tma_type(dera_dtype t) {
+  return t == DERA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
+
+// q / out-like tensor [BH, N, 64] read in 128-row tiles
+bool map_rows(CUtensorMap* m, const void* p, dera_dtype t, int BH, int N) {
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(N) * 128};
+  const cuuint32_t box[3] = {64, 128, 1};
+  return make_map(m, p, tma_type(t), 3, dims, strides, box);
+}
+
+// k / v viewed as [BH, H, W, 64], read in tiles of KHT grid rows x WP columns
+bool map_keys(CUtensorMap* m, const void* p, dera_dtype t, int BH, int H, int W, int WP, int KHT) {
+  const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(W), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[3] = {128, static_cast<cuuint64_t>(W) * 128, static_cast<cuuint64_t>(H) * W * 128};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(WP), static_cast<cuuint32_t>(KHT), 1};
+  return make_map(m, p, tma_type(t), 4, dims, strides, box);
+}
+
+// table [2L-1, 64], one 128-row box (rows past 2L-1 read as zero)
+bool map_table(CUtensorMap* m, const void* p, dera_dtype t, int L) {
+  const cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(2 * L - 1)};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {64, 128};
+  return make_map(m, p, tma_type(t), 2, dims, strides, box);
+}
+
+int padded_width(int W) { return W <= 16 ? 16 : (W <= 32 ? 32 : (W <= 40 ? 40 : 64)); }
+int rows_per_tile(int WP) { return WP <= 16 ? 8 : (WP <= 32 ? 4 : 2); }
+
+dera_status current_device(int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess) {
+    cudaGetLastError();
+    return DERA_ERR_CUDA;
+  }
+  return DERA_OK;
+}
+
+#define DERA_TRY(expr)              \
+  do {                              \
+    const dera_status s_ = (expr);  \
+    if (s_ != DERA_OK) return s_;   \
+  } while (0)
+
+dera_status run_attention(const void* q, const void* k, const void* v, const void* a, const void* b, void* out,
+                          int BH, int H, int W, float scale, dera_dtype in_dtype, dera_dtype bias_dtype,
+                          dera_dtype out_dtype, bool fused, void* stream) {
+  int dev = 0;
+  DERA_TRY(current_device(&dev));
+  const int N = H * W;
+  const int WP = padded_width(W), KHT = rows_per_tile(WP);
+  AttnMaps maps;
+  if (!map_rows(&maps.q, q, in_dtype, BH, N) || !map_keys(&maps.k, k, in_dtype, BH, H, W, WP, KHT) ||
+      !map_keys(&maps.v, v, in_dtype, BH, H, W, WP, KHT))
+    return DERA_ERR_CUDA;
+  if (fused) {
+    if (!map_table(&maps.th, a, in_dtype, H) || !map_table(&maps.tw, b, in_dtype, W)) return DERA_ERR_CUDA;
+  } else {
+    maps.th = maps.q;  // unused by the compact-bias kernel
+    maps.tw = maps.q;
+  }
+  AttnArgs args;
+  args.rel_h = fused ? nullptr : a;
+  args.rel_w = fused ? nullptr : b;
+  args.out = out;
+  args.status = status_ptr(dev);
+  if (!args.status) return DERA_ERR_CUDA;
+  args.BH = BH;
+  args.H = H;
+  args.W = W;
+  args.N = N;
+  args.n_qtiles = (N + kBlockM - 1) / kBlockM;
+  args.n_pairs = (args.n_qtiles + 1) / 2;
+  args.n_kv = (H + KHT - 1) / KHT;
+  args.scale_log2 = scale * kLog2e;
+  args.in_fmt = fmt_of(in_dtype);
+  args.bias_fmt = fmt_of(bias_dtype);
+  args.out_fmt = fmt_of(out_dtype);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  switch (WP) {
+    case 16: e = launch_attention<16>(maps, args, fused, s); break;
+    case 32: e = launch_attention<32>(maps, args, fused, s); break;
+    case 40: e = launch_attention<40>(maps, args, fused, s); break;
+    default: e = launch_attention<64>(maps, args, fused, s); break;
+  }
+  return e == cudaSuccess ? DERA_OK : DERA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dera_status_string(dera_status status) {
+  switch (status) {
+    case DERA_OK: return "DERA_OK";
+    case DERA_ERR_NULL: return "DERA_ERR_NULL: a required pointer is NULL";
+    case DERA_ERR_SHAPE: return "DERA_ERR_SHAPE: H, W or BH out of range";
+    case DERA_ERR_DTYPE: return "DERA_ERR_DTYPE: unsupported dtype for this argument";
+    case DERA_ERR_HEAD_DIM: return "DERA_ERR_HEAD_DIM: head_dim must be 64";
+    case DERA_ERR_ALIGN: return "DERA_ERR_ALIGN: pointer not 16-byte aligned";
+    case DERA_ERR_DEVICE: return "DERA_ERR_DEVICE: pointer is not device memory of the current device";
+    case DERA_ERR_TIMEOUT: return "DERA_ERR_TIMEOUT: a bounded wait expired inside a kernel";
+    case DERA_ERR_CUDA: return "DERA_ERR_CUDA: a CUDA call failed";
+  }
+  return "DERA_ERR_UNKNOWN";
+}
+
+int dera_relpos_abi_version(void) { return DERA_RELPOS_ABI_VERSION; }
+
+dera_status dera_relpos_project(const void* q, const void* rel_pos_h, const void* rel_pos_w, void* rel_h,
+                                void* rel_w, int BH, int H, int W, int head_dim, dera_dtype in_dtype,
+                                dera_dtype bias_dtype, void* stream) {
+  DERA_TRY(check_shape(BH, H, W, head_dim));
+  if (!is16(in_dtype) || !is_float(bias_dtype)) return DERA_ERR_DTYPE;
+  DERA_TRY(check_host({q, rel_pos_h, rel_pos_w, rel_h, rel_w}));
+  if (BH == 0) return DERA_OK;
+  int dev = 0;
+  DERA_TRY(current_device(&dev));
+  for (const void* p : {q, rel_pos_h, rel_pos_w, static_cast<const void*>(rel_h), static_cast<const void*>(rel_w)})
+    DERA_TRY(check_ptr(p, dev));
+  const int N = H * W;
+  CUtensorMap mq, mh, mw;
+  if (!map_rows(&mq, q, in_dtype, BH, N) || !map_table(&mh, rel_pos_h, in_dtype, H) ||
+      !map_table(&mw, rel_pos_w, in_dtype, W))
+    return DERA_ERR_CUDA;
+  ProjArgs args;
+  args.rel_h = rel_h;
+  args.rel_w = rel_w;
+  args.status = status_ptr(dev);
+  if (!args.status) return DERA_ERR_CUDA;
+  args.BH = BH;
+  args.H = H;
+  args.W = W;
+  args.N = N;
+  args.bias_fmt = fmt_of(bias_dtype);
+  const cudaError_t e = launch_project(mq, mh, mw, args, fmt_of(in_dtype), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DERA_OK : DERA_ERR_CUDA;
+}
+
+dera_status dera_relpos_attention(const void* q, const void* k, const void* v, const void* rel_h,
+                                  const void* rel_w, void* out, int BH, int H, int W, int head_dim, float scale,
+                                  dera_dtype in_dtype, dera_dtype bias_dtype, dera_dtype out_dtype,
+                                  void* stream) {
+  DERA_TRY(check_shape(BH, H, W, head_dim));
+  if (!is16(in_dtype) || !is_float(bias_dtype) || !(out_dtype == DERA_F32 || out_dtype == in_dtype))
+    return DERA_ERR_DTYPE;
+  DERA_TRY(check_host({q, k, v, rel_h, rel_w, out}));
+  if (BH == 0) return DERA_OK;
+  int dev = 0;
+  DERA_TRY(current_device(&dev));
+  for (const void* p : {q, k, v, rel_h, rel_w, static_cast<const void*>(out)}) DERA_TRY(check_ptr(p, dev));
+  return run_attention(q, k, v, rel_h, rel_w, out, BH, H, W, scale, in_dtype, bias_dtype, out_dtype, false,
+                       stream);
+}
+
+dera_status dera_relpos_fused(const void* q, const void* k, const void* v, const void* rel_pos_h,
+                              const void* rel_pos_w, void* out, int BH, int H, int W, int head_dim, float scale,
+                              dera_dtype in_dtype, dera_dtype out_dtype, void* stream) {
+  DERA_TRY(check_shape(BH, H, W, head_dim));
+  if (!is16(in_dtype) || !(out_dtype == DERA_F32 || out_dtype == in_dtype)) return DERA_ERR_DTYPE;
+  DERA_TRY(check_host({q, k, v, rel_pos_h, rel_pos_w, out}));
+  if (BH == 0) return DERA_OK;
+  int dev = 0;
+  DERA_TRY(current_device(&dev));
+  for (const void* p : {q, k, v, rel_pos_h, rel_pos_w, static_cast<const void*>(out)})
+    DERA_TRY(check_ptr(p, dev));
+  return run_attention(q, k, v, rel_pos_h, rel_pos_w, out, BH, H, W, scale, in_dtype, in_dtype, out_dtype, true,
+                       stream);
+}
+
+dera_status dera_relpos_device_status(int* status, int reset) {
+  if (!status) return DERA_ERR_NULL;
+  if (cudaDeviceSynchronize() != cudaSuccess) return DERA_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(status, g_status_word, sizeof(int)) != cudaSuccess) return DERA_ERR_CUDA;
+  if (reset) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int)) != cudaSuccess) return DERA_ERR_CUDA;
+  }
+  return DERA_OK;
+}
+
+dera_status dera_relpos_selftest_wait_timeout(long long budget_cycles, void* stream) {
+  int dev = 0;
+  DERA_TRY(current_device(&dev));
+  int* st = status_ptr(dev);
+  if (!st) return DERA_ERR_CUDA;
+  if (budget_cycles < 1000) budget_cycles = 1000;
+  if (budget_cycles > 4000000000LL) budget_cycles = 4000000000LL;
+  return launch_wait_selftest(st, budget_cycles, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? DERA_OK
+             : DERA_ERR_CUDA;
+}
+
+}  // extern "C"

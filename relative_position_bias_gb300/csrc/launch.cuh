@@ -1,0 +1,23 @@
+// Host-side launchers of the kernel templates; each padded width WP is
+// instantiated in its own translation unit so the build compiles in parallel.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace dera {
+
+struct AttnMaps {
+  CUtensorMap q, k, v, th, tw;
+};
+
+template <int WP>
+cudaError_t launch_attention(const AttnMaps& maps, const AttnArgs& args, bool fused, cudaStream_t stream);
+
+cudaError_t launch_project(const CUtensorMap& q, const CUtensorMap& th, const CUtensorMap& tw,
+                           const ProjArgs& args, int in_fmt, cudaStream_t stream);
+
+cudaError_t launch_wait_selftest(int* status, long long budget, cudaStream_t stream);
+
+}  // namespace dera

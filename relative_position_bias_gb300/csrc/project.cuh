@@ -1,0 +1,132 @@
+// Decomposed rel-pos projection (vLLM PR #55629 page, section 关键源码片段:
+// add_decomposed_rel_pos, squeezed to the compact [.., HW, H] / [.., HW, W]
+// form of section 实现拆解 item 2):
+//   rel_h[b, n, kh] = q[b, n] . rel_pos_h[qh - kh + H - 1]
+//   rel_w[b, n, kw] = q[b, n] . rel_pos_w[qw - kw + W - 1]
+//
+// One CTA per 128-token tile of one head.  The tile's products with every
+// table row, G = Q [T_h ; T_w]^T (128 x 256, fp32), come from one tcgen05.mma
+// of N = 256 into TMEM; each thread then skews its row through shared memory
+// (a per-row shift, see skew_row_to_smem), and the CTA writes the tile's
+// rel_h rows and rel_w rows, which are contiguous in global memory, with
+// coalesced stores.
+#pragma once
+#include "common.cuh"
+
+namespace dera {
+
+constexpr int kProjThreads = 128;
+
+struct ProjSmem {
+  static constexpr int kQ = 0;                       // 16 KB
+  static constexpr int kTables = kTileBytes;         // T_h rows 0..127, T_w rows 128..255 (32 KB)
+  static constexpr int kStage = kTables + 2 * kTileBytes;
+  static constexpr int kStride = 65;                 // floats per staged row (>= 64 + 1)
+  static constexpr int kStageBytes = kBlockM * kStride * 4;
+  static constexpr int kBars = kStage + kStageBytes;
+  static constexpr int kMisc = kBars + 16;
+  static constexpr int kTotal = kMisc + 16;
+  static constexpr int kAlloc = kTotal + 1024;
+};
+
+__device__ __forceinline__ void store_elem(void* p, size_t i, float x, int fmt) {
+  if (fmt == kF32) {
+    reinterpret_cast<float*>(p)[i] = x;
+  } else if (fmt == kBF16) {
+    reinterpret_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(x);
+  } else {
+    reinterpret_cast<__half*>(p)[i] = __float2half_rn(x);
+  }
+}
+
+__global__ void __launch_bounds__(kProjThreads, 1)
+    relpos_project_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_th,
+                          const __grid_constant__ CUtensorMap tm_tw, const ProjArgs args, int in_fmt,
+                          int n_qtiles) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_u + 1023u) & ~1023u) - raw_u);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ProjSmem::kBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + ProjSmem::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + ProjSmem::kMisc + 4);
+  float* stage = reinterpret_cast<float*>(smem + ProjSmem::kStage);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = blockIdx.x % n_qtiles;
+  const int bh = blockIdx.x / n_qtiles;
+  const int H = args.H, W = args.W, N = args.N;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(&bars[0], 3 * kTileBytes);
+    tma_load_3d(smem + ProjSmem::kQ, &tm_q, &bars[0], 0, qt * kBlockM, bh);
+    tma_load_2d(smem + ProjSmem::kTables, &tm_th, &bars[0], 0, 0);
+    tma_load_2d(smem + ProjSmem::kTables + kTileBytes, &tm_tw, &bars[0], 0, 0);
+  }
+  bool ok = mbar_wait(&bars[0], 0, abort_flag, args.status);
+  if (threadIdx.x == 0) {
+    if (ok) {
+      tc_fence_after();
+      const uint32_t fmt = static_cast<uint32_t>(in_fmt);
+      const uint32_t id = idesc_f16(kBlockM, 256, fmt, fmt, 0, 0);
+      #pragma unroll
+      for (int k = 0; k < 4; ++k)
+        umma_ss(tbase, sdesc_sw128(smem_u32(smem + ProjSmem::kQ) + 32 * k, 16, 1024),
+                sdesc_sw128(smem_u32(smem + ProjSmem::kTables) + 32 * k, 16, 1024), id, k > 0);
+    }
+    umma_commit(&bars[1]);
+  }
+  ok = mbar_wait(&bars[1], 0, abort_flag, args.status) && ok;
+  ok = __syncthreads_and(ok);
+  tc_fence_after();
+
+  const int r = warp * 32 + lane;
+  const int n0 = qt * kBlockM;
+  const int n = n0 + r;
+  const bool row_valid = n < N;
+  const int qh = row_valid ? n / W : 0;
+  const int qw = row_valid ? n - qh * W : 0;
+  const int rows = min(kBlockM, N - n0);
+  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+
+  if (ok) {
+    // rel_h rows of the tile, then rel_w rows (both contiguous in global memory)
+    for (int part = 0; part < 2; ++part) {
+      const int len = part == 0 ? H : W;
+      skew_row_to_smem(tbase + lane_off + 128 * part, part == 0 ? qh : qw, len,
+                       stage + r * ProjSmem::kStride, 1.0f);
+      __syncthreads();
+      void* dst = part == 0 ? args.rel_h : args.rel_w;
+      const size_t base = (static_cast<size_t>(bh) * N + n0) * len;
+      const int total = rows * len;
+      for (int e = threadIdx.x; e < total; e += kProjThreads) {
+        const int rr = e / len, cc = e - rr * len;
+        store_elem(dst, base + e, stage[rr * ProjSmem::kStride + cc], args.bias_fmt);
+      }
+      __syncthreads();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 256);
+  }
+}
+
+}  // namespace dera

@@ -1,0 +1,303 @@
+"""GPU parity of the CUDA path against the CPU float64 oracle.
+
+Inputs come from the seeded generator (relative_position_bias_gb300.inputs)
+and are rounded to the workload dtype once; the same bytes go to the GPU and,
+widened exactly to float64, to the oracle.
+
+Tolerances (from the target stated for this method: max-abs 4e-3 and
+relative L2 1e-2 against the float64 oracle):
+  * fp32 output mode: |out - oracle| <= 4e-3 everywhere, rel-L2 <= 1e-2.
+  * 16-bit output: the kernel's only extra step is the final round-to-nearest,
+    which alone can move a value by half an ulp of the output dtype (for bf16
+    and |out| in [2, 4) that is 7.8e-3, above 4e-3).  So a 16-bit output must
+    be bit-equal to the rounded fp32-mode output of the same call, and within
+    4e-3 + ulp/2 of the oracle, and rel-L2 <= 1e-2.
+  * projection: fp32 accumulation of 64 exact products; |err| <= 2e-4 * (1 + |x|).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import relative_position_bias_gb300 as rpb
+from relative_position_bias_gb300 import build as rbuild
+from relative_position_bias_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+ABS_TOL = 4e-3
+RL2_TOL = 1e-2
+MANT_BITS = {torch.bfloat16: 7, torch.float16: 10}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    rbuild.build()
+    rpb.load_library()
+    yield
+    assert rpb.device_status() == 0, "a kernel hit its bounded-wait budget"
+
+
+def _dev(x: dict) -> dict:
+    return {k: t.cuda() for k, t in x.items()}
+
+
+def _f64(x: dict) -> dict:
+    return {k: I.to_f64(t) for k, t in x.items()}
+
+
+def half_ulp(x: np.ndarray, dtype: torch.dtype) -> np.ndarray:
+    ax = np.maximum(np.abs(x), 2.0 ** -14)
+    return 0.5 * 2.0 ** (np.floor(np.log2(ax)) - MANT_BITS[dtype])
+
+
+def check_out(got32: torch.Tensor, want: np.ndarray, got16: torch.Tensor | None = None, what: str = ""):
+    g = got32.double().cpu().numpy()
+    assert np.isfinite(g).all(), f"{what}: non-finite output"
+    err = np.abs(g - want)
+    rl2 = np.linalg.norm(g - want) / max(np.linalg.norm(want), 1e-300)
+    assert err.max() <= ABS_TOL, f"{what}: max-abs {err.max():.3e}"
+    assert rl2 <= RL2_TOL, f"{what}: rel-L2 {rl2:.3e}"
+    if got16 is not None:
+        rounded = got32.to(got16.dtype)
+        assert torch.equal(got16.view(torch.int16), rounded.view(torch.int16)), f"{what}: 16-bit != RN(fp32 mode)"
+        g16 = got16.double().cpu().numpy()
+        assert (np.abs(g16 - want) <= ABS_TOL + half_ulp(want, got16.dtype)).all(), f"{what}: 16-bit bound"
+        assert np.linalg.norm(g16 - want) / np.linalg.norm(want) <= RL2_TOL
+    return float(err.max()), float(rl2)
+
+
+def sample_rows(w: I.Workload, n_heads: int = 4, n_rows: int = 96, seed: int = 0):
+    """Heads and token rows for sampled checks: first/last tile rows, ragged tail and random rows."""
+    r = np.random.default_rng(seed)
+    heads = sorted({0, w.BH - 1, *r.choice(w.BH, size=min(n_heads, w.BH), replace=False).tolist()})
+    fixed = [0, 1, 127, 128, 255, 256, w.N - 129, w.N - 128, w.N - 2, w.N - 1]
+    rows = sorted({x for x in fixed if 0 <= x < w.N} | set(r.choice(w.N, size=n_rows, replace=False).tolist()))
+    return heads, np.array(rows)
+
+
+# --------------------------------------------------------------------------- projection
+@pytest.mark.parametrize("name", list(I.WORKLOADS))
+def test_project_parity(name):
+    w = I.WORKLOADS[name]
+    x = I.make_inputs(w)
+    d = _dev(x)
+    rh, rw = rpb.project(d["q"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W)
+    torch.cuda.synchronize()
+    f = _f64(x)
+    want_h, want_w = oracle.project(f["q"], f["rel_pos_h"], f["rel_pos_w"], w.H, w.W)
+    for got, want in ((rh, want_h), (rw, want_w)):
+        g = got.double().cpu().numpy()
+        assert (np.abs(g - want) <= 2e-4 * (1 + np.abs(want))).all(), np.abs(g - want).max()
+
+
+@pytest.mark.parametrize("bias_dtype", [torch.bfloat16, torch.float16])
+def test_project_16bit_bias(bias_dtype):
+    w = I.WORKLOADS["global64"].with_grid(24, 40, B=1, heads=3)
+    x = I.make_inputs(w, seed=3)
+    d = _dev(x)
+    rh32, rw32 = rpb.project(d["q"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W)
+    rh, rw = rpb.project(d["q"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W, bias_dtype=bias_dtype)
+    torch.cuda.synchronize()
+    assert torch.equal(rh, rh32.to(bias_dtype)) and torch.equal(rw, rw32.to(bias_dtype))
+
+
+# --------------------------------------------------------------------------- full workloads
+def _oracle_full_or_rows(w, f, entry, rel=None):
+    """Whole oracle output when it is cheap, else (heads, rows, values) sampled."""
+    if w.BH * w.N * w.N <= 12 * 4096 * 4096:
+        if entry == "fused":
+            return None, None, oracle.fused(f["q"], f["k"], f["v"], f["rel_pos_h"], f["rel_pos_w"], w.H, w.W, w.scale)
+        return None, None, oracle.attention(f["q"], f["k"], f["v"], rel[0], rel[1], w.H, w.W, w.scale)
+    heads, rows = sample_rows(w)
+    vals = []
+    for b in heads:
+        if entry == "fused":
+            vals.append(oracle.fused_rows(f["q"], f["k"], f["v"], f["rel_pos_h"], f["rel_pos_w"], b, rows, w.H, w.W,
+                                          w.scale))
+        else:
+            vals.append(oracle.attention_rows(f["q"], f["k"], f["v"], rel[0][b][rows], rel[1][b][rows], b, rows,
+                                              w.H, w.W, w.scale))
+    return heads, rows, np.stack(vals)
+
+
+def _select(t: torch.Tensor, heads, rows):
+    if heads is None:
+        return t
+    return t[heads][:, rows]
+
+
+@pytest.mark.parametrize("name", list(I.WORKLOADS))
+def test_fused_parity(name):
+    w = I.WORKLOADS[name]
+    x = I.make_inputs(w)
+    d = _dev(x)
+    args = (d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W, w.scale)
+    o32 = rpb.fused(*args, out_dtype=torch.float32)
+    o16 = rpb.fused(*args)
+    torch.cuda.synchronize()
+    heads, rows, want = _oracle_full_or_rows(w, _f64(x), "fused")
+    check_out(_select(o32, heads, rows), want, _select(o16, heads, rows), what=f"fused {name}")
+
+
+@pytest.mark.parametrize("name", list(I.WORKLOADS))
+def test_attention_parity_f32_bias(name):
+    """Compact-bias entry fed the oracle's projection (rounded to fp32); the
+    oracle consumes exactly those fp32 values."""
+    w = I.WORKLOADS[name]
+    x = I.make_inputs(w)
+    f = _f64(x)
+    rh, rw = oracle.project(f["q"], f["rel_pos_h"], f["rel_pos_w"], w.H, w.W)
+    rh32, rw32 = torch.from_numpy(rh).float(), torch.from_numpy(rw).float()
+    d = _dev(x)
+    o32 = rpb.attention(d["q"], d["k"], d["v"], rh32.cuda(), rw32.cuda(), w.H, w.W, w.scale,
+                        out_dtype=torch.float32)
+    o16 = rpb.attention(d["q"], d["k"], d["v"], rh32.cuda(), rw32.cuda(), w.H, w.W, w.scale)
+    torch.cuda.synchronize()
+    rel = (rh32.double().numpy(), rw32.double().numpy())
+    heads, rows, want = _oracle_full_or_rows(w, f, "attention", rel)
+    check_out(_select(o32, heads, rows), want, _select(o16, heads, rows), what=f"attention {name}")
+
+
+@pytest.mark.parametrize("bias_dtype", [torch.bfloat16, torch.float16])
+def test_attention_16bit_bias(bias_dtype):
+    """A 16-bit compact bias: the oracle consumes the same rounded values."""
+    w = I.WORKLOADS["grid16"].with_grid(24, 24, B=2, heads=3)
+    x = I.make_inputs(w, seed=5)
+    f = _f64(x)
+    rh, rw = oracle.project(f["q"], f["rel_pos_h"], f["rel_pos_w"], w.H, w.W)
+    rh16, rw16 = torch.from_numpy(rh).to(bias_dtype), torch.from_numpy(rw).to(bias_dtype)
+    d = _dev(x)
+    o32 = rpb.attention(d["q"], d["k"], d["v"], rh16.cuda(), rw16.cuda(), w.H, w.W, w.scale, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    want = oracle.attention(f["q"], f["k"], f["v"], rh16.double().numpy(), rw16.double().numpy(), w.H, w.W, w.scale)
+    check_out(o32, want, what="attention 16-bit bias")
+
+
+def test_two_step_matches_oracle():
+    """dera_relpos_project then dera_relpos_attention against the oracle's fused result."""
+    w = I.WORKLOADS["global64"]
+    x = I.make_inputs(w)
+    d = _dev(x)
+    rh, rw = rpb.project(d["q"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W)
+    o32 = rpb.attention(d["q"], d["k"], d["v"], rh, rw, w.H, w.W, w.scale, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    f = _f64(x)
+    want = oracle.fused(f["q"], f["k"], f["v"], f["rel_pos_h"], f["rel_pos_w"], w.H, w.W, w.scale)
+    check_out(o32, want, what="two-step global64")
+
+
+# --------------------------------------------------------------------------- edge grids
+EDGE_GRIDS = [(1, 1), (1, 2), (2, 1), (3, 5), (5, 3), (17, 13), (1, 64), (64, 1), (7, 40), (33, 33), (20, 48),
+              (64, 17), (5, 64), (2, 16), (9, 16), (16, 9), (40, 40), (63, 63), (11, 37), (64, 33)]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("grid", EDGE_GRIDS, ids=lambda g: f"{g[0]}x{g[1]}")
+def test_edge_grids(grid, dtype):
+    H, W = grid
+    base = I.WORKLOADS["ragged40"] if dtype == "f16" else I.WORKLOADS["grid16"]
+    w = base.with_grid(H, W, B=1, heads=3)
+    x = I.make_inputs(w, seed=H * 97 + W)
+    d = _dev(x)
+    f = _f64(x)
+    o32 = rpb.fused(d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], H, W, w.scale, out_dtype=torch.float32)
+    rh, rw = rpb.project(d["q"], d["rel_pos_h"], d["rel_pos_w"], H, W)
+    a32 = rpb.attention(d["q"], d["k"], d["v"], rh, rw, H, W, w.scale, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    want = oracle.fused(f["q"], f["k"], f["v"], f["rel_pos_h"], f["rel_pos_w"], H, W, w.scale)
+    check_out(o32, want, what=f"fused {H}x{W} {dtype}")
+    check_out(a32, want, what=f"two-step {H}x{W} {dtype}")
+
+
+def test_empty_batch_is_a_noop():
+    w = I.WORKLOADS["grid16"]
+    q = torch.empty(0, w.N, 64, dtype=torch.bfloat16, device="cuda")
+    t = torch.zeros(2 * w.H - 1, 64, dtype=torch.bfloat16, device="cuda")
+    out = rpb.fused(q, q, q, t, t, w.H, w.W, w.scale)
+    assert out.shape == (0, w.N, 64)
+
+
+# --------------------------------------------------------------------------- properties of the call
+def test_deterministic_and_graph_capturable():
+    w = I.WORKLOADS["global64"]
+    d = _dev(I.make_inputs(w))
+    args = (d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W, w.scale)
+    a = rpb.fused(*args)
+    b = rpb.fused(*args)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    out = torch.empty_like(a)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        rpb.fused(*args, out=out)          # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    out.zero_()
+    with torch.cuda.graph(g):
+        rpb.fused(*args, out=out)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, a)
+
+
+def test_no_device_allocation_in_calls():
+    w = I.WORKLOADS["global64"]
+    x = I.make_inputs(w)
+    d = _dev(x)
+    out = torch.empty(w.BH, w.N, 64, dtype=torch.bfloat16, device="cuda")
+    rh = torch.empty(w.BH, w.N, w.H, device="cuda")
+    rw = torch.empty(w.BH, w.N, w.W, device="cuda")
+    args = (d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W, w.scale)
+    rpb.fused(*args, out=out)
+    rpb.project(d["q"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W, rel_h=rh, rel_w=rw)
+    rpb.attention(d["q"], d["k"], d["v"], rh, rw, w.H, w.W, w.scale, out=out)
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats()
+    free0, _ = torch.cuda.mem_get_info()
+    alloc0 = torch.cuda.memory_allocated()
+    for _ in range(3):
+        rpb.fused(*args, out=out)
+        rpb.project(d["q"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W, rel_h=rh, rel_w=rw)
+        rpb.attention(d["q"], d["k"], d["v"], rh, rw, w.H, w.W, w.scale, out=out)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert torch.cuda.max_memory_allocated() == alloc0
+    assert free1 == free0
+
+
+def test_rejects_host_and_misaligned_pointers():
+    w = I.WORKLOADS["grid16"]
+    x = I.make_inputs(w)
+    d = _dev(x)
+    with pytest.raises(rpb.DeraError) as ei:
+        rpb.fused(x["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W)
+    assert ei.value.status == 6
+    pinned = x["v"].pin_memory()
+    with pytest.raises(rpb.DeraError) as ei:
+        rpb.fused(d["q"], d["k"], pinned, d["rel_pos_h"], d["rel_pos_w"], w.H, w.W)
+    assert ei.value.status == 6
+    buf = torch.empty(w.BH * w.N * 64 + 8, dtype=torch.bfloat16, device="cuda")
+    qm = buf[1:1 + w.BH * w.N * 64].view(w.BH, w.N, 64)      # 2-byte offset
+    with pytest.raises(rpb.DeraError) as ei:
+        rpb.fused(qm, d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W)
+    assert ei.value.status == 5
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    assert rpb.device_status(reset=True) == 0
+    rpb.selftest_wait_timeout(budget_cycles=2_000_000)
+    assert rpb.device_status(reset=True) == 7
+    assert rpb.device_status(reset=False) == 0
+    # the context is still usable
+    w = I.WORKLOADS["grid16"]
+    x = I.make_inputs(w)
+    d = _dev(x)
+    out = rpb.fused(d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W, w.scale, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    f = _f64(x)
+    check_out(out, oracle.fused(f["q"], f["k"], f["v"], f["rel_pos_h"], f["rel_pos_w"], w.H, w.W, w.scale))
