@@ -34,7 +34,8 @@
  *       rel_h        : [BH, N, H]            rel_w     : [BH, N, W]
  *   - head_dim must be 64.  q, k, v, tables share one dtype: DERA_F16 or
  *     DERA_BF16.  1 <= H, W <= 64.  BH >= 0 (BH == 0 is a no-op).
- *   - Every pointer must be 16-byte aligned (TMA operands).
+ *   - Every pointer must be 16-byte aligned (TMA operands).  With BH == 0
+ *     the call returns DERA_OK before looking at any pointer.
  *   - Argument errors are detected on the host before anything is enqueued
  *     and returned as a status; nothing falls back to another backend.
  *   - DERA_ERR_CUDA: a CUDA call made by the library failed (launch error,

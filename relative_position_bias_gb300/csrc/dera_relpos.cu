@@ -244,8 +244,8 @@ dera_status dera_relpos_project(const void* q, const void* rel_pos_h, const void
                                 dera_dtype bias_dtype, void* stream) {
   DERA_TRY(check_shape(BH, H, W, head_dim));
   if (!is16(in_dtype) || !is_float(bias_dtype)) return DERA_ERR_DTYPE;
+  if (BH == 0) return DERA_OK;  // empty batch: nothing to read or write
   DERA_TRY(check_host({q, rel_pos_h, rel_pos_w, rel_h, rel_w}));
-  if (BH == 0) return DERA_OK;
   int dev = 0;
   DERA_TRY(current_device(&dev));
   for (const void* p : {q, rel_pos_h, rel_pos_w, static_cast<const void*>(rel_h), static_cast<const void*>(rel_w)})
@@ -276,8 +276,8 @@ dera_status dera_relpos_attention(const void* q, const void* k, const void* v, c
   DERA_TRY(check_shape(BH, H, W, head_dim));
   if (!is16(in_dtype) || !is_float(bias_dtype) || !(out_dtype == DERA_F32 || out_dtype == in_dtype))
     return DERA_ERR_DTYPE;
+  if (BH == 0) return DERA_OK;  // empty batch: nothing to read or write
   DERA_TRY(check_host({q, k, v, rel_h, rel_w, out}));
-  if (BH == 0) return DERA_OK;
   int dev = 0;
   DERA_TRY(current_device(&dev));
   for (const void* p : {q, k, v, rel_h, rel_w, static_cast<const void*>(out)}) DERA_TRY(check_ptr(p, dev));
@@ -290,8 +290,8 @@ dera_status dera_relpos_fused(const void* q, const void* k, const void* v, const
                               dera_dtype in_dtype, dera_dtype out_dtype, void* stream) {
   DERA_TRY(check_shape(BH, H, W, head_dim));
   if (!is16(in_dtype) || !(out_dtype == DERA_F32 || out_dtype == in_dtype)) return DERA_ERR_DTYPE;
+  if (BH == 0) return DERA_OK;  // empty batch: nothing to read or write
   DERA_TRY(check_host({q, k, v, rel_pos_h, rel_pos_w, out}));
-  if (BH == 0) return DERA_OK;
   int dev = 0;
   DERA_TRY(current_device(&dev));
   for (const void* p : {q, k, v, rel_pos_h, rel_pos_w, static_cast<const void*>(out)})

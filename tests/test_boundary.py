@@ -76,6 +76,7 @@ def test_host_validation(lib, call):
         ptrs[i] = FAKE_MISALIGNED
         assert call(lib, ptrs=tuple(ptrs)) == 5       # alignment
     assert call(lib, BH=0) == 0                       # empty batch: no work, no CUDA call
+    assert call(lib, BH=0, ptrs=(None,) * n) == 0     # ... and no pointer is looked at
 
 
 def test_dtype_rules(lib):
