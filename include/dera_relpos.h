@@ -47,15 +47,18 @@
  *     Its output is then undefined.
  *   - All entry points are stream-ordered and allocation-free, so they can be
  *     captured in a CUDA graph.
+ *   - DERA_ERR_ALIGN also covers a workspace that is not 256-byte aligned.
  */
 #ifndef DERA_RELPOS_H
 #define DERA_RELPOS_H
+
+#include <stddef.h>
 
 #ifdef __cplusplus
 extern "C" {
 #endif
 
-#define DERA_RELPOS_ABI_VERSION 1
+#define DERA_RELPOS_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define DERA_API __attribute__((visibility("default")))
@@ -99,6 +102,7 @@ DERA_API dera_status dera_relpos_project(const void* q, const void* rel_pos_h, c
  * in:  q, k, v [BH,N,64] in_dtype (DERA_F16 | DERA_BF16);
  *      rel_h [BH,N,H], rel_w [BH,N,W] in bias_dtype (DERA_F32 | DERA_BF16 | DERA_F16).
  * out: out [BH,N,64] in out_dtype (DERA_F32, or in_dtype).
+ * workspace / workspace_bytes: optional scratch, see dera_relpos_workspace_size.
  * Softmax runs in base 2 with fp32 accumulation; P is rounded to fp16 for the
  * P.V product (for bf16 inputs, V tiles are converted to fp16 on chip, so
  * |v| must stay below 65504).
@@ -106,7 +110,7 @@ DERA_API dera_status dera_relpos_project(const void* q, const void* rel_pos_h, c
 DERA_API dera_status dera_relpos_attention(const void* q, const void* k, const void* v, const void* rel_h,
                                   const void* rel_w, void* out, int BH, int H, int W, int head_dim, float scale,
                                   dera_dtype in_dtype, dera_dtype bias_dtype, dera_dtype out_dtype,
-                                  void* stream);
+                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * A1..A7 fused — projection computed inside the attention kernel (tensor-core
@@ -114,10 +118,31 @@ DERA_API dera_status dera_relpos_attention(const void* q, const void* k, const v
  * nor the compact rel_h / rel_w ever reaches global memory.
  * in:  q, k, v [BH,N,64], rel_pos_h [2H-1,64], rel_pos_w [2W-1,64], in_dtype.
  * out: out [BH,N,64] in out_dtype (DERA_F32, or in_dtype).
+ * workspace / workspace_bytes: optional scratch, see dera_relpos_workspace_size.
  */
 DERA_API dera_status dera_relpos_fused(const void* q, const void* k, const void* v, const void* rel_pos_h,
                               const void* rel_pos_w, void* out, int BH, int H, int W, int head_dim, float scale,
-                              dera_dtype in_dtype, dera_dtype out_dtype, void* stream);
+                              dera_dtype in_dtype, dera_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/*
+ * Scratch needed by dera_relpos_attention / dera_relpos_fused for a problem
+ * size on the current device, written to *bytes (host pointer); 0 when the
+ * work splits evenly over the device (no scratch used).
+ *
+ * Scheduling (no counterpart on the pages, which give no kernel schedule):
+ * the work unit is a pair of 128-row query tiles of one head.  When the
+ * number of units is not a whole number of waves of one CTA per SM, the
+ * kernel runs one persistent CTA per SM over equal shares of the
+ * (unit, key tile) iteration space and cuts some units between two CTAs; the
+ * partial results (unnormalised O, row max, row sum, fp32) and one arrival
+ * counter per unit live in the caller's `workspace`.  A NULL workspace, or one
+ * smaller than this size, selects one CTA per unit instead (same result, no
+ * scratch, less even load).  The workspace must be device memory, 256-byte
+ * aligned, owned by the caller, and not used by another call in flight: the
+ * entry point clears the counters with cudaMemsetAsync on `stream` first.
+ */
+DERA_API dera_status dera_relpos_workspace_size(int BH, int H, int W, int head_dim, size_t* bytes);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 DERA_API const char* dera_status_string(dera_status status);
@@ -140,7 +165,7 @@ DERA_API dera_status dera_relpos_device_status(int* status, int reset);
  */
 DERA_API dera_status dera_relpos_selftest_wait_timeout(long long budget_cycles, void* stream);
 
-/* Compile-time ABI version of the loaded library (DERA_RELPOS_ABI_VERSION). */
+/* ABI version of the loaded library (DERA_RELPOS_ABI_VERSION; 2 added the workspace arguments). */
 DERA_API int dera_relpos_abi_version(void);
 
 #ifdef __cplusplus

@@ -6,7 +6,7 @@ thin Python binding.  Entry points: :func:`project`, :func:`attention`,
 :func:`fused`.
 """
 from .api import (DERA_BF16, DERA_F16, DERA_F32, DeraError, attention, declared_entry_points, device_status, fused,
-                  load_library, project, selftest_wait_timeout)
+                  load_library, project, selftest_wait_timeout, workspace_size)
 
 __all__ = ["DERA_BF16", "DERA_F16", "DERA_F32", "DeraError", "attention", "declared_entry_points", "device_status",
-           "fused", "load_library", "project", "selftest_wait_timeout"]
+           "fused", "load_library", "project", "selftest_wait_timeout", "workspace_size"]

@@ -27,6 +27,7 @@ STATUS_NAMES = {0: "DERA_OK", 1: "DERA_ERR_NULL", 2: "DERA_ERR_SHAPE", 3: "DERA_
 
 _lib = None
 _lock = threading.Lock()
+_workspaces: dict = {}    # device index -> uint8 tensor reused by every call on that device
 
 
 class DeraError(RuntimeError):
@@ -48,10 +49,13 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         lib.dera_relpos_project.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
         lib.dera_relpos_project.restype = i
-        lib.dera_relpos_attention.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, i, vp]
+        sz = ctypes.c_size_t
+        lib.dera_relpos_attention.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, i, vp, sz, vp]
         lib.dera_relpos_attention.restype = i
-        lib.dera_relpos_fused.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
+        lib.dera_relpos_fused.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, sz, vp]
         lib.dera_relpos_fused.restype = i
+        lib.dera_relpos_workspace_size.argtypes = [i, i, i, i, ctypes.POINTER(sz)]
+        lib.dera_relpos_workspace_size.restype = i
         lib.dera_status_string.argtypes = [i]
         lib.dera_status_string.restype = ctypes.c_char_p
         lib.dera_relpos_device_status.argtypes = [ctypes.POINTER(i), i]
@@ -96,6 +100,31 @@ def _stream(device: torch.device, stream) -> int | None:
     return torch.cuda.current_stream(device).cuda_stream
 
 
+def workspace_size(BH: int, H: int, W: int, head_dim: int = 64) -> int:
+    """Scratch bytes the attention entries use for this size on the current device (0 if none)."""
+    n = ctypes.c_size_t(0)
+    _check(load_library().dera_relpos_workspace_size(BH, H, W, head_dim, ctypes.byref(n)))
+    return n.value
+
+
+def _workspace(device: torch.device, BH: int, H: int, W: int, d: int, workspace):
+    """(pointer, bytes) of the scratch for one call: the caller's tensor, none, or a cached per-device buffer."""
+    if workspace is False or device.type != "cuda" or BH == 0:
+        return None, 0
+    if isinstance(workspace, torch.Tensor):
+        return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    with torch.cuda.device(device):
+        need = workspace_size(BH, H, W, d)
+    if need == 0:
+        return None, 0
+    idx = device.index if device.index is not None else torch.cuda.current_device()
+    buf = _workspaces.get(idx)
+    if buf is None or buf.numel() < need:
+        buf = torch.empty(need, dtype=torch.uint8, device=device)
+        _workspaces[idx] = buf
+    return buf.data_ptr(), buf.numel()
+
+
 def _expect(t: torch.Tensor, shape: tuple, name: str) -> None:
     if tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
@@ -127,8 +156,11 @@ def project(q: torch.Tensor, rel_pos_h: torch.Tensor, rel_pos_w: torch.Tensor, H
 
 def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, rel_h: torch.Tensor, rel_w: torch.Tensor,
               H: int, W: int, scale: float | None = None, out_dtype: torch.dtype | None = None,
-              out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """Attention with a compact bias via ``dera_relpos_attention``."""
+              out: torch.Tensor | None = None, stream=None, workspace=None) -> torch.Tensor:
+    """Attention with a compact bias via ``dera_relpos_attention``.
+
+    ``workspace``: None = a cached per-device scratch buffer (allocated once),
+    False = no scratch (one CTA per unit), or a caller-owned uint8 tensor."""
     BH, N, d = q.shape
     scale = d ** -0.5 if scale is None else scale
     if out is None:
@@ -142,16 +174,17 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, rel_h: torch.Te
     if rel_h.dtype != rel_w.dtype:
         raise TypeError("rel_h and rel_w must share a dtype")
     lib = load_library()
+    ws, ws_bytes = _workspace(q.device, BH, H, W, d, workspace)
     _check(lib.dera_relpos_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(rel_h), _ptr(rel_w), _ptr(out), BH, H, W, d,
-                                     float(scale), _code(q.dtype), _code(rel_h.dtype), _code(out.dtype),
-                                     _stream(q.device, stream)))
+                                     float(scale), _code(q.dtype), _code(rel_h.dtype), _code(out.dtype), ws,
+                                     ws_bytes, _stream(q.device, stream)))
     return out
 
 
 def fused(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, rel_pos_h: torch.Tensor, rel_pos_w: torch.Tensor,
           H: int, W: int, scale: float | None = None, out_dtype: torch.dtype | None = None,
-          out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """Projection + attention in one kernel via ``dera_relpos_fused``."""
+          out: torch.Tensor | None = None, stream=None, workspace=None) -> torch.Tensor:
+    """Projection + attention in one kernel via ``dera_relpos_fused`` (``workspace`` as in :func:`attention`)."""
     BH, N, d = q.shape
     scale = d ** -0.5 if scale is None else scale
     if out is None:
@@ -164,8 +197,10 @@ def fused(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, rel_pos_h: torch.Te
         if t.dtype != q.dtype:
             raise TypeError("q, k, v and the tables must share a dtype")
     lib = load_library()
+    ws, ws_bytes = _workspace(q.device, BH, H, W, d, workspace)
     _check(lib.dera_relpos_fused(_ptr(q), _ptr(k), _ptr(v), _ptr(rel_pos_h), _ptr(rel_pos_w), _ptr(out), BH, H, W,
-                                 d, float(scale), _code(q.dtype), _code(out.dtype), _stream(q.device, stream)))
+                                 d, float(scale), _code(q.dtype), _code(out.dtype), ws, ws_bytes,
+                                 _stream(q.device, stream)))
     return out
 
 

@@ -6,8 +6,16 @@
 // 实现拆解 item 1 and 关键源码片段).  The softmax is online, in base 2, with
 // fp32 statistics (section 风险与影响).
 //
-// One CTA owns a pair of 128-row query tiles of one head and streams the
-// head's keys/values once for both.  Warp roles:
+// Work unit: a pair of 128-row query tiles of one head; both tiles share every
+// K/V tile the CTA streams.  The kernel is persistent: CTA c runs the
+// contiguous range [c*T/G, (c+1)*T/G) of the T = units x key-tiles iteration
+// space (stream-K), so all CTAs get the same number of key tiles whatever the
+// unit count.  A unit cut between CTAs leaves partial results (unnormalised O,
+// row max, row sum) in the caller's workspace; the CTA that finishes a unit
+// last merges them.  With one CTA per unit (no workspace) every segment is a
+// whole unit and nothing is written to the workspace.
+//
+// Warp roles (384 threads):
 //   warp 0      TMA producer: Q pair, [tables,] K/V ring (3 stages)
 //   warp 1      tcgen05.mma issuer (one thread)
 //   warp 2      TMEM allocator; with warp 3, converts bf16 V tiles to fp16
@@ -15,7 +23,7 @@
 //   warps 8-11  softmax / epilogue of query tile 1
 // TMEM (512 columns): S0 [0,128) S1 [128,256) P0 [256,320) P1 [320,384)
 //                     O0 [384,448) O1 [448,512); the fused prologue uses all
-//                     512 columns for G_i = Q_i [T_h ; T_w]^T before the loop.
+//                     512 columns for G_i = Q_i [T_h ; T_w]^T before each segment.
 #pragma once
 #include "common.cuh"
 
@@ -23,7 +31,7 @@ namespace dera {
 
 constexpr int kStages = 3;
 constexpr int kAttnThreads = 384;
-constexpr float kRescaleTau = 8.0f;   // lazy rescale threshold (log2 units)
+constexpr float kSpecSumLimit = 32768.0f;  // largest accepted row sum of a speculative tile
 constexpr int kBiasStride = 66;       // floats per row of a bias staging area
 
 struct AttnSmem {
@@ -33,8 +41,8 @@ struct AttnSmem {
   static constexpr int kBias = kRing + kStages * kStageBytes;    // 2 x 128 x 66 floats
   static constexpr int kBiasBytes = 2 * kBlockM * kBiasStride * 4;
   static constexpr int kBars = kBias + kBiasBytes;
-  static constexpr int kNumBars = 24;
-  static constexpr int kMisc = kBars + kNumBars * 8;             // tmem slot, abort flag
+  static constexpr int kNumBars = 32;
+  static constexpr int kMisc = kBars + kNumBars * 8;             // tmem slot, abort flag, merge flag
   static constexpr int kTotal = kMisc + 16;
   static constexpr int kAlloc = kTotal + 1024;                   // slack for 1 KB alignment
 };
@@ -43,7 +51,8 @@ static_assert(AttnSmem::kAlloc <= 232448, "shared memory budget");
 // barrier indices
 enum : int {
   kBarQFull = 0,
-  kBarKVFull = 1,                 // + stage
+  kBarQEmpty = 1,
+  kBarKVFull = 2,                     // + stage
   kBarKVEmpty = kBarKVFull + kStages,
   kBarVReady = kBarKVEmpty + kStages,
   kBarSFull = kBarVReady + kStages,   // + tile
@@ -51,10 +60,38 @@ enum : int {
   kBarODone = kBarPFull + 2,
   kBarGFull = kBarODone + 2,
   kBarGFree = kBarGFull + 1,
-  kBarMmaDone = kBarGFree + 1,
+  kBarEpiDone = kBarGFree + 1,
+  kBarStg = kBarEpiDone + 1,          // + tile
+  kBarPartWritten = kBarStg + 2,
+  kBarMergeGo = kBarPartWritten + 1,
+  kBarMmaDone = kBarMergeGo + 1,
   kBarCount = kBarMmaDone + 1
 };
 static_assert(kBarCount <= AttnSmem::kNumBars, "barrier slots");
+
+// Stream-K partition of the (unit, key tile) iteration space.
+struct Schedule {
+  long long T;   // units * n_kv
+  int G;         // CTAs
+  int n_kv;
+  __device__ __forceinline__ long long begin(int c) const { return static_cast<long long>(c) * T / G; }
+  __device__ __forceinline__ int cta_of(long long t) const { return static_cast<int>(((t + 1) * G - 1) / T); }
+};
+
+// One segment of a CTA's range: key tiles [j0, j1) of unit u.
+struct Segment {
+  int u, j0, j1;
+  __device__ __forceinline__ bool full(int n_kv) const { return j0 == 0 && j1 == n_kv; }
+};
+
+__device__ __forceinline__ Segment segment_at(long long it, long long end, int n_kv) {
+  Segment s;
+  s.u = static_cast<int>(it / n_kv);
+  s.j0 = static_cast<int>(it - static_cast<long long>(s.u) * n_kv);
+  const long long left = end - it;
+  s.j1 = static_cast<int>(min(static_cast<long long>(n_kv), s.j0 + left));
+  return s;
+}
 
 // Warp-uniform wait result: tcgen05.ld/st are warp-collective, so a warp
 // either proceeds as a whole or stops as a whole.
@@ -74,7 +111,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   using KT = KeyTile<WP>;
   constexpr int KHT = KT::KHT;
   constexpr int BN = KT::BN;
-  constexpr int kChunks = BN / 16;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u = smem_u32(smem_raw);
@@ -82,14 +118,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + AttnSmem::kBars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + AttnSmem::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + AttnSmem::kMisc + 4);
+  volatile int* merge_flag = reinterpret_cast<volatile int*>(smem + AttnSmem::kMisc + 8);
   int* status = args.status;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.x / args.n_pairs;         // consecutive CTAs share one head's K/V
-  const int qt0 = 2 * (blockIdx.x % args.n_pairs);
   const int n_kv = args.n_kv;
-  const int ring0 = FUSED ? 1 : 0;  // ring slot 0 carries the tables in the fused kernel
+  const Schedule sched{static_cast<long long>(args.n_units) * n_kv, static_cast<int>(gridDim.x), n_kv};
+  const long long it_begin = sched.begin(blockIdx.x);
+  const long long it_end = sched.begin(blockIdx.x + 1);
   const bool convert_v = args.in_fmt == kBF16;
 
   auto sQ = [&](int i) { return smem + AttnSmem::kQ + i * kTileBytes; };
@@ -98,7 +135,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
+    *merge_flag = 0;
     mbar_init(&bars[kBarQFull], 1);
+    mbar_init(&bars[kBarQEmpty], 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars[kBarKVFull + s], 1);
       mbar_init(&bars[kBarKVEmpty + s], 1);
@@ -111,6 +150,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     mbar_init(&bars[kBarGFull], 1);
     mbar_init(&bars[kBarGFree], 2 * kBlockM);
+    mbar_init(&bars[kBarEpiDone], 2 * kBlockM);
+    mbar_init(&bars[kBarStg + 0], kBlockM);
+    mbar_init(&bars[kBarStg + 1], kBlockM);
+    mbar_init(&bars[kBarPartWritten], 2 * kBlockM);
+    mbar_init(&bars[kBarMergeGo], 1);
     mbar_init(&bars[kBarMmaDone], 1);
     fence_mbar_init();
   }
@@ -123,36 +167,49 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
+  if (warp < 4) {
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(&bars[kBarQFull], 2 * kTileBytes);
-      tma_load_3d(sQ(0), &tm_q, &bars[kBarQFull], 0, qt0 * kBlockM, bh);
-      tma_load_3d(sQ(1), &tm_q, &bars[kBarQFull], 0, (qt0 + 1) * kBlockM, bh);
-      int issued = 0;
+      int rg = 0, seg = 0;
       bool ok = true;
-      if (FUSED) {
-        mbar_arrive_expect_tx(&bars[kBarKVFull + 0], 2 * kTileBytes);
-        tma_load_2d(sK(0), &tm_th, &bars[kBarKVFull + 0], 0, 0);
-        tma_load_2d(sV(0), &tm_tw, &bars[kBarKVFull + 0], 0, 0);
-        issued = 1;
-      }
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int r = ring0 + j, s = r % kStages;
-        ok = mbar_wait(&bars[kBarKVEmpty + s], ((r / kStages) & 1) ^ 1, abort_flag, status);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&bars[kBarKVFull + s], 2 * BN * kRowBytes);
-        tma_load_4d(sK(s), &tm_k, &bars[kBarKVFull + s], 0, 0, j * KHT, bh);
-        tma_load_4d(sV(s), &tm_v, &bars[kBarKVFull + s], 0, 0, j * KHT, bh);
-        issued = r + 1;
+      for (long long it = it_begin; it < it_end && ok; ++seg) {
+        const Segment sg = segment_at(it, it_end, n_kv);
+        it += sg.j1 - sg.j0;
+        const int bh = sg.u / args.n_pairs;
+        const int qt0 = 2 * (sg.u - bh * args.n_pairs);
+        if (seg > 0) {
+          ok = mbar_wait(&bars[kBarQEmpty], (seg - 1) & 1, abort_flag, status);
+          if (!ok) break;
+        }
+        mbar_arrive_expect_tx(&bars[kBarQFull], 2 * kTileBytes);
+        tma_load_3d(sQ(0), &tm_q, &bars[kBarQFull], 0, qt0 * kBlockM, bh);
+        tma_load_3d(sQ(1), &tm_q, &bars[kBarQFull], 0, (qt0 + 1) * kBlockM, bh);
+        if (FUSED) {
+          const int s = rg % kStages;
+          ok = mbar_wait(&bars[kBarKVEmpty + s], ((rg / kStages) & 1) ^ 1, abort_flag, status);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&bars[kBarKVFull + s], 2 * kTileBytes);
+          tma_load_2d(sK(s), &tm_th, &bars[kBarKVFull + s], 0, 0);
+          tma_load_2d(sV(s), &tm_tw, &bars[kBarKVFull + s], 0, 0);
+          ++rg;
+        }
+        for (int j = sg.j0; j < sg.j1; ++j, ++rg) {
+          const int s = rg % kStages;
+          ok = mbar_wait(&bars[kBarKVEmpty + s], ((rg / kStages) & 1) ^ 1, abort_flag, status);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&bars[kBarKVFull + s], 2 * BN * kRowBytes);
+          tma_load_4d(sK(s), &tm_k, &bars[kBarKVFull + s], 0, 0, j * KHT, bh);
+          tma_load_4d(sV(s), &tm_v, &bars[kBarKVFull + s], 0, 0, j * KHT, bh);
+        }
       }
       if (!ok) {
         // Let the copies already in flight land before the CTA exits.
-        mbar_wait_budget(&bars[kBarQFull], 0, kWaitBudgetCycles);
-        for (int r = max(0, issued - kStages); r < issued; ++r)
+        if (seg > 0) mbar_wait_budget(&bars[kBarQFull], (seg - 1) & 1, kWaitBudgetCycles);
+        for (int r = max(0, rg - kStages); r < rg; ++r)
           mbar_wait_budget(&bars[kBarKVFull + r % kStages], (r / kStages) & 1, kWaitBudgetCycles);
       }
     }
@@ -163,76 +220,97 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const uint32_t id_qk = idesc_f16(kBlockM, BN, fmt, fmt, 0, 0);
       const uint32_t id_pv = idesc_f16(kBlockM, kHeadDim, kF16, kF16, 0, 1);
       const uint32_t id_g = idesc_f16(kBlockM, 256, fmt, fmt, 0, 0);
+      // Descriptors differ only in their 14-bit start-address field (address / 16),
+      // which stays below 2^14 for any shared-memory address, so offsets are
+      // added to one base descriptor per operand.
+      const uint64_t d_q = sdesc_sw128(smem_u32(sQ(0)), 16, 1024);
+      const uint64_t d_k = sdesc_sw128(smem_u32(sK(0)), 16, 1024);
+      const uint64_t d_v = sdesc_sw128(smem_u32(sV(0)), 16, 1024);
+      constexpr uint32_t kQStep = kTileBytes >> 4, kStageStep = AttnSmem::kStageBytes >> 4;
       auto issue_qk = [&](int i, int s) {
+        const uint64_t a = d_q + i * kQStep, b = d_k + s * kStageStep;
         #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          umma_ss(tbase + 128 * i, sdesc_sw128(smem_u32(sQ(i)) + 32 * k, 16, 1024),
-                  sdesc_sw128(smem_u32(sK(s)) + 32 * k, 16, 1024), id_qk, k > 0);
+        for (int k = 0; k < 4; ++k) umma_ss(tbase + 128 * i, a + 2 * k, b + 2 * k, id_qk, k > 0);
       };
       auto issue_pv = [&](int i, int s, bool acc) {
+        const uint64_t b = d_v + s * kStageStep;
         #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
-          umma_ts(tbase + 384 + 64 * i, tbase + 256 + 64 * i + 8 * k,
-                  sdesc_sw128(smem_u32(sV(s)) + 2048 * k, 16, 1024), id_pv, (acc || k > 0) ? 1u : 0u);
+          umma_ts(tbase + 384 + 64 * i, tbase + 256 + 64 * i + 8 * k, b + 128 * k, id_pv,
+                  (acc || k > 0) ? 1u : 0u);
       };
-      bool ok = mbar_wait(&bars[kBarQFull], 0, abort_flag, status);
-      if (FUSED && ok) {
-        ok = mbar_wait(&bars[kBarKVFull + 0], 0, abort_flag, status);
-        if (ok) {
+      int rg = 0, gi = 0, seg = 0;
+      bool ok = true;
+      for (long long it = it_begin; it < it_end && ok; ++seg) {
+        const Segment sg = segment_at(it, it_end, n_kv);
+        it += sg.j1 - sg.j0;
+        const int len = sg.j1 - sg.j0;
+        ok = mbar_wait(&bars[kBarQFull], seg & 1, abort_flag, status);
+        if (!ok) break;
+        if (FUSED) {
+          if (seg > 0) {
+            ok = mbar_wait(&bars[kBarEpiDone], (seg - 1) & 1, abort_flag, status);
+            if (!ok) break;
+          }
+          const int s = rg % kStages;
+          ok = mbar_wait(&bars[kBarKVFull + s], (rg / kStages) & 1, abort_flag, status);
+          if (!ok) break;
           tc_fence_after();
           for (int i = 0; i < 2; ++i) {
+            const uint64_t a = d_q + i * kQStep, b = d_k + s * kStageStep;
             #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              umma_ss(tbase + 256 * i, sdesc_sw128(smem_u32(sQ(i)) + 32 * k, 16, 1024),
-                      sdesc_sw128(smem_u32(sK(0)) + 32 * k, 16, 1024), id_g, k > 0);
+            for (int k = 0; k < 4; ++k) umma_ss(tbase + 256 * i, a + 2 * k, b + 2 * k, id_g, k > 0);
           }
           umma_commit(&bars[kBarGFull]);
-          umma_commit(&bars[kBarKVEmpty + 0]);
-          ok = mbar_wait(&bars[kBarGFree], 0, abort_flag, status);
-          tc_fence_after();
-        }
-      }
-      if (ok) {
-        const int s0 = ring0 % kStages;
-        ok = mbar_wait(&bars[kBarKVFull + s0], (ring0 / kStages) & 1, abort_flag, status);
-        if (ok) {
-          tc_fence_after();
-          issue_qk(0, s0);
-          umma_commit(&bars[kBarSFull + 0]);
-          issue_qk(1, s0);
-          umma_commit(&bars[kBarSFull + 1]);
-        }
-      }
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int r = ring0 + j, s = r % kStages, ph = (r / kStages) & 1;
-        const int rn = r + 1, sn = rn % kStages, phn = (rn / kStages) & 1;
-        const bool more = j + 1 < n_kv;
-        if (convert_v) {
-          ok = mbar_wait(&bars[kBarVReady + s], ph, abort_flag, status);
-          if (!ok) break;
-        }
-        ok = mbar_wait(&bars[kBarPFull + 0], j & 1, abort_flag, status);
-        if (!ok) break;
-        tc_fence_after();
-        issue_pv(0, s, j > 0);
-        umma_commit(&bars[kBarODone + 0]);
-        if (more) {
-          ok = mbar_wait(&bars[kBarKVFull + sn], phn, abort_flag, status);
+          umma_commit(&bars[kBarKVEmpty + s]);
+          ++rg;
+          ok = mbar_wait(&bars[kBarGFree], seg & 1, abort_flag, status);
           if (!ok) break;
           tc_fence_after();
-          issue_qk(0, sn);
-          umma_commit(&bars[kBarSFull + 0]);
         }
-        ok = mbar_wait(&bars[kBarPFull + 1], j & 1, abort_flag, status);
-        if (!ok) break;
-        tc_fence_after();
-        issue_pv(1, s, j > 0);
-        umma_commit(&bars[kBarODone + 1]);
-        if (more) {
-          issue_qk(1, sn);
+        {
+          const int s = rg % kStages;
+          ok = mbar_wait(&bars[kBarKVFull + s], (rg / kStages) & 1, abort_flag, status);
+          if (!ok) break;
+          tc_fence_after();
+          issue_qk(0, s);
+          umma_commit(&bars[kBarSFull + 0]);
+          issue_qk(1, s);
           umma_commit(&bars[kBarSFull + 1]);
         }
-        umma_commit(&bars[kBarKVEmpty + s]);
+        for (int jj = 0; jj < len && ok; ++jj, ++rg, ++gi) {
+          const int s = rg % kStages, ph = (rg / kStages) & 1;
+          const int sn = (rg + 1) % kStages, phn = ((rg + 1) / kStages) & 1;
+          const bool more = jj + 1 < len;
+          if (convert_v) {
+            ok = mbar_wait(&bars[kBarVReady + s], ph, abort_flag, status);
+            if (!ok) break;
+          }
+          ok = mbar_wait(&bars[kBarPFull + 0], gi & 1, abort_flag, status);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(0, s, jj > 0);
+          umma_commit(&bars[kBarODone + 0]);
+          if (more) {
+            ok = mbar_wait(&bars[kBarKVFull + sn], phn, abort_flag, status);
+            if (!ok) break;
+            tc_fence_after();
+            issue_qk(0, sn);
+            umma_commit(&bars[kBarSFull + 0]);
+          }
+          ok = mbar_wait(&bars[kBarPFull + 1], gi & 1, abort_flag, status);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(1, s, jj > 0);
+          umma_commit(&bars[kBarODone + 1]);
+          if (more) {
+            issue_qk(1, sn);
+            umma_commit(&bars[kBarSFull + 1]);
+          } else {
+            umma_commit(&bars[kBarQEmpty]);  // no more reads of this segment's Q
+          }
+          umma_commit(&bars[kBarKVEmpty + s]);
+        }
       }
       // Drain: every MMA issued above completes before TMEM is released.
       umma_commit(&bars[kBarMmaDone]);
@@ -240,38 +318,42 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else if (warp < 4) {
     // ------------------------------------------------------------ bf16 -> fp16 V conversion
-    // The fused kernel's table slot (ring index 0) is passed through
-    // unconverted so that v_ready completes once per ring index.
+    // The fused kernel's table slots are passed through unconverted, so that
+    // v_ready completes once per ring index.
     if (convert_v) {
       const int ct = threadIdx.x - 64;
-      for (int r = 0; r < ring0 + n_kv; ++r) {
-        const int s = r % kStages;
-        if (!mbar_wait(&bars[kBarKVFull + s], (r / kStages) & 1, abort_flag, status)) break;
-        if (r >= ring0) {
-          uint4* vp = reinterpret_cast<uint4*>(sV(s));
-          for (int idx = ct; idx < BN * kRowBytes / 16; idx += 64) {
-            uint4 w = vp[idx];
-            w.x = bf16x2_to_f16x2(w.x);
-            w.y = bf16x2_to_f16x2(w.y);
-            w.z = bf16x2_to_f16x2(w.z);
-            w.w = bf16x2_to_f16x2(w.w);
-            vp[idx] = w;
+      int rg = 0;
+      bool ok = true;
+      for (long long it = it_begin; it < it_end && ok;) {
+        const Segment sg = segment_at(it, it_end, n_kv);
+        it += sg.j1 - sg.j0;
+        for (int j = FUSED ? sg.j0 - 1 : sg.j0; j < sg.j1; ++j, ++rg) {
+          const int s = rg % kStages;
+          ok = mbar_wait(&bars[kBarKVFull + s], (rg / kStages) & 1, abort_flag, status);
+          if (!ok) break;
+          if (j >= sg.j0) {
+            uint4* vp = reinterpret_cast<uint4*>(sV(s));
+            for (int idx = ct; idx < BN * kRowBytes / 16; idx += 64) {
+              uint4 w = vp[idx];
+              w.x = bf16x2_to_f16x2(w.x);
+              w.y = bf16x2_to_f16x2(w.y);
+              w.z = bf16x2_to_f16x2(w.z);
+              w.w = bf16x2_to_f16x2(w.w);
+              vp[idx] = w;
+            }
+            fence_proxy_async_smem();
           }
-          fence_proxy_async_smem();
+          mbar_arrive(&bars[kBarVReady + s]);
         }
-        mbar_arrive(&bars[kBarVReady + s]);
       }
     }
+  }
   } else {
     // ------------------------------------------------------------ softmax / epilogue
     const int wg = (warp - 4) >> 2;          // query tile of this warpgroup
     const int wq = warp & 3;                 // TMEM lane quarter
     const int r = wq * 32 + lane;            // row inside the tile
     const int H = args.H, W = args.W, N = args.N;
-    const int n = (qt0 + wg) * kBlockM + r;
-    const bool row_valid = n < N;
-    const int qh = row_valid ? n / W : 0;
-    const int qw = row_valid ? n - qh * W : 0;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tbase + lane_off + 128 * wg;
     const uint32_t tP = tbase + lane_off + 256 + 64 * wg;
@@ -281,151 +363,277 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int HS = Hpad + 1;
     float* bh_row = area + r * HS;
     const float NEG_INF = -__int_as_float(0x7f800000);
-
-    float bw[WP];
-    bool ok = true;
-    if (FUSED) {
-      ok = warp_all(mbar_wait(&bars[kBarGFull], 0, abort_flag, status));
-      tc_fence_after();
-      float* stg = area + r * kBiasStride;
-      if (ok) skew_row_to_smem(tbase + lane_off + 256 * wg + 128, qw, W, stg, kLog2e);
-      #pragma unroll
-      for (int kw = 0; kw < WP; ++kw) bw[kw] = (ok && kw < W) ? stg[kw] : NEG_INF;
-      // the staging rows (stride kBiasStride) overlap the bias rows (stride HS)
-      named_bar_sync(1 + wg, kBlockM);
-      if (ok) {
-        skew_row_to_smem(tbase + lane_off + 256 * wg, qh, H, bh_row, kLog2e);
-        for (int kh = H; kh < Hpad; ++kh) bh_row[kh] = NEG_INF;
-      }
-      tc_fence_before();
-      mbar_arrive(&bars[kBarGFree]);
-    } else {
-      const size_t row = static_cast<size_t>(bh) * N + n;
-      #pragma unroll
-      for (int kw = 0; kw < WP; ++kw)
-        bw[kw] = kw < W ? (row_valid ? kLog2e * load_elem(args.rel_w, row * W + kw, args.bias_fmt) : 0.f)
-                        : NEG_INF;
-      for (int kh = 0; kh < Hpad; ++kh)
-        bh_row[kh] = kh < H ? (row_valid ? kLog2e * load_elem(args.rel_h, row * H + kh, args.bias_fmt) : 0.f)
-                            : NEG_INF;
-    }
-
     const float sl2 = args.scale_log2;
     const float2 sl2v = make_float2(sl2, sl2);
-    float m_used = 0.f;
-    float2 lsum = make_float2(0.f, 0.f);
-    for (int j = 0; j < n_kv && ok; ++j) {
-      ok = warp_all(mbar_wait(&bars[kBarSFull + wg], j & 1, abort_flag, status));
-      if (!ok) break;
-      tc_fence_after();
-      float bhv[KHT];
-      #pragma unroll
-      for (int g = 0; g < KHT; ++g) bhv[g] = bh_row[j * KHT + g];
 
-      // pass 1: per-grid-row maxima of scale*s*log2e + rel_w*log2e
-      float gm[KHT];
-      #pragma unroll
-      for (int g = 0; g < KHT; ++g) gm[g] = NEG_INF;
-      #pragma unroll
-      for (int c = 0; c < kChunks; ++c) {
-        uint32_t u[16];
-        tmem_ld16(tS + 16 * c, u);
-        tmem_wait_ld();
+    int gi = 0, seg = 0, pseg = 0;
+    bool ok = true;
+    for (long long it = it_begin; it < it_end && ok; ++seg) {
+      const Segment sg = segment_at(it, it_end, n_kv);
+      it += sg.j1 - sg.j0;
+      const int bh = sg.u / args.n_pairs;
+      const int qt = 2 * (sg.u - bh * args.n_pairs) + wg;
+      const int n = qt * kBlockM + r;
+      const bool row_valid = n < N;
+      const int qh = row_valid ? n / W : 0;
+      const int qw = row_valid ? n - qh * W : 0;
+
+      float bw[WP];
+      if (FUSED) {
+        ok = warp_all(mbar_wait(&bars[kBarGFull], seg & 1, abort_flag, status));
+        tc_fence_after();
+        float* stg = area + r * kBiasStride;
+        if (ok) skew_row_to_smem(tbase + lane_off + 256 * wg + 128, qw, W, stg, kLog2e);
         #pragma unroll
-        for (int k = 0; k < 16; k += 2) {
-          const int col = 16 * c + k;
-          const int g = col / WP, kw = col % WP;
-          const float2 t = ffma2(make_float2(__uint_as_float(u[k]), __uint_as_float(u[k + 1])), sl2v,
-                                 make_float2(bw[kw], bw[kw + 1]));
-          gm[g] = fmax3(gm[g], t.x, t.y);
+        for (int kw = 0; kw < WP; ++kw) bw[kw] = (ok && kw < W) ? stg[kw] : NEG_INF;
+        // the staging rows (stride kBiasStride) overlap the bias rows (stride HS):
+        // every thread of the warpgroup has read its staged row before any bias row is written
+        mbar_arrive(&bars[kBarStg + wg]);
+        ok = warp_all(mbar_wait(&bars[kBarStg + wg], seg & 1, abort_flag, status) && ok);
+        if (ok) {
+          skew_row_to_smem(tbase + lane_off + 256 * wg, qh, H, bh_row, kLog2e);
+          for (int kh = H; kh < Hpad; ++kh) bh_row[kh] = NEG_INF;
         }
+        tc_fence_before();
+        mbar_arrive(&bars[kBarGFree]);
+        if (!ok) break;
+      } else {
+        const size_t row = static_cast<size_t>(bh) * N + n;
+        #pragma unroll
+        for (int kw = 0; kw < WP; ++kw)
+          bw[kw] = kw < W ? (row_valid ? kLog2e * load_elem(args.rel_w, row * W + kw, args.bias_fmt) : 0.f)
+                          : NEG_INF;
+        // each thread rewrites only its own bias row, which no other thread reads
+        for (int kh = 0; kh < Hpad; ++kh)
+          bh_row[kh] = kh < H ? (row_valid ? kLog2e * load_elem(args.rel_h, row * H + kh, args.bias_fmt) : 0.f)
+                              : NEG_INF;
       }
-      float mt = NEG_INF;
-      #pragma unroll
-      for (int g = 0; g < KHT; ++g) mt = fmaxf(mt, gm[g] + bhv[g]);
 
-      if (j > 0) {
-        ok = warp_all(mbar_wait(&bars[kBarODone + wg], (j - 1) & 1, abort_flag, status));
+      // S is processed in blocks of kBlk columns (one TMEM load and one wait
+      // each); narrow grids, with more grid rows per tile, use 16 to keep
+      // their per-row bias terms in registers.
+      constexpr int kBlk = WP <= 16 ? 16 : 32;
+      auto load_block = [&](int cb, uint32_t (&u)[kBlk]) {
+        if (kBlk == 32 && BN - cb >= 32) tmem_ld32(tS + cb, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+        else tmem_ld16(tS + cb, *reinterpret_cast<uint32_t(*)[16]>(&u[0]));
+        tmem_wait_ld();
+      };
+      // Exact tile maximum of x = s*scale*log2e + rel_w*log2e + rel_h*log2e.
+      auto tile_max = [&](const float (&bhv)[KHT]) -> float {
+        float gm[KHT];
+        #pragma unroll
+        for (int g = 0; g < KHT; ++g) gm[g] = NEG_INF;
+        #pragma unroll
+        for (int cb = 0; cb < BN; cb += kBlk) {
+          uint32_t u[kBlk];
+          load_block(cb, u);
+          #pragma unroll
+          for (int k = 0; k < kBlk; k += 2) {
+            const int col = cb + k;
+            if (col < BN) {
+              const int g = col / WP, kw = col % WP;
+              const float2 t = ffma2(make_float2(__uint_as_float(u[k]), __uint_as_float(u[k + 1])), sl2v,
+                                     make_float2(bw[kw], bw[kw + 1]));
+              gm[g] = fmax3(gm[g], t.x, t.y);
+            }
+          }
+        }
+        float mt = NEG_INF;
+        #pragma unroll
+        for (int g = 0; g < KHT; ++g) mt = fmaxf(mt, gm[g] + bhv[g]);
+        return mt;
+      };
+      // p = 2^(x - m) for the whole tile into P (fp16, TMEM); returns the row sum.
+      auto exp_pass = [&](const float (&bhv)[KHT], float m) -> float2 {
+        float2 off[KHT];
+        #pragma unroll
+        for (int g = 0; g < KHT; ++g) off[g] = make_float2(bhv[g] - m, bhv[g] - m);
+        float2 ts = make_float2(0.f, 0.f);
+        #pragma unroll
+        for (int cb = 0; cb < BN; cb += kBlk) {
+          uint32_t u[kBlk];
+          load_block(cb, u);
+          uint32_t pk[kBlk / 2];
+          #pragma unroll
+          for (int k = 0; k < kBlk; k += 2) {
+            const int col = cb + k;
+            if (col < BN) {
+              const int g = col / WP, kw = col % WP;
+              float2 t = ffma2(make_float2(__uint_as_float(u[k]), __uint_as_float(u[k + 1])), sl2v,
+                               make_float2(bw[kw], bw[kw + 1]));
+              t = fadd2(t, off[g]);
+              const float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+              ts = fadd2(ts, p);
+              pk[k / 2] = pack_f16x2(p.x, p.y);
+            }
+          }
+          if (kBlk == 32 && BN - cb >= 32) tmem_st16(tP + cb / 2, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+          else tmem_st8(tP + cb / 2, *reinterpret_cast<uint32_t(*)[8]>(&pk[0]));
+        }
+        return ts;
+      };
+
+      // Online softmax over the segment's key tiles.  The first tile takes the
+      // exact maximum; later tiles exponentiate against the running maximum
+      // at once and are redone exactly only if their row sum exceeds 2^15
+      // (so every p stays below the fp16 limit).  The final O / l uses the
+      // same running maximum, so skipping rescales changes nothing.
+      float m_used = 0.f;
+      float2 lsum = make_float2(0.f, 0.f);
+      for (int j = sg.j0; j < sg.j1; ++j, ++gi) {
+        ok = warp_all(mbar_wait(&bars[kBarSFull + wg], gi & 1, abort_flag, status));
         if (!ok) break;
         tc_fence_after();
-      }
-      if (j == 0) {
-        m_used = mt;
-      } else if (__any_sync(0xffffffffu, mt > m_used + kRescaleTau)) {
-        // Lazy rescale: only when some row of the warp outgrew its stale max.
-        const float m_new = fmaxf(m_used, mt);
-        const float alpha = ex2_approx(m_used - m_new);
-        m_used = m_new;
-        lsum.x *= alpha;
-        lsum.y *= alpha;
-        #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[16];
-          tmem_ld16(tO + 16 * c, o);
-          tmem_wait_ld();
-          #pragma unroll
-          for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-          tmem_st16(tO + 16 * c, o);
+        if (j > sg.j0) {
+          // PV of the previous tile has finished reading P and writing O
+          ok = warp_all(mbar_wait(&bars[kBarODone + wg], (gi - 1) & 1, abort_flag, status));
+          if (!ok) break;
+          tc_fence_after();
         }
-      }
-      float2 off[KHT];
-      #pragma unroll
-      for (int g = 0; g < KHT; ++g) off[g] = make_float2(bhv[g] - m_used, bhv[g] - m_used);
-
-      // pass 2: p = 2^(x - m), row sums, P (fp16) into TMEM
-      #pragma unroll
-      for (int c = 0; c < kChunks; ++c) {
-        uint32_t u[16];
-        tmem_ld16(tS + 16 * c, u);
-        tmem_wait_ld();
-        uint32_t pk[8];
+        float bhv[KHT];
         #pragma unroll
-        for (int k = 0; k < 16; k += 2) {
-          const int col = 16 * c + k;
-          const int g = col / WP, kw = col % WP;
-          float2 t = ffma2(make_float2(__uint_as_float(u[k]), __uint_as_float(u[k + 1])), sl2v,
-                           make_float2(bw[kw], bw[kw + 1]));
-          t = fadd2(t, off[g]);
-          const float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
-          lsum = fadd2(lsum, p);
-          pk[k / 2] = pack_f16x2(p.x, p.y);
-        }
-        tmem_st8(tP + 8 * c, pk);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars[kBarPFull + wg]);
-    }
+        for (int g = 0; g < KHT; ++g) bhv[g] = bh_row[j * KHT + g];
 
-    // epilogue: out = O / l
-    if (ok) ok = warp_all(mbar_wait(&bars[kBarODone + wg], (n_kv - 1) & 1, abort_flag, status));
-    if (ok) {
+        float2 ts = make_float2(0.f, 0.f);
+        bool exact = j == sg.j0;
+        if (!exact) {
+          ts = exp_pass(bhv, m_used);
+          exact = __any_sync(0xffffffffu, !(ts.x + ts.y <= kSpecSumLimit));
+        }
+        if (exact) {
+          const float mt = tile_max(bhv);
+          if (j == sg.j0) {
+            m_used = mt;
+          } else {
+            const float m_new = fmaxf(m_used, mt);
+            const float alpha = ex2_approx(m_used - m_new);
+            m_used = m_new;
+            lsum.x *= alpha;
+            lsum.y *= alpha;
+            #pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              uint32_t o[32];
+              tmem_ld32(tO + 32 * c, o);
+              tmem_wait_ld();
+              #pragma unroll
+              for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+              tmem_st32(tO + 32 * c, o);
+            }
+          }
+          ts = exp_pass(bhv, m_used);
+        }
+        lsum = fadd2(lsum, ts);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars[kBarPFull + wg]);
+      }
+      if (!ok) break;
+
+      // epilogue: O (fp32, unnormalised) out of TMEM
+      ok = warp_all(mbar_wait(&bars[kBarODone + wg], (gi - 1) & 1, abort_flag, status));
+      if (!ok) break;
       tc_fence_after();
-      const float inv_l = 1.0f / (lsum.x + lsum.y);
-      uint8_t* orow = reinterpret_cast<uint8_t*>(args.out) +
-                      (static_cast<size_t>(bh) * N + (row_valid ? n : 0)) * kHeadDim * (args.out_fmt == kF32 ? 4 : 2);
+      float o[kHeadDim];
       #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t o[16];
-        tmem_ld16(tO + 16 * c, o);
+        uint32_t v16[16];
+        tmem_ld16(tO + 16 * c, v16);
         tmem_wait_ld();
-        if (row_valid) {
-          if (args.out_fmt == kF32) {
-            float4* dst = reinterpret_cast<float4*>(orow) + 4 * c;
+        #pragma unroll
+        for (int k = 0; k < 16; ++k) o[16 * c + k] = __uint_as_float(v16[k]);
+      }
+      tc_fence_before();
+      if (FUSED) mbar_arrive(&bars[kBarEpiDone]);
+      float l = lsum.x + lsum.y;
+      float m = m_used;
+
+      bool store = true;
+      if (!sg.full(n_kv)) {
+        // Partial unit: publish (O, m, l) and let the last CTA of the unit merge.
+        const int c = blockIdx.x;
+        const int slot = (seg == 0) ? 2 * c : 2 * c + 1;
+        float* ws = args.partials + (static_cast<size_t>(slot) * 2 + wg) * kBlockM * kSlotRow + r * kSlotRow;
+        #pragma unroll
+        for (int q4 = 0; q4 < 16; ++q4)
+          __stcg(reinterpret_cast<float4*>(ws) + q4, make_float4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]));
+        __stcg(reinterpret_cast<float2*>(ws + 64), make_float2(m, l));
+        __threadfence();
+        mbar_arrive(&bars[kBarPartWritten]);
+        const long long u0 = static_cast<long long>(sg.u) * n_kv;
+        const int c_first = sched.cta_of(u0);
+        const int nseg = sched.cta_of(u0 + n_kv - 1) - c_first + 1;
+        if (wg == 0 && r == 0) {
+          bool w_ok = mbar_wait(&bars[kBarPartWritten], pseg & 1, abort_flag, status);
+          int last = 0;
+          if (w_ok) {
+            const int old = atomicAdd(args.counters + sg.u, 1);
+            last = old == nseg - 1;
+            if (last) {
+              __threadfence();
+              args.counters[sg.u] = 0;  // ready for the next launch
+            }
+          }
+          *merge_flag = last;
+          mbar_arrive(&bars[kBarMergeGo]);
+        }
+        ok = mbar_wait(&bars[kBarMergeGo], pseg & 1, abort_flag, status);
+        ++pseg;
+        if (!ok) break;
+        store = *merge_flag != 0;
+        if (store) {
+          // merge the unit's segments: rescale each to the largest max
+          const bool first_is_first = sched.begin(c_first) == u0;
+          float mm[4], ll[4];
+          const float* rowp[4];
+          float mstar = NEG_INF;
+          const int ns = min(nseg, 4);
+          for (int s = 0; s < ns; ++s) {
+            const int cs = c_first + s;
+            const int sl = (s > 0 || first_is_first) ? 2 * cs : 2 * cs + 1;
+            rowp[s] = args.partials + (static_cast<size_t>(sl) * 2 + wg) * kBlockM * kSlotRow + r * kSlotRow;
+            const float2 ml = __ldcg(reinterpret_cast<const float2*>(rowp[s] + 64));
+            mm[s] = ml.x;
+            ll[s] = ml.y;
+            mstar = fmaxf(mstar, mm[s]);
+          }
+          #pragma unroll
+          for (int k = 0; k < kHeadDim; ++k) o[k] = 0.f;
+          l = 0.f;
+          for (int s = 0; s < ns; ++s) {
+            const float a = ex2_approx(mm[s] - mstar);
+            l += a * ll[s];
             #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-              dst[q4] = make_float4(__uint_as_float(o[4 * q4]) * inv_l, __uint_as_float(o[4 * q4 + 1]) * inv_l,
-                                    __uint_as_float(o[4 * q4 + 2]) * inv_l, __uint_as_float(o[4 * q4 + 3]) * inv_l);
-          } else {
-            uint32_t w[8];
+            for (int q4 = 0; q4 < 16; ++q4) {
+              const float4 v4 = __ldcg(reinterpret_cast<const float4*>(rowp[s]) + q4);
+              o[4 * q4] += a * v4.x;
+              o[4 * q4 + 1] += a * v4.y;
+              o[4 * q4 + 2] += a * v4.z;
+              o[4 * q4 + 3] += a * v4.w;
+            }
+          }
+        }
+      }
+      if (store && row_valid) {
+        const float inv_l = 1.0f / l;
+        uint8_t* orow = reinterpret_cast<uint8_t*>(args.out) +
+                        (static_cast<size_t>(bh) * N + n) * kHeadDim * (args.out_fmt == kF32 ? 4 : 2);
+        if (args.out_fmt == kF32) {
+          float4* dst = reinterpret_cast<float4*>(orow);
+          #pragma unroll
+          for (int q4 = 0; q4 < 16; ++q4)
+            dst[q4] = make_float4(o[4 * q4] * inv_l, o[4 * q4 + 1] * inv_l, o[4 * q4 + 2] * inv_l,
+                                  o[4 * q4 + 3] * inv_l);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(orow);
+          #pragma unroll
+          for (int q8 = 0; q8 < 8; ++q8) {
+            uint32_t w[4];
             #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const float a = __uint_as_float(o[2 * k]) * inv_l, b = __uint_as_float(o[2 * k + 1]) * inv_l;
+            for (int k = 0; k < 4; ++k) {
+              const float a = o[8 * q8 + 2 * k] * inv_l, b = o[8 * q8 + 2 * k + 1] * inv_l;
               w[k] = args.out_fmt == kBF16 ? pack_bf16x2(a, b) : pack_f16x2(a, b);
             }
-            uint4* dst = reinterpret_cast<uint4*>(orow) + 2 * c;
-            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            dst[q8] = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
       }

@@ -6,11 +6,11 @@
 namespace dera {
 
 template <int WP>
-cudaError_t launch_attention(const AttnMaps& maps, const AttnArgs& args, bool fused, cudaStream_t stream) {
+cudaError_t launch_attention(const AttnMaps& maps, const AttnArgs& args, int ctas, bool fused, cudaStream_t stream) {
   auto kern = fused ? relpos_attn_kernel<WP, true> : relpos_attn_kernel<WP, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnSmem::kAlloc);
   if (e != cudaSuccess) return e;
-  const unsigned grid = static_cast<unsigned>(args.n_pairs) * static_cast<unsigned>(args.BH);
+  const unsigned grid = static_cast<unsigned>(ctas);
   kern<<<grid, kAttnThreads, AttnSmem::kAlloc, stream>>>(maps.q, maps.k, maps.v, maps.th, maps.tw, args);
   return cudaGetLastError();
 }

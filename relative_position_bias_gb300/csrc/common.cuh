@@ -14,6 +14,7 @@ constexpr int kBlockM = 128;      // query rows per tile (one TMEM lane per row)
 constexpr int kRowBytes = 128;    // one 64-element 16-bit row
 constexpr int kTileBytes = 128 * kRowBytes;  // a 128-row operand tile (16 KB)
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kSlotRow = 68;      // floats per row of a partial-result slot: O[64], m, l, pad
 
 // Key tiles cover KHT whole grid rows of WP (>= W) padded columns, so the
 // column of a key inside its tile fixes kw at compile time.  The padded
@@ -35,9 +36,12 @@ struct AttnArgs {
   const void* rel_w;   // [BH, N, W]
   void* out;           // [BH, N, 64]
   int* status;         // device status word
+  float* partials;     // [2 * gridDim.x][2][128][kSlotRow] partial results (split units only)
+  int* counters;       // [n_units] segment arrivals per unit, zero at launch (split units only)
   int BH, H, W, N;
   int n_qtiles;        // ceil(N / 128)
-  int n_pairs;         // ceil(n_qtiles / 2): CTAs per head
+  int n_pairs;         // ceil(n_qtiles / 2): query-tile pairs per head
+  int n_units;         // BH * n_pairs
   int n_kv;            // ceil(H / KHT)
   float scale_log2;    // scale * log2(e)
   int in_fmt;          // kF16 | kBF16

@@ -159,6 +159,49 @@ bool map_table(CUtensorMap* m, const void* p, dera_dtype t, int L) {
 int padded_width(int W) { return W <= 16 ? 16 : (W <= 32 ? 32 : (W <= 40 ? 40 : 64)); }
 int rows_per_tile(int WP) { return WP <= 16 ? 8 : (WP <= 32 ? 4 : 2); }
 
+// Streaming-multiprocessor count of a device (cached).
+int sm_count(int dev) {
+  static int counts[kMaxDevices] = {};
+  if (dev < 0 || dev >= kMaxDevices) return 0;
+  if (counts[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    counts[dev] = n;
+  }
+  return counts[dev];
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Work decomposition of one call: units are pairs of 128-row query tiles.
+struct Plan {
+  int n_qtiles, n_pairs, n_units, n_kv, ctas;
+  bool split;              // stream-K over `ctas` persistent CTAs (needs the workspace)
+  size_t counters_bytes, partial_bytes;
+};
+
+Plan make_plan(int BH, int H, int W, int sms) {
+  Plan p;
+  const int N = H * W;
+  const int KHT = rows_per_tile(padded_width(W));
+  p.n_qtiles = (N + kBlockM - 1) / kBlockM;
+  p.n_pairs = (p.n_qtiles + 1) / 2;
+  p.n_units = BH * p.n_pairs;
+  p.n_kv = (H + KHT - 1) / KHT;
+  // Split only when the units do not fill whole waves of one CTA per SM; with
+  // more units than CTAs every CTA range spans at least one unit's key tiles,
+  // so a unit is cut into at most two segments.
+  p.split = sms > 0 && p.n_units > sms && p.n_units % sms != 0;
+  p.ctas = p.split ? sms : p.n_units;
+  p.counters_bytes = align256(static_cast<size_t>(p.n_units) * sizeof(int));
+  p.partial_bytes = static_cast<size_t>(2) * sms * 2 * kBlockM * kSlotRow * sizeof(float);
+  return p;
+}
+
+size_t workspace_bytes_for(const Plan& p) { return p.split ? p.counters_bytes + p.partial_bytes : 0; }
 dera_status current_device(int* dev) {
   if (cudaGetDevice(dev) != cudaSuccess) {
     cudaGetLastError();
@@ -175,10 +218,16 @@ dera_status current_device(int* dev) {
 
 dera_status run_attention(const void* q, const void* k, const void* v, const void* a, const void* b, void* out,
                           int BH, int H, int W, float scale, dera_dtype in_dtype, dera_dtype bias_dtype,
-                          dera_dtype out_dtype, bool fused, void* stream) {
+                          dera_dtype out_dtype, bool fused, void* workspace, size_t workspace_bytes,
+                          void* stream) {
   int dev = 0;
   DERA_TRY(current_device(&dev));
   const int N = H * W;
+  Plan plan = make_plan(BH, H, W, sm_count(dev));
+  if (plan.split && (workspace == nullptr || workspace_bytes < workspace_bytes_for(plan))) {
+    plan.split = false;  // no (or too small a) workspace: one CTA per unit
+    plan.ctas = plan.n_units;
+  }
   const int WP = padded_width(W), KHT = rows_per_tile(WP);
   AttnMaps maps;
   if (!map_rows(&maps.q, q, in_dtype, BH, N) || !map_keys(&maps.k, k, in_dtype, BH, H, W, WP, KHT) ||
@@ -200,20 +249,31 @@ dera_status run_attention(const void* q, const void* k, const void* v, const voi
   args.H = H;
   args.W = W;
   args.N = N;
-  args.n_qtiles = (N + kBlockM - 1) / kBlockM;
-  args.n_pairs = (args.n_qtiles + 1) / 2;
-  args.n_kv = (H + KHT - 1) / KHT;
+  args.n_qtiles = plan.n_qtiles;
+  args.n_pairs = plan.n_pairs;
+  args.n_units = plan.n_units;
+  args.n_kv = plan.n_kv;
+  args.partials = nullptr;
+  args.counters = nullptr;
   args.scale_log2 = scale * kLog2e;
   args.in_fmt = fmt_of(in_dtype);
   args.bias_fmt = fmt_of(bias_dtype);
   args.out_fmt = fmt_of(out_dtype);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (plan.split) {
+    args.counters = static_cast<int*>(workspace);
+    args.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.counters_bytes);
+    // the counters must start at zero; the kernel leaves them at zero too,
+    // but a launch that stopped early would not
+    if (cudaMemsetAsync(args.counters, 0, static_cast<size_t>(plan.n_units) * sizeof(int), s) != cudaSuccess)
+      return DERA_ERR_CUDA;
+  }
   cudaError_t e;
   switch (WP) {
-    case 16: e = launch_attention<16>(maps, args, fused, s); break;
-    case 32: e = launch_attention<32>(maps, args, fused, s); break;
-    case 40: e = launch_attention<40>(maps, args, fused, s); break;
-    default: e = launch_attention<64>(maps, args, fused, s); break;
+    case 16: e = launch_attention<16>(maps, args, plan.ctas, fused, s); break;
+    case 32: e = launch_attention<32>(maps, args, plan.ctas, fused, s); break;
+    case 40: e = launch_attention<40>(maps, args, plan.ctas, fused, s); break;
+    default: e = launch_attention<64>(maps, args, plan.ctas, fused, s); break;
   }
   return e == cudaSuccess ? DERA_OK : DERA_ERR_CUDA;
 }
@@ -269,10 +329,21 @@ dera_status dera_relpos_project(const void* q, const void* rel_pos_h, const void
   return e == cudaSuccess ? DERA_OK : DERA_ERR_CUDA;
 }
 
+dera_status dera_relpos_workspace_size(int BH, int H, int W, int head_dim, size_t* bytes) {
+  if (!bytes) return DERA_ERR_NULL;
+  DERA_TRY(check_shape(BH, H, W, head_dim));
+  *bytes = 0;
+  if (BH == 0) return DERA_OK;
+  int dev = 0;
+  DERA_TRY(current_device(&dev));
+  *bytes = workspace_bytes_for(make_plan(BH, H, W, sm_count(dev)));
+  return DERA_OK;
+}
+
 dera_status dera_relpos_attention(const void* q, const void* k, const void* v, const void* rel_h,
                                   const void* rel_w, void* out, int BH, int H, int W, int head_dim, float scale,
                                   dera_dtype in_dtype, dera_dtype bias_dtype, dera_dtype out_dtype,
-                                  void* stream) {
+                                  void* workspace, size_t workspace_bytes, void* stream) {
   DERA_TRY(check_shape(BH, H, W, head_dim));
   if (!is16(in_dtype) || !is_float(bias_dtype) || !(out_dtype == DERA_F32 || out_dtype == in_dtype))
     return DERA_ERR_DTYPE;
@@ -281,13 +352,18 @@ dera_status dera_relpos_attention(const void* q, const void* k, const void* v, c
   int dev = 0;
   DERA_TRY(current_device(&dev));
   for (const void* p : {q, k, v, rel_h, rel_w, static_cast<const void*>(out)}) DERA_TRY(check_ptr(p, dev));
+  if (workspace) {
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return DERA_ERR_ALIGN;
+    DERA_TRY(check_ptr(workspace, dev));
+  }
   return run_attention(q, k, v, rel_h, rel_w, out, BH, H, W, scale, in_dtype, bias_dtype, out_dtype, false,
-                       stream);
+                       workspace, workspace_bytes, stream);
 }
 
 dera_status dera_relpos_fused(const void* q, const void* k, const void* v, const void* rel_pos_h,
                               const void* rel_pos_w, void* out, int BH, int H, int W, int head_dim, float scale,
-                              dera_dtype in_dtype, dera_dtype out_dtype, void* stream) {
+                              dera_dtype in_dtype, dera_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                              void* stream) {
   DERA_TRY(check_shape(BH, H, W, head_dim));
   if (!is16(in_dtype) || !(out_dtype == DERA_F32 || out_dtype == in_dtype)) return DERA_ERR_DTYPE;
   if (BH == 0) return DERA_OK;  // empty batch: nothing to read or write
@@ -296,8 +372,12 @@ dera_status dera_relpos_fused(const void* q, const void* k, const void* v, const
   DERA_TRY(current_device(&dev));
   for (const void* p : {q, k, v, rel_pos_h, rel_pos_w, static_cast<const void*>(out)})
     DERA_TRY(check_ptr(p, dev));
+  if (workspace) {
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return DERA_ERR_ALIGN;
+    DERA_TRY(check_ptr(workspace, dev));
+  }
   return run_attention(q, k, v, rel_pos_h, rel_pos_w, out, BH, H, W, scale, in_dtype, in_dtype, out_dtype, true,
-                       stream);
+                       workspace, workspace_bytes, stream);
 }
 
 dera_status dera_relpos_device_status(int* status, int reset) {

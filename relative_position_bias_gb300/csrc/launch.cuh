@@ -13,7 +13,7 @@ struct AttnMaps {
 };
 
 template <int WP>
-cudaError_t launch_attention(const AttnMaps& maps, const AttnArgs& args, bool fused, cudaStream_t stream);
+cudaError_t launch_attention(const AttnMaps& maps, const AttnArgs& args, int ctas, bool fused, cudaStream_t stream);
 
 cudaError_t launch_project(const CUtensorMap& q, const CUtensorMap& th, const CUtensorMap& tw,
                            const ProjArgs& args, int in_fmt, cudaStream_t stream);

@@ -14,7 +14,8 @@ from relative_position_bias_gb300 import api
 from relative_position_bias_gb300 import build as rbuild
 
 EXPECTED = {"dera_relpos_project", "dera_relpos_attention", "dera_relpos_fused", "dera_status_string",
-            "dera_relpos_device_status", "dera_relpos_selftest_wait_timeout", "dera_relpos_abi_version"}
+            "dera_relpos_device_status", "dera_relpos_selftest_wait_timeout", "dera_relpos_abi_version",
+            "dera_relpos_workspace_size"}
 
 FAKE = 0x10000          # aligned, never dereferenced: every call below fails before any CUDA work
 FAKE_MISALIGNED = 0x10008
@@ -41,18 +42,18 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.dera_relpos_abi_version() == 1
+    assert lib.dera_relpos_abi_version() == 2
     for code, name in api.STATUS_NAMES.items():
         assert lib.dera_status_string(code).decode().startswith(name)
     assert lib.dera_status_string(99).decode() == "DERA_ERR_UNKNOWN"
 
 
 def _fused(lib, *, ptrs=(FAKE,) * 6, BH=1, H=4, W=4, d=64, in_dt=1, out_dt=2):
-    return lib.dera_relpos_fused(*ptrs, BH, H, W, d, 0.125, in_dt, out_dt, None)
+    return lib.dera_relpos_fused(*ptrs, BH, H, W, d, 0.125, in_dt, out_dt, None, 0, None)
 
 
 def _attn(lib, *, ptrs=(FAKE,) * 6, BH=1, H=4, W=4, d=64, in_dt=1, bias_dt=2, out_dt=2):
-    return lib.dera_relpos_attention(*ptrs, BH, H, W, d, 0.125, in_dt, bias_dt, out_dt, None)
+    return lib.dera_relpos_attention(*ptrs, BH, H, W, d, 0.125, in_dt, bias_dt, out_dt, None, 0, None)
 
 
 def _proj(lib, *, ptrs=(FAKE,) * 5, BH=1, H=4, W=4, d=64, in_dt=1, bias_dt=2):
@@ -77,6 +78,14 @@ def test_host_validation(lib, call):
         assert call(lib, ptrs=tuple(ptrs)) == 5       # alignment
     assert call(lib, BH=0) == 0                       # empty batch: no work, no CUDA call
     assert call(lib, BH=0, ptrs=(None,) * n) == 0     # ... and no pointer is looked at
+
+
+def test_workspace_size_validation(lib):
+    n = ctypes.c_size_t(123)
+    assert lib.dera_relpos_workspace_size(1, 4, 4, 64, None) == 1
+    assert lib.dera_relpos_workspace_size(1, 4, 4, 32, ctypes.byref(n)) == 4
+    assert lib.dera_relpos_workspace_size(1, 0, 4, 64, ctypes.byref(n)) == 2
+    assert lib.dera_relpos_workspace_size(0, 4, 4, 64, ctypes.byref(n)) == 0 and n.value == 0
 
 
 def test_dtype_rules(lib):

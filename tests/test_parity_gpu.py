@@ -129,17 +129,68 @@ def _select(t: torch.Tensor, heads, rows):
     return t[heads][:, rows]
 
 
+@pytest.mark.parametrize("split", [True, False], ids=["workspace", "no-workspace"])
 @pytest.mark.parametrize("name", list(I.WORKLOADS))
-def test_fused_parity(name):
+def test_fused_parity(name, split):
+    """Default call (scratch workspace: units split across CTAs where that evens
+    the load) and the one-CTA-per-unit schedule, both against the oracle."""
     w = I.WORKLOADS[name]
     x = I.make_inputs(w)
     d = _dev(x)
     args = (d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W, w.scale)
-    o32 = rpb.fused(*args, out_dtype=torch.float32)
-    o16 = rpb.fused(*args)
+    ws = None if split else False
+    o32 = rpb.fused(*args, out_dtype=torch.float32, workspace=ws)
+    o16 = rpb.fused(*args, workspace=ws)
     torch.cuda.synchronize()
     heads, rows, want = _oracle_full_or_rows(w, _f64(x), "fused")
     check_out(_select(o32, heads, rows), want, _select(o16, heads, rows), what=f"fused {name}")
+
+
+@pytest.mark.parametrize("entry", ["fused", "attention"])
+@pytest.mark.parametrize("BH", [None, 1, 2, 3], ids=["sms+1", "sms+sms/2", "2sms+1", "3sms-1"])
+def test_split_schedule_ragged(entry, BH):
+    """Unit counts just past whole waves of the device, on a ragged 40x40 grid
+    (7 query-tile pairs per head), so most units are cut between two CTAs."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    pairs = 7
+    units = {None: sms + 1, 1: sms + sms // 2, 2: 2 * sms + 1, 3: 3 * sms - 1}[BH]
+    heads = -(-units // pairs)
+    w = I.WORKLOADS["ragged40"].with_grid(40, 40, B=1, heads=heads)
+    assert rpb.workspace_size(w.BH, w.H, w.W) > 0
+    x = I.make_inputs(w, seed=heads)
+    d = _dev(x)
+    f = _f64(x)
+    if entry == "fused":
+        o32 = rpb.fused(d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W, w.scale,
+                        out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        heads_s, rows, want = _oracle_full_or_rows(w, f, "fused")
+    else:
+        rh, rw = oracle.project(f["q"], f["rel_pos_h"], f["rel_pos_w"], w.H, w.W)
+        rh32, rw32 = torch.from_numpy(rh).float(), torch.from_numpy(rw).float()
+        o32 = rpb.attention(d["q"], d["k"], d["v"], rh32.cuda(), rw32.cuda(), w.H, w.W, w.scale,
+                            out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        heads_s, rows, want = _oracle_full_or_rows(w, f, "attention", (rh32.double().numpy(), rw32.double().numpy()))
+    check_out(_select(o32, heads_s, rows), want, what=f"split {entry} {w.BH} heads")
+
+
+def test_caller_workspace_and_reuse():
+    """A caller-owned workspace gives the same bytes as the cached one, call after call."""
+    w = I.WORKLOADS["global64"]
+    d = _dev(I.make_inputs(w))
+    args = (d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W, w.scale)
+    ref = rpb.fused(*args)
+    ws = torch.empty(rpb.workspace_size(w.BH, w.H, w.W), dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        again = rpb.fused(*args, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(again, ref)
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")          # too small: one CTA per unit
+    alt = rpb.fused(*args, out_dtype=torch.float32, workspace=small)
+    torch.cuda.synchronize()
+    f = _f64(I.make_inputs(w))
+    check_out(alt, oracle.fused(f["q"], f["k"], f["v"], f["rel_pos_h"], f["rel_pos_w"], w.H, w.W, w.scale))
 
 
 @pytest.mark.parametrize("name", list(I.WORKLOADS))
