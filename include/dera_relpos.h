@@ -75,7 +75,8 @@ typedef enum dera_status {
   DERA_ERR_ALIGN = 5,       /* a pointer is not 16-byte aligned */
   DERA_ERR_DEVICE = 6,      /* a pointer is not device memory of the current device */
   DERA_ERR_TIMEOUT = 7,     /* (device status only) a bounded wait expired */
-  DERA_ERR_CUDA = 8         /* a CUDA runtime/driver call failed */
+  DERA_ERR_CUDA = 8,        /* a CUDA runtime/driver call failed */
+  DERA_ERR_SCRATCH = 9      /* (dera_relpos_fused_noalloc) the problem needs more scratch than its static buffer */
 } dera_status;
 
 typedef enum dera_dtype { DERA_F16 = 0, DERA_BF16 = 1, DERA_F32 = 2 } dera_dtype;
@@ -143,6 +144,45 @@ DERA_API dera_status dera_relpos_fused(const void* q, const void* k, const void*
  * entry point clears the counters with cudaMemsetAsync on `stream` first.
  */
 DERA_API dera_status dera_relpos_workspace_size(int BH, int H, int W, int head_dim, size_t* bytes);
+
+/*
+ * Allocation-free variant of dera_relpos_fused (the pages have no
+ * counterpart: it exists for callers of this library that are not allowed
+ * to allocate device memory).  Some callers cannot call cudaMalloc at all:
+ * plug-ins living inside a host engine that owns every byte of device memory
+ * and forbids allocations after start-up, or latency-critical code that must
+ * never hit the implicit device synchronisation an allocation can cause.
+ * Such a caller still passes its own inputs and output, but cannot hand over
+ * the scratch workspace that dera_relpos_fused uses when it splits work
+ * units between CTAs.
+ *
+ * This entry point computes exactly what dera_relpos_fused computes (same
+ * arguments minus the workspace) and takes its scratch from a buffer
+ * compiled into the library: a file-scope device array of
+ * DERA_NOALLOC_SCRATCH_BYTES (24 MiB) that every GPU which loads the library
+ * holds until the process exits.  It calls no cudaMalloc/cudaFree and no
+ * allocating library routine.
+ *   - Set-up: the first call on each device looks up the device address of
+ *     that buffer (cudaGetSymbolAddress) with the device current and caches
+ *     it; make that first call on a device before any stream capture.
+ *   - Limit: problems whose split schedule needs more scratch than the
+ *     buffer holds are rejected with DERA_ERR_SCRATCH before anything is
+ *     enqueued.  The need is what dera_relpos_workspace_size reports: on a
+ *     152-SM GB300, 21 168 128 bytes of partial-result slots plus 4 bytes per
+ *     work unit (a pair of 128-row query tiles of one head), so problems of
+ *     up to about 999 000 units fit.  Problems that need no scratch always run.
+ *   - Sharing: every call on a device uses the same buffer and leaves its
+ *     contents behind; the call clears the per-unit counters it relies on
+ *     (cudaMemsetAsync on `stream`) before the launch.  Calls that overlap on
+ *     the GPU (for example on two streams) race on the buffer and give wrong
+ *     results: serialise them.
+ * Other arguments, layouts and errors: as dera_relpos_fused.
+ */
+#define DERA_NOALLOC_SCRATCH_BYTES (24u * 1024u * 1024u)
+DERA_API dera_status dera_relpos_fused_noalloc(const void* q, const void* k, const void* v, const void* rel_pos_h,
+                                               const void* rel_pos_w, void* out, int BH, int H, int W,
+                                               int head_dim, float scale, dera_dtype in_dtype, dera_dtype out_dtype,
+                                               void* stream);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 DERA_API const char* dera_status_string(dera_status status);

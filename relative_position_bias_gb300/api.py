@@ -23,7 +23,7 @@ DERA_F16, DERA_BF16, DERA_F32 = 0, 1, 2
 _DTYPE_CODE = {torch.float16: DERA_F16, torch.bfloat16: DERA_BF16, torch.float32: DERA_F32}
 STATUS_NAMES = {0: "DERA_OK", 1: "DERA_ERR_NULL", 2: "DERA_ERR_SHAPE", 3: "DERA_ERR_DTYPE",
                 4: "DERA_ERR_HEAD_DIM", 5: "DERA_ERR_ALIGN", 6: "DERA_ERR_DEVICE", 7: "DERA_ERR_TIMEOUT",
-                8: "DERA_ERR_CUDA"}
+                8: "DERA_ERR_CUDA", 9: "DERA_ERR_SCRATCH"}
 
 _lib = None
 _lock = threading.Lock()

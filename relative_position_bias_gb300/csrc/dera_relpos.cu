@@ -278,6 +278,28 @@ dera_status run_attention(const void* q, const void* k, const void* v, const voi
   return e == cudaSuccess ? DERA_OK : DERA_ERR_CUDA;
 }
 
+// Scratch of dera_relpos_fused_noalloc: a buffer compiled into the library,
+// for callers that cannot allocate device memory.  In host code the array's
+// name only stands in for the symbol; its device address is looked up once
+// per device (with that device current) and passed to the kernel.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DERA_NOALLOC_SCRATCH_BYTES];
+
+void* noalloc_scratch(int dev) {
+  static void* ptrs[kMaxDevices] = {};
+  static std::mutex mu;
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    ptrs[dev] = p;
+  }
+  return ptrs[dev];
+}
+
 }  // namespace
 
 extern "C" {
@@ -293,6 +315,7 @@ const char* dera_status_string(dera_status status) {
     case DERA_ERR_DEVICE: return "DERA_ERR_DEVICE: pointer is not device memory of the current device";
     case DERA_ERR_TIMEOUT: return "DERA_ERR_TIMEOUT: a bounded wait expired inside a kernel";
     case DERA_ERR_CUDA: return "DERA_ERR_CUDA: a CUDA call failed";
+    case DERA_ERR_SCRATCH: return "DERA_ERR_SCRATCH: the problem needs more scratch than the static buffer holds";
   }
   return "DERA_ERR_UNKNOWN";
 }
@@ -401,6 +424,28 @@ dera_status dera_relpos_selftest_wait_timeout(long long budget_cycles, void* str
   return launch_wait_selftest(st, budget_cycles, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? DERA_OK
              : DERA_ERR_CUDA;
+}
+
+dera_status dera_relpos_fused_noalloc(const void* q, const void* k, const void* v, const void* rel_pos_h,
+                                      const void* rel_pos_w, void* out, int BH, int H, int W, int head_dim,
+                                      float scale, dera_dtype in_dtype, dera_dtype out_dtype, void* stream) {
+  DERA_TRY(check_shape(BH, H, W, head_dim));
+  if (!is16(in_dtype) || !(out_dtype == DERA_F32 || out_dtype == in_dtype)) return DERA_ERR_DTYPE;
+  if (BH == 0) return DERA_OK;  // empty batch: nothing to read or write
+  DERA_TRY(check_host({q, k, v, rel_pos_h, rel_pos_w, out}));
+  int dev = 0;
+  DERA_TRY(current_device(&dev));
+  for (const void* p : {q, k, v, rel_pos_h, rel_pos_w, static_cast<const void*>(out)})
+    DERA_TRY(check_ptr(p, dev));
+  const size_t need = workspace_bytes_for(make_plan(BH, H, W, sm_count(dev)));
+  if (need > DERA_NOALLOC_SCRATCH_BYTES) return DERA_ERR_SCRATCH;
+  void* scratch = nullptr;
+  if (need > 0) {
+    scratch = noalloc_scratch(dev);
+    if (!scratch) return DERA_ERR_CUDA;
+  }
+  return run_attention(q, k, v, rel_pos_h, rel_pos_w, out, BH, H, W, scale, in_dtype, in_dtype, out_dtype, true,
+                       scratch, need, stream);
 }
 
 }  // extern "C"

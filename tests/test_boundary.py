@@ -15,7 +15,7 @@ from relative_position_bias_gb300 import build as rbuild
 
 EXPECTED = {"dera_relpos_project", "dera_relpos_attention", "dera_relpos_fused", "dera_status_string",
             "dera_relpos_device_status", "dera_relpos_selftest_wait_timeout", "dera_relpos_abi_version",
-            "dera_relpos_workspace_size"}
+            "dera_relpos_workspace_size", "dera_relpos_fused_noalloc"}
 
 FAKE = 0x10000          # aligned, never dereferenced: every call below fails before any CUDA work
 FAKE_MISALIGNED = 0x10008
