@@ -311,9 +311,41 @@ def run_ours(args, w, rank: int, world: int) -> dict | None:
     e2e_s = aggregate_max(e0.elapsed_time(e1) / 1e3)
     e2e_value = job_value(flops, e2e_steps, world, e2e_s)
 
+    # the other kernels of the path, on the same workload: projection alone
+    # (HBM-bound) and the two-step path (projection + compact-bias attention)
+    rh = torch.empty(w.BH, w.N, w.H, device=dev)
+    rw = torch.empty(w.BH, w.N, w.W, device=dev)
+    extra_steps = max(3, min(args.steps, 100))
+
+    def timed(fn):
+        evs = []
+        for _ in range(3):
+            flush.fill_(3)
+            fn()
+        for _ in range(extra_steps):
+            flush.fill_(7)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+    proj_ms = timed(lambda: rpb.project(d["q"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W, rel_h=rh, rel_w=rw))
+    attn_ms = timed(lambda: rpb.attention(d["q"], d["k"], d["v"], rh, rw, w.H, w.W, w.scale, out=out))
     if rank != 0:
         return None
     peaks, peak_src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    proj_bytes = (w.BH * w.N * w.d * 2 + w.BH * w.N * (w.H + w.W) * 4 + (2 * w.H - 1 + 2 * w.W - 1) * w.d * 2)
+    extra = {
+        "projection": {"kernel": "relpos_project_kernel", "ms": proj_ms, "bytes_per_launch": proj_bytes,
+                       "gbs": proj_bytes / (proj_ms * 1e-3) / 1e9, "hbm_peak_gbs": hbm,
+                       "frac_hbm": proj_bytes / (proj_ms * 1e-3) / 1e9 / hbm},
+        "two_step": {"ms": proj_ms + attn_ms, "attention_ms": attn_ms,
+                     "attention_tflops": attention_flops(w.BH, w.N, w.d) / (attn_ms * 1e-3) / 1e12},
+    }
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     achieved = flops / (sum(ms) / len(ms) / 1e3) / 1e12
     kernel = "relpos_attn_kernel<64,fused>" if args.entry == "fused" else "relpos_attn_kernel<64,compact>"
@@ -333,6 +365,7 @@ def run_ours(args, w, rank: int, world: int) -> dict | None:
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
         "wall_s_timed_region": t_wall,
+        "other_kernels": extra,
     }
     if not args.no_cpu_baseline:
         v, sample, _ = cpu_oracle_throughput(w, budget_s=args.cpu_budget)

@@ -69,29 +69,61 @@ enum : int {
 };
 static_assert(kBarCount <= AttnSmem::kNumBars, "barrier slots");
 
-// Stream-K partition of the (unit, key tile) iteration space.
+// Work schedule over G persistent CTAs: all but the last one-and-a-fraction
+// waves of units run as data-parallel rounds (CTA c takes unit r*G + c in
+// round r, so the CTAs active together work on consecutive units, i.e. on the
+// same heads, and share those heads' K/V in L2); the remaining G + (U mod G)
+// units form a stream-K tail whose (unit, key tile) iterations are cut into G
+// equal contiguous ranges.  Every tail range holds at least one unit's worth
+// of key tiles, so a unit is cut into at most two segments.  With U a
+// multiple of G the tail is one whole unit per CTA and nothing is cut.
+// Iterations are numbered globally: t = unit * n_kv + key tile.
 struct Schedule {
-  long long T;   // units * n_kv
-  int G;         // CTAs
-  int n_kv;
-  __device__ __forceinline__ long long begin(int c) const { return static_cast<long long>(c) * T / G; }
-  __device__ __forceinline__ int cta_of(long long t) const { return static_cast<int>(((t + 1) * G - 1) / T); }
+  int G, n_kv, dp_rounds;
+  long long sk_base, T;  // first tail iteration, tail length
+  __device__ __forceinline__ Schedule(int U, int G_, int n_kv_) : G(G_), n_kv(n_kv_) {
+    dp_rounds = max(U / G - 1, 0);
+    sk_base = static_cast<long long>(dp_rounds) * G * n_kv;
+    T = static_cast<long long>(U - dp_rounds * G) * n_kv;
+  }
+  __device__ __forceinline__ long long begin(int c) const { return sk_base + static_cast<long long>(c) * T / G; }
+  // CTA whose tail range holds iteration t (t >= sk_base)
+  __device__ __forceinline__ int cta_of(long long t) const {
+    return static_cast<int>(((t - sk_base + 1) * G - 1) / T);
+  }
 };
 
-// One segment of a CTA's range: key tiles [j0, j1) of unit u.
+// One segment of a CTA's work: key tiles [j0, j1) of unit u; tail = index of
+// the segment within the CTA's stream-K range (-1 for a data-parallel unit).
 struct Segment {
-  int u, j0, j1;
+  int u, j0, j1, tail;
   __device__ __forceinline__ bool full(int n_kv) const { return j0 == 0 && j1 == n_kv; }
 };
 
-__device__ __forceinline__ Segment segment_at(long long it, long long end, int n_kv) {
-  Segment s;
-  s.u = static_cast<int>(it / n_kv);
-  s.j0 = static_cast<int>(it - static_cast<long long>(s.u) * n_kv);
-  const long long left = end - it;
-  s.j1 = static_cast<int>(min(static_cast<long long>(n_kv), s.j0 + left));
-  return s;
-}
+// Walks one CTA's segments in order; every role of the CTA walks the same list.
+struct Cursor {
+  int c, round, tail;
+  long long it, end;
+  __device__ __forceinline__ Cursor(const Schedule& s, int c_)
+      : c(c_), round(0), tail(0), it(s.begin(c_)), end(s.begin(c_ + 1)) {}
+  __device__ __forceinline__ bool next(const Schedule& s, Segment& sg) {
+    if (round < s.dp_rounds) {
+      sg.u = round * s.G + c;
+      sg.j0 = 0;
+      sg.j1 = s.n_kv;
+      sg.tail = -1;
+      ++round;
+      return true;
+    }
+    if (it >= end) return false;
+    sg.u = static_cast<int>(it / s.n_kv);
+    sg.j0 = static_cast<int>(it - static_cast<long long>(sg.u) * s.n_kv);
+    sg.j1 = static_cast<int>(min(static_cast<long long>(s.n_kv), sg.j0 + (end - it)));
+    sg.tail = tail++;
+    it += sg.j1 - sg.j0;
+    return true;
+  }
+};
 
 // Warp-uniform wait result: tcgen05.ld/st are warp-collective, so a warp
 // either proceeds as a whole or stops as a whole.
@@ -124,9 +156,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_kv = args.n_kv;
-  const Schedule sched{static_cast<long long>(args.n_units) * n_kv, static_cast<int>(gridDim.x), n_kv};
-  const long long it_begin = sched.begin(blockIdx.x);
-  const long long it_end = sched.begin(blockIdx.x + 1);
+  const Schedule sched(args.n_units, static_cast<int>(gridDim.x), n_kv);
   const bool convert_v = args.in_fmt == kBF16;
 
   auto sQ = [&](int i) { return smem + AttnSmem::kQ + i * kTileBytes; };
@@ -176,9 +206,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tma_prefetch_desc(&tm_v);
       int rg = 0, seg = 0;
       bool ok = true;
-      for (long long it = it_begin; it < it_end && ok; ++seg) {
-        const Segment sg = segment_at(it, it_end, n_kv);
-        it += sg.j1 - sg.j0;
+      Cursor cur(sched, blockIdx.x);
+      Segment sg;
+      for (; ok && cur.next(sched, sg); ++seg) {
         const int bh = sg.u / args.n_pairs;
         const int qt0 = 2 * (sg.u - bh * args.n_pairs);
         if (seg > 0) {
@@ -215,7 +245,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp walks the loop (waits and operand arithmetic are
+    // warp-uniform); one elected lane issues each tcgen05 instruction.
+    {
       const uint32_t fmt = static_cast<uint32_t>(args.in_fmt);
       const uint32_t id_qk = idesc_f16(kBlockM, BN, fmt, fmt, 0, 0);
       const uint32_t id_pv = idesc_f16(kBlockM, kHeadDim, kF16, kF16, 0, 1);
@@ -230,91 +262,95 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       auto issue_qk = [&](int i, int s) {
         const uint64_t a = d_q + i * kQStep, b = d_k + s * kStageStep;
         #pragma unroll
-        for (int k = 0; k < 4; ++k) umma_ss(tbase + 128 * i, a + 2 * k, b + 2 * k, id_qk, k > 0);
+        for (int k = 0; k < 4; ++k) umma_ss_w(tbase + 128 * i, a + 2 * k, b + 2 * k, id_qk, k > 0);
       };
       auto issue_pv = [&](int i, int s, bool acc) {
         const uint64_t b = d_v + s * kStageStep;
         #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
-          umma_ts(tbase + 384 + 64 * i, tbase + 256 + 64 * i + 8 * k, b + 128 * k, id_pv,
+          umma_ts_w(tbase + 384 + 64 * i, tbase + 256 + 64 * i + 8 * k, b + 128 * k, id_pv,
                   (acc || k > 0) ? 1u : 0u);
       };
       int rg = 0, gi = 0, seg = 0;
       bool ok = true;
-      for (long long it = it_begin; it < it_end && ok; ++seg) {
-        const Segment sg = segment_at(it, it_end, n_kv);
-        it += sg.j1 - sg.j0;
+      Cursor cur(sched, blockIdx.x);
+      Segment sg;
+      for (; ok && cur.next(sched, sg); ++seg) {
         const int len = sg.j1 - sg.j0;
-        ok = mbar_wait(&bars[kBarQFull], seg & 1, abort_flag, status);
+        ok = warp_all(mbar_wait(&bars[kBarQFull], seg & 1, abort_flag, status));
         if (!ok) break;
         if (FUSED) {
           if (seg > 0) {
-            ok = mbar_wait(&bars[kBarEpiDone], (seg - 1) & 1, abort_flag, status);
+            ok = warp_all(mbar_wait(&bars[kBarEpiDone], (seg - 1) & 1, abort_flag, status));
             if (!ok) break;
           }
           const int s = rg % kStages;
-          ok = mbar_wait(&bars[kBarKVFull + s], (rg / kStages) & 1, abort_flag, status);
+          ok = warp_all(mbar_wait(&bars[kBarKVFull + s], (rg / kStages) & 1, abort_flag, status));
           if (!ok) break;
           tc_fence_after();
           for (int i = 0; i < 2; ++i) {
             const uint64_t a = d_q + i * kQStep, b = d_k + s * kStageStep;
             #pragma unroll
-            for (int k = 0; k < 4; ++k) umma_ss(tbase + 256 * i, a + 2 * k, b + 2 * k, id_g, k > 0);
+            for (int k = 0; k < 4; ++k) umma_ss_w(tbase + 256 * i, a + 2 * k, b + 2 * k, id_g, k > 0);
           }
-          umma_commit(&bars[kBarGFull]);
-          umma_commit(&bars[kBarKVEmpty + s]);
+          umma_commit_w(&bars[kBarGFull]);
+          umma_commit_w(&bars[kBarKVEmpty + s]);
           ++rg;
-          ok = mbar_wait(&bars[kBarGFree], seg & 1, abort_flag, status);
+          ok = warp_all(mbar_wait(&bars[kBarGFree], seg & 1, abort_flag, status));
           if (!ok) break;
           tc_fence_after();
         }
         {
           const int s = rg % kStages;
-          ok = mbar_wait(&bars[kBarKVFull + s], (rg / kStages) & 1, abort_flag, status);
+          ok = warp_all(mbar_wait(&bars[kBarKVFull + s], (rg / kStages) & 1, abort_flag, status));
           if (!ok) break;
           tc_fence_after();
           issue_qk(0, s);
-          umma_commit(&bars[kBarSFull + 0]);
+          umma_commit_w(&bars[kBarSFull + 0]);
           issue_qk(1, s);
-          umma_commit(&bars[kBarSFull + 1]);
+          umma_commit_w(&bars[kBarSFull + 1]);
         }
         for (int jj = 0; jj < len && ok; ++jj, ++rg, ++gi) {
           const int s = rg % kStages, ph = (rg / kStages) & 1;
           const int sn = (rg + 1) % kStages, phn = ((rg + 1) / kStages) & 1;
           const bool more = jj + 1 < len;
           if (convert_v) {
-            ok = mbar_wait(&bars[kBarVReady + s], ph, abort_flag, status);
+            ok = warp_all(mbar_wait(&bars[kBarVReady + s], ph, abort_flag, status));
             if (!ok) break;
           }
-          ok = mbar_wait(&bars[kBarPFull + 0], gi & 1, abort_flag, status);
+          // Once softmax i has written P_i(j) (and so finished reading S_i),
+          // the next S_i goes first: the softmax can start on it while PV_i(j)
+          // runs, and waits for PV_i(j) only before it next writes P_i or O_i.
+          ok = warp_all(mbar_wait(&bars[kBarPFull + 0], gi & 1, abort_flag, status));
           if (!ok) break;
           tc_fence_after();
-          issue_pv(0, s, jj > 0);
-          umma_commit(&bars[kBarODone + 0]);
           if (more) {
-            ok = mbar_wait(&bars[kBarKVFull + sn], phn, abort_flag, status);
+            ok = warp_all(mbar_wait(&bars[kBarKVFull + sn], phn, abort_flag, status));
             if (!ok) break;
             tc_fence_after();
             issue_qk(0, sn);
-            umma_commit(&bars[kBarSFull + 0]);
+            umma_commit_w(&bars[kBarSFull + 0]);
           }
-          ok = mbar_wait(&bars[kBarPFull + 1], gi & 1, abort_flag, status);
+          issue_pv(0, s, jj > 0);
+          umma_commit_w(&bars[kBarODone + 0]);
+          ok = warp_all(mbar_wait(&bars[kBarPFull + 1], gi & 1, abort_flag, status));
           if (!ok) break;
           tc_fence_after();
-          issue_pv(1, s, jj > 0);
-          umma_commit(&bars[kBarODone + 1]);
           if (more) {
             issue_qk(1, sn);
-            umma_commit(&bars[kBarSFull + 1]);
+            umma_commit_w(&bars[kBarSFull + 1]);
           } else {
-            umma_commit(&bars[kBarQEmpty]);  // no more reads of this segment's Q
+            umma_commit_w(&bars[kBarQEmpty]);  // no more reads of this segment's Q
           }
-          umma_commit(&bars[kBarKVEmpty + s]);
+          issue_pv(1, s, jj > 0);
+          umma_commit_w(&bars[kBarODone + 1]);
+          umma_commit_w(&bars[kBarKVEmpty + s]);
         }
       }
       // Drain: every MMA issued above completes before TMEM is released.
-      umma_commit(&bars[kBarMmaDone]);
+      umma_commit_w(&bars[kBarMmaDone]);
       mbar_wait_budget(&bars[kBarMmaDone], 0, kWaitBudgetCycles);
+      __syncwarp();
     }
   } else if (warp < 4) {
     // ------------------------------------------------------------ bf16 -> fp16 V conversion
@@ -324,9 +360,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const int ct = threadIdx.x - 64;
       int rg = 0;
       bool ok = true;
-      for (long long it = it_begin; it < it_end && ok;) {
-        const Segment sg = segment_at(it, it_end, n_kv);
-        it += sg.j1 - sg.j0;
+      Cursor cur(sched, blockIdx.x);
+      Segment sg;
+      while (ok && cur.next(sched, sg)) {
         for (int j = FUSED ? sg.j0 - 1 : sg.j0; j < sg.j1; ++j, ++rg) {
           const int s = rg % kStages;
           ok = mbar_wait(&bars[kBarKVFull + s], (rg / kStages) & 1, abort_flag, status);
@@ -368,9 +404,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
     int gi = 0, seg = 0, pseg = 0;
     bool ok = true;
-    for (long long it = it_begin; it < it_end && ok; ++seg) {
-      const Segment sg = segment_at(it, it_end, n_kv);
-      it += sg.j1 - sg.j0;
+    Cursor cur(sched, blockIdx.x);
+    Segment sg;
+    for (; ok && cur.next(sched, sg); ++seg) {
       const int bh = sg.u / args.n_pairs;
       const int qt = 2 * (sg.u - bh * args.n_pairs) + wg;
       const int n = qt * kBlockM + r;
@@ -443,6 +479,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int g = 0; g < KHT; ++g) mt = fmaxf(mt, gm[g] + bhv[g]);
         return mt;
       };
+      // Waits (once, warp-uniformly) until PV of the previous key tile has
+      // read P and written O; needed before P or O is next written.
+      bool pv_pending = false;
+      auto wait_pv = [&]() {
+        if (pv_pending) {
+          ok = warp_all(mbar_wait(&bars[kBarODone + wg], (gi - 1) & 1, abort_flag, status)) && ok;
+          tc_fence_after();
+          pv_pending = false;
+        }
+      };
       // p = 2^(x - m) for the whole tile into P (fp16, TMEM); returns the row sum.
       auto exp_pass = [&](const float (&bhv)[KHT], float m) -> float2 {
         float2 off[KHT];
@@ -467,6 +513,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
               pk[k / 2] = pack_f16x2(p.x, p.y);
             }
           }
+          if (cb == 0) wait_pv();
           if (kBlk == 32 && BN - cb >= 32) tmem_st16(tP + cb / 2, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
           else tmem_st8(tP + cb / 2, *reinterpret_cast<uint32_t(*)[8]>(&pk[0]));
         }
@@ -484,12 +531,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         ok = warp_all(mbar_wait(&bars[kBarSFull + wg], gi & 1, abort_flag, status));
         if (!ok) break;
         tc_fence_after();
-        if (j > sg.j0) {
-          // PV of the previous tile has finished reading P and writing O
-          ok = warp_all(mbar_wait(&bars[kBarODone + wg], (gi - 1) & 1, abort_flag, status));
-          if (!ok) break;
-          tc_fence_after();
-        }
+        pv_pending = j > sg.j0;
         float bhv[KHT];
         #pragma unroll
         for (int g = 0; g < KHT; ++g) bhv[g] = bh_row[j * KHT + g];
@@ -505,6 +547,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (j == sg.j0) {
             m_used = mt;
           } else {
+            wait_pv();
             const float m_new = fmaxf(m_used, mt);
             const float alpha = ex2_approx(m_used - m_new);
             m_used = m_new;
@@ -523,6 +566,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           ts = exp_pass(bhv, m_used);
         }
         lsum = fadd2(lsum, ts);
+        if (!ok) break;
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&bars[kBarPFull + wg]);
@@ -551,13 +595,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (!sg.full(n_kv)) {
         // Partial unit: publish (O, m, l) and let the last CTA of the unit merge.
         const int c = blockIdx.x;
-        const int slot = (seg == 0) ? 2 * c : 2 * c + 1;
+        const int slot = (sg.tail == 0) ? 2 * c : 2 * c + 1;
         float* ws = args.partials + (static_cast<size_t>(slot) * 2 + wg) * kBlockM * kSlotRow + r * kSlotRow;
         #pragma unroll
         for (int q4 = 0; q4 < 16; ++q4)
           __stcg(reinterpret_cast<float4*>(ws) + q4, make_float4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]));
         __stcg(reinterpret_cast<float2*>(ws + 64), make_float2(m, l));
-        __threadfence();
+        // mbarrier arrive/wait order these writes before the elected thread's
+        // GPU-scope release below (release is cumulative)
         mbar_arrive(&bars[kBarPartWritten]);
         const long long u0 = static_cast<long long>(sg.u) * n_kv;
         const int c_first = sched.cta_of(u0);
@@ -566,12 +611,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           bool w_ok = mbar_wait(&bars[kBarPartWritten], pseg & 1, abort_flag, status);
           int last = 0;
           if (w_ok) {
-            const int old = atomicAdd(args.counters + sg.u, 1);
+            const int old = atomic_add_acq_rel_gpu(args.counters + sg.u, 1);
             last = old == nseg - 1;
-            if (last) {
-              __threadfence();
-              args.counters[sg.u] = 0;  // ready for the next launch
-            }
+            if (last) args.counters[sg.u] = 0;  // ready for the next launch (stream-ordered)
           }
           *merge_flag = last;
           mbar_arrive(&bars[kBarMergeGo]);
