@@ -43,7 +43,7 @@ struct AttnSmem {
   static constexpr int kBars = kBias + kBiasBytes;
   static constexpr int kNumBars = 32;
   static constexpr int kMisc = kBars + kNumBars * 8;             // tmem slot, abort flag, merge flag
-  static constexpr int kTotal = kMisc + 16;
+  static constexpr int kTotal = kMisc + 32;
   static constexpr int kAlloc = kTotal + 1024;                   // slack for 1 KB alignment
 };
 static_assert(AttnSmem::kAlloc <= 232448, "shared memory budget");
@@ -62,9 +62,9 @@ enum : int {
   kBarGFree = kBarGFull + 1,
   kBarEpiDone = kBarGFree + 1,
   kBarStg = kBarEpiDone + 1,          // + tile
-  kBarPartWritten = kBarStg + 2,
-  kBarMergeGo = kBarPartWritten + 1,
-  kBarMmaDone = kBarMergeGo + 1,
+  kBarPartWritten = kBarStg + 2,     // + tile
+  kBarMergeGo = kBarPartWritten + 2,  // + tile
+  kBarMmaDone = kBarMergeGo + 2,
   kBarCount = kBarMmaDone + 1
 };
 static_assert(kBarCount <= AttnSmem::kNumBars, "barrier slots");
@@ -135,7 +135,7 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   return pack_f16x2(lo, hi);
 }
 
-template <int WP, bool FUSED>
+template <int WP, bool FUSED, bool BF16>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     relpos_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_th,
@@ -150,14 +150,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + AttnSmem::kBars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + AttnSmem::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + AttnSmem::kMisc + 4);
-  volatile int* merge_flag = reinterpret_cast<volatile int*>(smem + AttnSmem::kMisc + 8);
+  volatile int* merge_flag = reinterpret_cast<volatile int*>(smem + AttnSmem::kMisc + 8);  // [2]
   int* status = args.status;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_kv = args.n_kv;
   const Schedule sched(args.n_units, static_cast<int>(gridDim.x), n_kv);
-  const bool convert_v = args.in_fmt == kBF16;
+  constexpr bool convert_v = BF16;  // P is fp16, so bf16 V tiles are converted to fp16 on chip
 
   auto sQ = [&](int i) { return smem + AttnSmem::kQ + i * kTileBytes; };
   auto sK = [&](int s) { return smem + AttnSmem::kRing + s * AttnSmem::kStageBytes; };
@@ -165,7 +165,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    *merge_flag = 0;
+    merge_flag[0] = 0;
+    merge_flag[1] = 0;
     mbar_init(&bars[kBarQFull], 1);
     mbar_init(&bars[kBarQEmpty], 1);
     for (int s = 0; s < kStages; ++s) {
@@ -183,8 +184,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     mbar_init(&bars[kBarEpiDone], 2 * kBlockM);
     mbar_init(&bars[kBarStg + 0], kBlockM);
     mbar_init(&bars[kBarStg + 1], kBlockM);
-    mbar_init(&bars[kBarPartWritten], 2 * kBlockM);
-    mbar_init(&bars[kBarMergeGo], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[kBarPartWritten + i], kBlockM);
+      mbar_init(&bars[kBarMergeGo + i], 1);
+    }
     mbar_init(&bars[kBarMmaDone], 1);
     fence_mbar_init();
   }
@@ -248,10 +251,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // The whole warp walks the loop (waits and operand arithmetic are
     // warp-uniform); one elected lane issues each tcgen05 instruction.
     {
-      const uint32_t fmt = static_cast<uint32_t>(args.in_fmt);
-      const uint32_t id_qk = idesc_f16(kBlockM, BN, fmt, fmt, 0, 0);
-      const uint32_t id_pv = idesc_f16(kBlockM, kHeadDim, kF16, kF16, 0, 1);
-      const uint32_t id_g = idesc_f16(kBlockM, 256, fmt, fmt, 0, 0);
+      constexpr uint32_t fmt = BF16 ? kBF16 : kF16;
+      constexpr uint32_t id_qk = idesc_f16(kBlockM, BN, fmt, fmt, 0, 0);
+      constexpr uint32_t id_pv = idesc_f16(kBlockM, kHeadDim, kF16, kF16, 0, 1);
+      constexpr uint32_t id_g = idesc_f16(kBlockM, 256, fmt, fmt, 0, 0);
       // Descriptors differ only in their 14-bit start-address field (address / 16),
       // which stays below 2^14 for any shared-memory address, so offsets are
       // added to one base descriptor per operand.
@@ -269,7 +272,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
           umma_ts_w(tbase + 384 + 64 * i, tbase + 256 + 64 * i + 8 * k, b + 128 * k, id_pv,
-                  (acc || k > 0) ? 1u : 0u);
+                    (acc || k > 0) ? 1u : 0u);
       };
       int rg = 0, gi = 0, seg = 0;
       bool ok = true;
@@ -532,9 +535,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (!ok) break;
         tc_fence_after();
         pv_pending = j > sg.j0;
+        const int kh0 = j * KHT;
         float bhv[KHT];
         #pragma unroll
-        for (int g = 0; g < KHT; ++g) bhv[g] = bh_row[j * KHT + g];
+        for (int g = 0; g < KHT; ++g) bhv[g] = bh_row[kh0 + g];
 
         float2 ts = make_float2(0.f, 0.f);
         bool exact = j == sg.j0;
@@ -573,109 +577,111 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       if (!ok) break;
 
-      // epilogue: O (fp32, unnormalised) out of TMEM
+      // epilogue: O (fp32, unnormalised) streamed out of TMEM 16 columns at a time
       ok = warp_all(mbar_wait(&bars[kBarODone + wg], (gi - 1) & 1, abort_flag, status));
       if (!ok) break;
       tc_fence_after();
-      float o[kHeadDim];
-      #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v16[16];
-        tmem_ld16(tO + 16 * c, v16);
-        tmem_wait_ld();
+      const float l = lsum.x + lsum.y;
+      uint8_t* orow = reinterpret_cast<uint8_t*>(args.out) +
+                      (static_cast<size_t>(bh) * N + (row_valid ? n : 0)) * kHeadDim * (args.out_fmt == kF32 ? 4 : 2);
+      auto store16 = [&](int c0, const float (&v)[16], float scale) {
+        if (!row_valid) return;
+        if (args.out_fmt == kF32) {
+          float4* dst = reinterpret_cast<float4*>(orow) + c0 / 4;
+          #pragma unroll
+          for (int q = 0; q < 4; ++q)
+            dst[q] = make_float4(v[4 * q] * scale, v[4 * q + 1] * scale, v[4 * q + 2] * scale, v[4 * q + 3] * scale);
+        } else {
+          uint32_t w[8];
+          #pragma unroll
+          for (int k = 0; k < 8; ++k)
+            w[k] = args.out_fmt == kBF16 ? pack_bf16x2(v[2 * k] * scale, v[2 * k + 1] * scale)
+                                         : pack_f16x2(v[2 * k] * scale, v[2 * k + 1] * scale);
+          uint4* dst = reinterpret_cast<uint4*>(orow) + c0 / 8;
+          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+      };
+      if (sg.full(n_kv)) {
+        const float inv_l = 1.0f / l;
         #pragma unroll
-        for (int k = 0; k < 16; ++k) o[16 * c + k] = __uint_as_float(v16[k]);
-      }
-      tc_fence_before();
-      if (FUSED) mbar_arrive(&bars[kBarEpiDone]);
-      float l = lsum.x + lsum.y;
-      float m = m_used;
-
-      bool store = true;
-      if (!sg.full(n_kv)) {
-        // Partial unit: publish (O, m, l) and let the last CTA of the unit merge.
+        for (int c = 0; c < 4; ++c) {
+          uint32_t u[16];
+          tmem_ld16(tO + 16 * c, u);
+          tmem_wait_ld();
+          float v[16];
+          #pragma unroll
+          for (int k = 0; k < 16; ++k) v[k] = __uint_as_float(u[k]);
+          store16(16 * c, v, inv_l);
+        }
+        tc_fence_before();
+        if (FUSED) mbar_arrive(&bars[kBarEpiDone]);
+      } else {
+        // Cut unit: publish this warpgroup's (O, m, l); the warpgroup that
+        // completes the unit's second segment (here or in another CTA) merges.
+        // Each query tile has its own counter, so the two warpgroups never
+        // wait for each other.  The schedule cuts a unit at most once.
         const int c = blockIdx.x;
         const int slot = (sg.tail == 0) ? 2 * c : 2 * c + 1;
         float* ws = args.partials + (static_cast<size_t>(slot) * 2 + wg) * kBlockM * kSlotRow + r * kSlotRow;
         #pragma unroll
-        for (int q4 = 0; q4 < 16; ++q4)
-          __stcg(reinterpret_cast<float4*>(ws) + q4, make_float4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]));
-        __stcg(reinterpret_cast<float2*>(ws + 64), make_float2(m, l));
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t u[16];
+          tmem_ld16(tO + 16 * cc, u);
+          tmem_wait_ld();
+          #pragma unroll
+          for (int q = 0; q < 4; ++q)
+            __stcg(reinterpret_cast<float4*>(ws + 16 * cc) + q,
+                   make_float4(__uint_as_float(u[4 * q]), __uint_as_float(u[4 * q + 1]),
+                               __uint_as_float(u[4 * q + 2]), __uint_as_float(u[4 * q + 3])));
+        }
+        __stcg(reinterpret_cast<float2*>(ws + 64), make_float2(m_used, l));
+        tc_fence_before();
+        if (FUSED) mbar_arrive(&bars[kBarEpiDone]);
         // mbarrier arrive/wait order these writes before the elected thread's
         // GPU-scope release below (release is cumulative)
-        mbar_arrive(&bars[kBarPartWritten]);
+        mbar_arrive(&bars[kBarPartWritten + wg]);
         const long long u0 = static_cast<long long>(sg.u) * n_kv;
         const int c_first = sched.cta_of(u0);
-        const int nseg = sched.cta_of(u0 + n_kv - 1) - c_first + 1;
-        if (wg == 0 && r == 0) {
-          bool w_ok = mbar_wait(&bars[kBarPartWritten], pseg & 1, abort_flag, status);
+        if (r == 0) {
+          const bool w_ok = mbar_wait(&bars[kBarPartWritten + wg], pseg & 1, abort_flag, status);
           int last = 0;
           if (w_ok) {
-            const int old = atomic_add_acq_rel_gpu(args.counters + sg.u, 1);
-            last = old == nseg - 1;
-            if (last) args.counters[sg.u] = 0;  // ready for the next launch (stream-ordered)
+            int* counter = args.counters + 2 * static_cast<size_t>(sg.u) + wg;
+            const int old = atomic_add_acq_rel_gpu(counter, 1);
+            last = old == 1;
+            if (last) *counter = 0;  // ready for the next launch (stream-ordered)
           }
-          *merge_flag = last;
-          mbar_arrive(&bars[kBarMergeGo]);
+          merge_flag[wg] = last;
+          mbar_arrive(&bars[kBarMergeGo + wg]);
         }
-        ok = mbar_wait(&bars[kBarMergeGo], pseg & 1, abort_flag, status);
+        ok = warp_all(mbar_wait(&bars[kBarMergeGo + wg], pseg & 1, abort_flag, status));
         ++pseg;
         if (!ok) break;
-        store = *merge_flag != 0;
-        if (store) {
-          // merge the unit's segments: rescale each to the largest max
-          const bool first_is_first = sched.begin(c_first) == u0;
-          float mm[4], ll[4];
-          const float* rowp[4];
-          float mstar = NEG_INF;
-          const int ns = min(nseg, 4);
-          for (int s = 0; s < ns; ++s) {
-            const int cs = c_first + s;
-            const int sl = (s > 0 || first_is_first) ? 2 * cs : 2 * cs + 1;
-            rowp[s] = args.partials + (static_cast<size_t>(sl) * 2 + wg) * kBlockM * kSlotRow + r * kSlotRow;
-            const float2 ml = __ldcg(reinterpret_cast<const float2*>(rowp[s] + 64));
-            mm[s] = ml.x;
-            ll[s] = ml.y;
-            mstar = fmaxf(mstar, mm[s]);
-          }
+        if (merge_flag[wg]) {
+          // the unit's two segments, rescaled to the larger running max
+          const int sl0 = (sched.begin(c_first) == u0) ? 2 * c_first : 2 * c_first + 1;
+          const int sl1 = 2 * (c_first + 1);
+          const float* pa = args.partials + (static_cast<size_t>(sl0) * 2 + wg) * kBlockM * kSlotRow + r * kSlotRow;
+          const float* pb = args.partials + (static_cast<size_t>(sl1) * 2 + wg) * kBlockM * kSlotRow + r * kSlotRow;
+          const float2 ma = __ldcg(reinterpret_cast<const float2*>(pa + 64));
+          const float2 mb = __ldcg(reinterpret_cast<const float2*>(pb + 64));
+          const float mstar = fmaxf(ma.x, mb.x);
+          const float fa = ex2_approx(ma.x - mstar), fb = ex2_approx(mb.x - mstar);
+          const float inv_l = 1.0f / (fa * ma.y + fb * mb.y);
           #pragma unroll
-          for (int k = 0; k < kHeadDim; ++k) o[k] = 0.f;
-          l = 0.f;
-          for (int s = 0; s < ns; ++s) {
-            const float a = ex2_approx(mm[s] - mstar);
-            l += a * ll[s];
+          for (int cc = 0; cc < 4; ++cc) {
+            float v[16];
             #pragma unroll
-            for (int q4 = 0; q4 < 16; ++q4) {
-              const float4 v4 = __ldcg(reinterpret_cast<const float4*>(rowp[s]) + q4);
-              o[4 * q4] += a * v4.x;
-              o[4 * q4 + 1] += a * v4.y;
-              o[4 * q4 + 2] += a * v4.z;
-              o[4 * q4 + 3] += a * v4.w;
+            for (int q = 0; q < 4; ++q) {
+              const float4 xa = __ldcg(reinterpret_cast<const float4*>(pa + 16 * cc) + q);
+              const float4 xb = __ldcg(reinterpret_cast<const float4*>(pb + 16 * cc) + q);
+              v[4 * q] = fa * xa.x + fb * xb.x;
+              v[4 * q + 1] = fa * xa.y + fb * xb.y;
+              v[4 * q + 2] = fa * xa.z + fb * xb.z;
+              v[4 * q + 3] = fa * xa.w + fb * xb.w;
             }
-          }
-        }
-      }
-      if (store && row_valid) {
-        const float inv_l = 1.0f / l;
-        uint8_t* orow = reinterpret_cast<uint8_t*>(args.out) +
-                        (static_cast<size_t>(bh) * N + n) * kHeadDim * (args.out_fmt == kF32 ? 4 : 2);
-        if (args.out_fmt == kF32) {
-          float4* dst = reinterpret_cast<float4*>(orow);
-          #pragma unroll
-          for (int q4 = 0; q4 < 16; ++q4)
-            dst[q4] = make_float4(o[4 * q4] * inv_l, o[4 * q4 + 1] * inv_l, o[4 * q4 + 2] * inv_l,
-                                  o[4 * q4 + 3] * inv_l);
-        } else {
-          uint4* dst = reinterpret_cast<uint4*>(orow);
-          #pragma unroll
-          for (int q8 = 0; q8 < 8; ++q8) {
-            uint32_t w[4];
-            #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float a = o[8 * q8 + 2 * k] * inv_l, b = o[8 * q8 + 2 * k + 1] * inv_l;
-              w[k] = args.out_fmt == kBF16 ? pack_bf16x2(a, b) : pack_f16x2(a, b);
-            }
-            dst[q8] = make_uint4(w[0], w[1], w[2], w[3]);
+            store16(16 * cc, v, inv_l);
           }
         }
       }

@@ -196,7 +196,7 @@ Plan make_plan(int BH, int H, int W, int sms) {
   // so a unit is cut into at most two segments.
   p.split = sms > 0 && p.n_units > sms && p.n_units % sms != 0;
   p.ctas = p.split ? sms : p.n_units;
-  p.counters_bytes = align256(static_cast<size_t>(p.n_units) * sizeof(int));
+  p.counters_bytes = align256(static_cast<size_t>(p.n_units) * 2 * sizeof(int));  // one per query tile
   p.partial_bytes = static_cast<size_t>(2) * sms * 2 * kBlockM * kSlotRow * sizeof(float);
   return p;
 }
@@ -265,7 +265,7 @@ dera_status run_attention(const void* q, const void* k, const void* v, const voi
     args.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.counters_bytes);
     // the counters must start at zero; the kernel leaves them at zero too,
     // but a launch that stopped early would not
-    if (cudaMemsetAsync(args.counters, 0, static_cast<size_t>(plan.n_units) * sizeof(int), s) != cudaSuccess)
+    if (cudaMemsetAsync(args.counters, 0, static_cast<size_t>(plan.n_units) * 2 * sizeof(int), s) != cudaSuccess)
       return DERA_ERR_CUDA;
   }
   cudaError_t e;
