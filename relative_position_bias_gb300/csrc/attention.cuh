@@ -493,34 +493,45 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
       };
       // p = 2^(x - m) for the whole tile into P (fp16, TMEM); returns the row sum.
+      // S is read in 16-column blocks with the next block always in flight,
+      // so the TMEM load latency overlaps the arithmetic of the current one;
+      // four partial sums keep the dependency chains short.
       auto exp_pass = [&](const float (&bhv)[KHT], float m) -> float2 {
         float2 off[KHT];
         #pragma unroll
         for (int g = 0; g < KHT; ++g) off[g] = make_float2(bhv[g] - m, bhv[g] - m);
-        float2 ts = make_float2(0.f, 0.f);
-        #pragma unroll
-        for (int cb = 0; cb < BN; cb += kBlk) {
-          uint32_t u[kBlk];
-          load_block(cb, u);
-          uint32_t pk[kBlk / 2];
+        float2 ts[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                        make_float2(0.f, 0.f)};
+        uint32_t ua[16], ub[16];
+        auto block = [&](int cb, const uint32_t (&u)[16]) {
+          uint32_t pk[8];
           #pragma unroll
-          for (int k = 0; k < kBlk; k += 2) {
+          for (int k = 0; k < 16; k += 2) {
             const int col = cb + k;
-            if (col < BN) {
-              const int g = col / WP, kw = col % WP;
-              float2 t = ffma2(make_float2(__uint_as_float(u[k]), __uint_as_float(u[k + 1])), sl2v,
-                               make_float2(bw[kw], bw[kw + 1]));
-              t = fadd2(t, off[g]);
-              const float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
-              ts = fadd2(ts, p);
-              pk[k / 2] = pack_f16x2(p.x, p.y);
-            }
+            const int g = col / WP, kw = col % WP;
+            float2 t = ffma2(make_float2(__uint_as_float(u[k]), __uint_as_float(u[k + 1])), sl2v,
+                             make_float2(bw[kw], bw[kw + 1]));
+            t = fadd2(t, off[g]);
+            const float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+            ts[(k / 2) & 3] = fadd2(ts[(k / 2) & 3], p);
+            pk[k / 2] = pack_f16x2(p.x, p.y);
           }
           if (cb == 0) wait_pv();
-          if (kBlk == 32 && BN - cb >= 32) tmem_st16(tP + cb / 2, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-          else tmem_st8(tP + cb / 2, *reinterpret_cast<uint32_t(*)[8]>(&pk[0]));
+          tmem_st8(tP + cb / 2, pk);
+        };
+        tmem_ld16(tS, ua);
+        #pragma unroll
+        for (int cb = 0; cb < BN; cb += 32) {
+          tmem_wait_ld();
+          if (cb + 16 < BN) tmem_ld16(tS + cb + 16, ub);
+          block(cb, ua);
+          if (cb + 16 < BN) {
+            tmem_wait_ld();
+            if (cb + 32 < BN) tmem_ld16(tS + cb + 32, ua);
+            block(cb + 16, ub);
+          }
         }
-        return ts;
+        return fadd2(fadd2(ts[0], ts[1]), fadd2(ts[2], ts[3]));
       };
 
       // Online softmax over the segment's key tiles.  The first tile takes the
