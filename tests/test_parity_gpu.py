@@ -142,8 +142,58 @@ def test_fused_parity(name, split):
     o32 = rpb.fused(*args, out_dtype=torch.float32, workspace=ws)
     o16 = rpb.fused(*args, workspace=ws)
     torch.cuda.synchronize()
+    # every row, not only the sampled ones, must be finite
+    assert bool(torch.isfinite(o32).all()) and bool(torch.isfinite(o16).all()), f"fused {name}: non-finite output"
     heads, rows, want = _oracle_full_or_rows(w, _f64(x), "fused")
     check_out(_select(o32, heads, rows), want, _select(o16, heads, rows), what=f"fused {name}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("case", ["inf", "clamp", "raise"])
+@pytest.mark.parametrize("entry", ["fused", "attention"])
+def test_late_large_scores(entry, case, dtype):
+    """Scores in a late key tile far above everything before them in the row.
+
+    The kernel exponentiates each tile against the row maximum it has seen so
+    far and stores P in fp16, so these rows exercise its overflow handling:
+    "inf": one key 150 (base-2 units) above the rest, whose 2^x overflows even
+    fp32; "clamp": one key about 18 above the running maximum (p beyond the
+    fp16 range); "raise": a whole tile about 12 above it (the row sum passes
+    2^15 with every p still in range).  All must match the oracle."""
+    base = I.WORKLOADS["grid16"] if dtype == "bf16" else I.WORKLOADS["ragged40"]
+    w = base.with_grid(32, 32, B=1, heads=2)
+    x = I.make_inputs(w, seed=11)
+    tdt = x["q"].dtype
+    q, k = x["q"].float(), x["k"].float()
+    q[..., 0] = 2.0
+    if case == "inf":
+        k[:, 677, :] = 0.0
+        k[:, 677, 0] = 416.0   # q.k = 832: 150 in base-2 units after scale * log2(e)
+    elif case == "clamp":
+        k[:, 677, :] = 0.0
+        k[:, 677, 0] = 60.0    # about 21.6 in base-2 units
+    else:
+        k[:, 640:768, 0] += 33.0  # about +11.9 for the whole key tile 5
+    x["q"], x["k"] = q.to(tdt), k.to(tdt)
+    x["rel_pos_h"] = (x["rel_pos_h"].float() * 0.1).to(tdt)
+    x["rel_pos_w"] = (x["rel_pos_w"].float() * 0.1).to(tdt)
+    d, f = _dev(x), _f64(x)
+    if entry == "fused":
+        args = (d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W, w.scale)
+        o32 = rpb.fused(*args, out_dtype=torch.float32)
+        o16 = rpb.fused(*args)
+        torch.cuda.synchronize()
+        want = oracle.fused(f["q"], f["k"], f["v"], f["rel_pos_h"], f["rel_pos_w"], w.H, w.W, w.scale)
+    else:
+        rh, rw = oracle.project(f["q"], f["rel_pos_h"], f["rel_pos_w"], w.H, w.W)
+        rh32, rw32 = torch.from_numpy(rh).float(), torch.from_numpy(rw).float()
+        args = (d["q"], d["k"], d["v"], rh32.cuda(), rw32.cuda(), w.H, w.W, w.scale)
+        o32 = rpb.attention(*args, out_dtype=torch.float32)
+        o16 = rpb.attention(*args)
+        torch.cuda.synchronize()
+        want = oracle.attention(f["q"], f["k"], f["v"], rh32.double().numpy(), rw32.double().numpy(), w.H, w.W,
+                                w.scale)
+    check_out(o32, want, o16, what=f"late large scores {entry} {case} {dtype}")
 
 
 @pytest.mark.parametrize("entry", ["fused", "attention"])
