@@ -406,6 +406,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const float2 sl2v = make_float2(sl2, sl2);
 
     int gi = 0, seg = 0, pseg = 0;
+    uint32_t stg_phase = 0;  // completed phases of this warpgroup's staging barrier
+    // Warpgroup-wide barrier on the staging mbarrier (all 128 threads arrive, then wait).
+    auto wg_sync = [&]() -> bool {
+      mbar_arrive(&bars[kBarStg + wg]);
+      const bool w = mbar_wait(&bars[kBarStg + wg], stg_phase & 1, abort_flag, status);
+      ++stg_phase;
+      return warp_all(w);
+    };
     bool ok = true;
     Cursor cur(sched, blockIdx.x);
     Segment sg;
@@ -427,8 +435,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int kw = 0; kw < WP; ++kw) bw[kw] = (ok && kw < W) ? stg[kw] : NEG_INF;
         // the staging rows (stride kBiasStride) overlap the bias rows (stride HS):
         // every thread of the warpgroup has read its staged row before any bias row is written
-        mbar_arrive(&bars[kBarStg + wg]);
-        ok = warp_all(mbar_wait(&bars[kBarStg + wg], seg & 1, abort_flag, status) && ok);
+        ok = wg_sync() && ok;
         if (ok) {
           skew_row_to_smem(tbase + lane_off + 256 * wg, qh, H, bh_row, kLog2e);
           for (int kh = H; kh < Hpad; ++kh) bh_row[kh] = NEG_INF;
@@ -437,15 +444,49 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_arrive(&bars[kBarGFree]);
         if (!ok) break;
       } else {
-        const size_t row = static_cast<size_t>(bh) * N + n;
+        // The tile's rows of rel_w, then of rel_h, are one contiguous block
+        // each: every warp copies a quarter of the rows into the staging area,
+        // a row per pass with the lanes along it (coalesced), scaled by log2e.
+        // Rows past N read as 0.
+        const size_t row0 = static_cast<size_t>(bh) * N + static_cast<size_t>(qt) * kBlockM;
+        const int nrows = min(kBlockM, N - qt * kBlockM);
+        // Loads for 8 rows go out together before any store (the stores could
+        // alias the source as far as the compiler knows).
+        auto copy_rows = [&](const void* src, int len, int stride) {
+          for (int rb = wq; rb < kBlockM; rb += 32) {
+            float v[8][2];
+            #pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int rr = rb + 4 * u;
+              #pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int c = lane + 32 * h;
+                v[u][h] = (rr < nrows && c < len)
+                              ? load_elem(src, (row0 + rr) * static_cast<size_t>(len) + c, args.bias_fmt)
+                              : 0.f;
+              }
+            }
+            #pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              #pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int c = lane + 32 * h;
+                if (c < len) area[(rb + 4 * u) * stride + c] = kLog2e * v[u][h];
+              }
+            }
+          }
+        };
+        copy_rows(args.rel_w, W, kBiasStride);
+        ok = wg_sync() && ok;
+        const float* stg = area + r * kBiasStride;
         #pragma unroll
-        for (int kw = 0; kw < WP; ++kw)
-          bw[kw] = kw < W ? (row_valid ? kLog2e * load_elem(args.rel_w, row * W + kw, args.bias_fmt) : 0.f)
-                          : NEG_INF;
-        // each thread rewrites only its own bias row, which no other thread reads
-        for (int kh = 0; kh < Hpad; ++kh)
-          bh_row[kh] = kh < H ? (row_valid ? kLog2e * load_elem(args.rel_h, row * H + kh, args.bias_fmt) : 0.f)
-                              : NEG_INF;
+        for (int kw = 0; kw < WP; ++kw) bw[kw] = kw < W ? stg[kw] : NEG_INF;
+        // every thread has its rel_w row before the area is reused for rel_h
+        ok = wg_sync() && ok;
+        copy_rows(args.rel_h, H, HS);
+        ok = wg_sync() && ok;
+        for (int kh = H; kh < Hpad; ++kh) bh_row[kh] = NEG_INF;
+        if (!ok) break;
       }
 
       // S is processed in blocks of kBlk columns (one TMEM load and one wait
