@@ -112,10 +112,23 @@ __global__ void __launch_bounds__(kProjThreads, 1)
       __syncthreads();
       void* dst = part == 0 ? args.rel_h : args.rel_w;
       const size_t base = (static_cast<size_t>(bh) * N + n0) * len;
-      const int total = rows * len;
-      for (int e = threadIdx.x; e < total; e += kProjThreads) {
-        const int rr = e / len, cc = e - rr * len;
-        store_elem(dst, base + e, stage[rr * ProjSmem::kStride + cc], args.bias_fmt);
+      if (args.bias_fmt == kF32 && len % 4 == 0) {
+        // 16-byte stores: a row of len floats is len / 4 chunks; the warp's
+        // lanes cover consecutive chunks of consecutive rows
+        const int cpr = len / 4;  // chunks per row
+        const int total = rows * cpr;
+        float4* out4 = reinterpret_cast<float4*>(static_cast<float*>(dst) + base);
+        for (int e = threadIdx.x; e < total; e += kProjThreads) {
+          const int rr = e / cpr, c4 = 4 * (e - rr * cpr);
+          const float* src = stage + rr * ProjSmem::kStride + c4;
+          out4[e] = make_float4(src[0], src[1], src[2], src[3]);
+        }
+      } else {
+        // a row per warp pass, lanes along it (len <= 64)
+        for (int rr = warp; rr < rows; rr += kProjThreads / 32)
+          for (int cc = lane; cc < len; cc += 32)
+            store_elem(dst, base + static_cast<size_t>(rr) * len + cc, stage[rr * ProjSmem::kStride + cc],
+                       args.bias_fmt);
       }
       __syncthreads();
     }
