@@ -1,6 +1,7 @@
 // C-ABI of libdera_relpos: argument validation, TMA descriptors and kernel
 // dispatch for the decomposed rel-pos attention path.  Declarations and the
 // contract of every entry point are in include/dera_relpos.h.
+#include <algorithm>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -20,12 +21,14 @@ namespace dera {
 __device__ int g_status_word = 0;
 
 cudaError_t launch_project(const CUtensorMap& q, const CUtensorMap& th, const CUtensorMap& tw,
-                           const ProjArgs& args, int in_fmt, cudaStream_t stream) {
+                           const ProjArgs& args, int in_fmt, int max_ctas, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(relpos_project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        ProjSmem::kAlloc);
   if (e != cudaSuccess) return e;
   const int n_qtiles = (args.N + kBlockM - 1) / kBlockM;
-  const unsigned grid = static_cast<unsigned>(n_qtiles) * static_cast<unsigned>(args.BH);
+  // persistent: at most max_ctas CTAs (two per SM), each walking a strided list of tiles
+  const unsigned tiles = static_cast<unsigned>(n_qtiles) * static_cast<unsigned>(args.BH);
+  const unsigned grid = max_ctas > 0 ? std::min(tiles, static_cast<unsigned>(max_ctas)) : tiles;
   relpos_project_kernel<<<grid, kProjThreads, ProjSmem::kAlloc, stream>>>(q, th, tw, args, in_fmt, n_qtiles);
   return cudaGetLastError();
 }
@@ -348,7 +351,8 @@ dera_status dera_relpos_project(const void* q, const void* rel_pos_h, const void
   args.W = W;
   args.N = N;
   args.bias_fmt = fmt_of(bias_dtype);
-  const cudaError_t e = launch_project(mq, mh, mw, args, fmt_of(in_dtype), static_cast<cudaStream_t>(stream));
+  const cudaError_t e =
+      launch_project(mq, mh, mw, args, fmt_of(in_dtype), 2 * sm_count(dev), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DERA_OK : DERA_ERR_CUDA;
 }
 
