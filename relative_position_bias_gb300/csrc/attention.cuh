@@ -32,6 +32,11 @@ namespace dera {
 constexpr int kStages = 3;
 constexpr int kAttnThreads = 384;
 constexpr float kSpecSumLimit = 32768.0f;  // largest accepted row sum of a speculative tile
+// Starting row maximum of a segment (base 2): at most kStartCap above the
+// exact maximum of its first key tile, which keeps that tile's largest p at or
+// above 2^-12, inside the fp16 normal range; kStartMargin below the estimate.
+constexpr float kStartCap = 12.0f;
+constexpr float kStartMargin = 4.0f;
 constexpr int kBiasStride = 66;       // floats per row of a bias staging area
 
 struct AttnSmem {
@@ -498,8 +503,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         else tmem_ld16(tS + cb, *reinterpret_cast<uint32_t(*)[16]>(&u[0]));
         tmem_wait_ld();
       };
-      // Exact tile maximum of x = s*scale*log2e + rel_w*log2e + rel_h*log2e.
-      auto tile_max = [&](const float (&bhv)[KHT]) -> float {
+      // Exact tile maximum of x = s*scale*log2e + rel_w*log2e + rel_h*log2e;
+      // base = the same without the rel_h term.
+      auto tile_max = [&](const float (&bhv)[KHT], float& base) -> float {
         float gm[KHT];
         #pragma unroll
         for (int g = 0; g < KHT; ++g) gm[g] = NEG_INF;
@@ -519,8 +525,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
         }
         float mt = NEG_INF;
+        base = NEG_INF;
         #pragma unroll
-        for (int g = 0; g < KHT; ++g) mt = fmaxf(mt, gm[g] + bhv[g]);
+        for (int g = 0; g < KHT; ++g) {
+          mt = fmaxf(mt, gm[g] + bhv[g]);
+          base = fmaxf(base, gm[g]);
+        }
         return mt;
       };
       // Waits (once, warp-uniformly) until PV of the previous key tile has
@@ -576,7 +586,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       };
 
       // Online softmax over the segment's key tiles.  The first tile takes the
-      // exact maximum; later tiles exponentiate against the running maximum
+      // exact maximum (raised by the rel_h estimate below); later tiles
+      // exponentiate against the running maximum
       // at once and are redone exactly only if their row sum exceeds 2^15
       // (so every p stays below the fp16 limit).  The final O / l uses the
       // same running maximum, so skipping rescales changes nothing.
@@ -599,9 +610,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           exact = __any_sync(0xffffffffu, !(ts.x + ts.y <= kSpecSumLimit));
         }
         if (exact) {
-          const float mt = tile_max(bhv);
+          float base;
+          const float mt = tile_max(bhv, base);
           if (j == sg.j0) {
-            m_used = mt;
+            // rel_h is the term that moves the row maximum most between key
+            // tiles, so start from this tile's largest s*scale + rel_w plus the
+            // row's largest rel_h (less a margin), capped above the exact
+            // maximum of this tile: later tiles then seldom pass the 2^15
+            // row-sum bound and need an exact redo
+            float mbh = NEG_INF;
+            for (int kh = 0; kh < H; ++kh) mbh = fmaxf(mbh, bh_row[kh]);
+            m_used = fmaxf(mt, fminf(mt + kStartCap, base + mbh - kStartMargin));
           } else {
             wait_pv();
             const float m_new = fmaxf(m_used, mt);
