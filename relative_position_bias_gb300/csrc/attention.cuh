@@ -31,7 +31,9 @@ namespace dera {
 
 constexpr int kStages = 3;
 constexpr int kAttnThreads = 384;
-constexpr float kSpecSumLimit = 32768.0f;  // largest accepted row sum of a speculative tile
+// Largest accepted row sum of a speculative tile: with the sum at most this,
+// every p rounds to at most 65504, the largest finite fp16.
+constexpr float kSpecSumLimit = 65000.0f;
 // Starting row maximum of a segment (base 2): at most kStartCap above the
 // exact maximum of its first key tile, which keeps that tile's largest p at or
 // above 2^-12, inside the fp16 normal range; kStartMargin below the estimate.
@@ -588,11 +590,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // Online softmax over the segment's key tiles.  The first tile takes the
       // exact maximum (raised by the rel_h estimate below); later tiles
       // exponentiate against the running maximum
-      // at once and are redone exactly only if their row sum exceeds 2^15
-      // (so every p stays below the fp16 limit).  The final O / l uses the
+      // at once and are redone exactly only if their row sum exceeds
+      // kSpecSumLimit (so every p stays within fp16).  The final O / l uses the
       // same running maximum, so skipping rescales changes nothing.
       float m_used = 0.f;
       float2 lsum = make_float2(0.f, 0.f);
+      float mbh = NEG_INF;  // largest rel_h term of the row (base 2)
+      for (int kh = 0; kh < H; ++kh) mbh = fmaxf(mbh, bh_row[kh]);
       for (int j = sg.j0; j < sg.j1; ++j, ++gi) {
         ok = warp_all(mbar_wait(&bars[kBarSFull + wg], gi & 1, abort_flag, status));
         if (!ok) break;
@@ -616,14 +620,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             // rel_h is the term that moves the row maximum most between key
             // tiles, so start from this tile's largest s*scale + rel_w plus the
             // row's largest rel_h (less a margin), capped above the exact
-            // maximum of this tile: later tiles then seldom pass the 2^15
-            // row-sum bound and need an exact redo
-            float mbh = NEG_INF;
-            for (int kh = 0; kh < H; ++kh) mbh = fmaxf(mbh, bh_row[kh]);
+            // maximum of this tile: later tiles then seldom pass the row-sum
+            // bound and need an exact redo
             m_used = fmaxf(mt, fminf(mt + kStartCap, base + mbh - kStartMargin));
           } else {
             wait_pv();
-            const float m_new = fmaxf(m_used, mt);
+            // the same estimate, capped above this tile's exact maximum
+            const float m_new = fmaxf(fmaxf(m_used, mt), fminf(mt + kStartCap, base + mbh - kStartMargin));
             const float alpha = ex2_approx(m_used - m_new);
             m_used = m_new;
             lsum.x *= alpha;

@@ -159,7 +159,7 @@ def test_late_large_scores(entry, case, dtype):
     "inf": one key 150 (base-2 units) above the rest, whose 2^x overflows even
     fp32; "clamp": one key about 18 above the running maximum (p beyond the
     fp16 range); "raise": a whole tile about 12 above it (the row sum passes
-    2^15 with every p still in range).  All must match the oracle."""
+    the kernel's bound with every p still in range).  All must match the oracle."""
     base = I.WORKLOADS["grid16"] if dtype == "bf16" else I.WORKLOADS["ragged40"]
     w = base.with_grid(32, 32, B=1, heads=2)
     x = I.make_inputs(w, seed=11)
