@@ -290,23 +290,56 @@ def run_ours(args, w, rank: int, world: int) -> dict | None:
     value = job_value(flops, args.steps, world, total_s)
     ms_med = statistics.median(ms)
 
-    # end to end through the public API: pinned host inputs -> device, compute, result -> pinned host
+    # end to end through the public API: every step copies its inputs from
+    # pinned host memory and reads its result back to pinned host memory.
+    # Steps alternate between two device buffer sets, with the input copies
+    # and the read-backs on streams of their own, so one step's copies overlap
+    # the neighbouring steps' kernels (the copies stay inside the timed region).
     host = {k: t.pin_memory() for k, t in x.items()}
-    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    host_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    dbuf = [d, {k: torch.empty_like(t) for k, t in d.items()}]
+    obuf = [out, torch.empty_like(out)]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = host_out.numel() * host_out.element_size()
+    d2h = host_out[0].numel() * host_out[0].element_size()
     e2e_steps = max(3, min(args.steps, 50))
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_read = [torch.cuda.Event() for _ in range(2)]
+
+    def step_on(b):
+        db = dbuf[b]
+        if args.entry == "fused":
+            rpb.fused(db["q"], db["k"], db["v"], db["rel_pos_h"], db["rel_pos_w"], w.H, w.W, w.scale, out=obuf[b])
+        else:
+            rh, rw = rpb.project(db["q"], db["rel_pos_h"], db["rel_pos_w"], w.H, w.W, rel_h=rel_h, rel_w=rel_w)
+            rpb.attention(db["q"], db["k"], db["v"], rh, rw, w.H, w.W, w.scale, out=obuf[b])
+
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        for k in d:
-            d[k].copy_(host[k], non_blocking=True)
-        step()
-        host_out.copy_(out, non_blocking=True)
-    e1.record(stream)
+    e0.record(s_in)
+    for i in range(e2e_steps):
+        b = i & 1
+        if i >= 2:
+            s_in.wait_event(ev_done[b])  # step i - 2 has finished reading buffer set b
+        with torch.cuda.stream(s_in):
+            for k in dbuf[b]:
+                dbuf[b][k].copy_(host[k], non_blocking=True)
+        ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
+        if i >= 2:
+            stream.wait_event(ev_read[b])  # the result of step i - 2 has been read back
+        with torch.cuda.stream(stream):
+            step_on(b)
+        ev_done[b].record(stream)
+        s_out.wait_event(ev_done[b])
+        with torch.cuda.stream(s_out):
+            host_out[b].copy_(obuf[b], non_blocking=True)
+        ev_read[b].record(s_out)
+    s_out.wait_event(ev_done[(e2e_steps - 1) & 1])
+    e1.record(s_out)
     torch.cuda.synchronize()
     e2e_s = aggregate_max(e0.elapsed_time(e1) / 1e3)
     e2e_value = job_value(flops, e2e_steps, world, e2e_s)
@@ -361,7 +394,8 @@ def run_ours(args, w, rank: int, world: int) -> dict | None:
                      "kernel": kernel, "peak_source": f"bf16_tflops (burst) of {peak_src}",
                      "flops_per_launch": flops},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps},
+                "steps": e2e_steps,
+                "overlap": "two device buffer sets; input copies and read-backs on their own streams"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
         "wall_s_timed_region": t_wall,
