@@ -85,18 +85,40 @@ static_assert(kBarCount <= AttnSmem::kNumBars, "barrier slots");
 // of key tiles, so a unit is cut into at most two segments.  With U a
 // multiple of G the tail is one whole unit per CTA and nothing is cut.
 // Iterations are numbered globally: t = unit * n_kv + key tile.
+//
+// The tail ranges are equal in cost rather than in key tiles: each segment
+// a CTA starts costs about kSegCost key tiles (prologue, epilogue, pipeline
+// refill), so the tail is cut evenly in a virtual space where every unit is
+// kSegCost slots of "segment start" followed by its n_kv key tiles.  A range
+// then holds fewer key tiles the more unit starts it contains.  Each range
+// still spans at least n_kv + kSegCost virtual slots, so no unit is cut into
+// more than two segments.
 struct Schedule {
+  static constexpr int kSegCost = 5;
   int G, n_kv, dp_rounds;
-  long long sk_base, T;  // first tail iteration, tail length
+  long long sk_base, V;  // first tail iteration; tail length in virtual slots
   __device__ __forceinline__ Schedule(int U, int G_, int n_kv_) : G(G_), n_kv(n_kv_) {
     dp_rounds = max(U / G - 1, 0);
     sk_base = static_cast<long long>(dp_rounds) * G * n_kv;
-    T = static_cast<long long>(U - dp_rounds * G) * n_kv;
+    V = static_cast<long long>(U - dp_rounds * G) * (n_kv + kSegCost);
   }
-  __device__ __forceinline__ long long begin(int c) const { return sk_base + static_cast<long long>(c) * T / G; }
+  // tail iteration (relative to sk_base) at virtual slot v, 0 <= v <= V
+  __device__ __forceinline__ long long real_of(long long v) const {
+    const long long per = n_kv + kSegCost;
+    const long long u = v / per, o = v - u * per;
+    return u * n_kv + max(0LL, o - kSegCost);
+  }
+  __device__ __forceinline__ long long begin(int c) const {
+    return sk_base + real_of(static_cast<long long>(c) * V / G);
+  }
   // CTA whose tail range holds iteration t (t >= sk_base)
   __device__ __forceinline__ int cta_of(long long t) const {
-    return static_cast<int>(((t - sk_base + 1) * G - 1) / T);
+    const long long tr = t - sk_base, u = tr / n_kv;
+    const long long v = u * (n_kv + kSegCost) + kSegCost + (tr - u * n_kv);
+    int c = static_cast<int>(min(static_cast<long long>(G - 1), v * G / V));
+    while (c + 1 < G && begin(c + 1) <= t) ++c;
+    while (c > 0 && begin(c) > t) --c;
+    return c;
   }
 };
 
