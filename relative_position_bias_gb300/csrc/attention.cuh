@@ -94,7 +94,7 @@ static_assert(kBarCount <= AttnSmem::kNumBars, "barrier slots");
 // still spans at least n_kv + kSegCost virtual slots, so no unit is cut into
 // more than two segments.
 struct Schedule {
-  static constexpr int kSegCost = 5;
+  static constexpr int kSegCost = 8;
   int G, n_kv, dp_rounds;
   long long sk_base, V;  // first tail iteration; tail length in virtual slots
   __device__ __forceinline__ Schedule(int U, int G_, int n_kv_) : G(G_), n_kv(n_kv_) {
