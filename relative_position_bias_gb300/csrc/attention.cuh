@@ -40,6 +40,16 @@ constexpr float kSpecSumLimit = 65000.0f;
 constexpr float kStartCap = 12.0f;
 constexpr float kStartMargin = 4.0f;
 constexpr int kBiasStride = 66;       // floats per row of a bias staging area
+// Register split: the producer / MMA / V-conversion warpgroup gives registers
+// back and the two softmax warpgroups take them, which removes the softmax's
+// spills.  The block launches with kLaunchRegs per thread (the most that 384
+// threads get); the host checks the compiled count before the first launch,
+// since a split larger than the launch pool would block forever.
+constexpr int kLaunchRegs = 168;
+constexpr int kRegsCtl = 104;
+constexpr int kRegsSmx = 200;
+static_assert(kRegsCtl * 128 + kRegsSmx * 256 <= kLaunchRegs * kAttnThreads, "register split exceeds the launch pool");
+static_assert(kRegsCtl % 8 == 0 && kRegsSmx % 8 == 0, "setmaxnreg counts are multiples of 8");
 
 struct AttnSmem {
   static constexpr int kQ = 0;                                   // 2 x 16 KB
@@ -230,6 +240,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t tbase = *tmem_slot;
 
   if (warp < 4) {
+  regs_release<kRegsCtl>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -417,6 +428,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   }
   } else {
+    regs_claim<kRegsSmx>();
     // ------------------------------------------------------------ softmax / epilogue
     const int wg = (warp - 4) >> 2;          // query tile of this warpgroup
     const int wq = warp & 3;                 // TMEM lane quarter
