@@ -136,12 +136,15 @@ DERA_API dera_status dera_relpos_fused(const void* q, const void* k, const void*
  * number of units is not a whole number of waves of one CTA per SM, the
  * kernel runs one persistent CTA per SM over equal shares of the
  * (unit, key tile) iteration space and cuts some units between two CTAs; the
- * partial results (unnormalised O, row max, row sum, fp32) and two arrival
- * counters per unit (one per query tile) live in the caller's `workspace`.  A NULL workspace, or one
- * smaller than this size, selects one CTA per unit instead (same result, no
- * scratch, less even load).  The workspace must be device memory, 256-byte
- * aligned, owned by the caller, and not used by another call in flight: the
- * entry point clears the counters with cudaMemsetAsync on `stream` first.
+ * partial results (unnormalised O, row max, row sum, fp32) and two 8-byte
+ * arrival counters per unit (one per query tile) live in the caller's
+ * `workspace`.  A NULL workspace, or one smaller than this size, selects one
+ * CTA per unit instead (same result, no scratch, less even load).  The
+ * workspace must be device memory, 256-byte aligned, owned by the caller, and
+ * not used by another call in flight.  Its contents need no initialisation
+ * and are never cleared: each launch marks its arrivals with a 64-bit tag that
+ * no earlier launch of the process used, so whatever an earlier call (or one
+ * that stopped early) left behind is ignored.
  */
 DERA_API dera_status dera_relpos_workspace_size(int BH, int H, int W, int head_dim, size_t* bytes);
 
@@ -168,12 +171,12 @@ DERA_API dera_status dera_relpos_workspace_size(int BH, int H, int W, int head_d
  *   - Limit: problems whose split schedule needs more scratch than the
  *     buffer holds are rejected with DERA_ERR_SCRATCH before anything is
  *     enqueued.  The need is what dera_relpos_workspace_size reports: on a
- *     152-SM GB300, 21 168 128 bytes of partial-result slots plus 8 bytes per
+ *     152-SM GB300, 21 168 128 bytes of partial-result slots plus 16 bytes per
  *     work unit (a pair of 128-row query tiles of one head), so problems of
- *     up to about 499 000 units fit.  Problems that need no scratch always run.
+ *     up to about 249 000 units fit.  Problems that need no scratch always run.
  *   - Sharing: every call on a device uses the same buffer and leaves its
- *     contents behind; the call clears the per-unit counters it relies on
- *     (cudaMemsetAsync on `stream`) before the launch.  Calls that overlap on
+ *     contents behind; like a caller's workspace, the buffer needs no
+ *     clearing between calls (see dera_relpos_workspace_size).  Calls that overlap on
  *     the GPU (for example on two streams) race on the buffer and give wrong
  *     results: serialise them.
  * Other arguments, layouts and errors: as dera_relpos_fused.

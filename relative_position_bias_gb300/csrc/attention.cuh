@@ -755,10 +755,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const bool w_ok = mbar_wait(&bars[kBarPartWritten + wg], pseg & 1, abort_flag, status);
           int last = 0;
           if (w_ok) {
-            int* counter = args.counters + 2 * static_cast<size_t>(sg.u) + wg;
-            const int old = atomic_add_acq_rel_gpu(counter, 1);
-            last = old == 1;
-            if (last) *counter = 0;  // ready for the next launch (stream-ordered)
+            // Each of the unit's two segments swaps this launch's tag in; the
+            // one that finds the tag already there arrived second.  Whatever
+            // an earlier (or stopped) launch left holds another tag, so the
+            // counters never need clearing.
+            unsigned long long* counter = args.counters + 2 * static_cast<size_t>(sg.u) + wg;
+            last = atomic_exch_acq_rel_gpu(counter, args.tag) == args.tag;
           }
           merge_flag[wg] = last;
           mbar_arrive(&bars[kBarMergeGo + wg]);

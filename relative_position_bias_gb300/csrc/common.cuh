@@ -37,7 +37,8 @@ struct AttnArgs {
   void* out;           // [BH, N, 64]
   int* status;         // device status word
   float* partials;     // [2 * gridDim.x][2][128][kSlotRow] partial results (split units only)
-  int* counters;       // [n_units][2] segment arrivals per unit and query tile, zero at launch (split units only)
+  unsigned long long* counters;  // [n_units][2] arrival tags per unit and query tile (split units only)
+  unsigned long long tag;        // this launch's arrival tag: no earlier launch of the process used it
   int BH, H, W, N;
   int n_qtiles;        // ceil(N / 128)
   int n_pairs;         // ceil(n_qtiles / 2): query-tile pairs per head

@@ -2,6 +2,9 @@
 // dispatch for the decomposed rel-pos attention path.  Declarations and the
 // contract of every entry point are in include/dera_relpos.h.
 #include <algorithm>
+#include <atomic>
+#include <chrono>
+#include <random>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -179,6 +182,24 @@ int sm_count(int dev) {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Arrival tags of the split schedule's per-unit counters: a 64-bit sequence
+// from a random start, so no two launches of this process share a tag and
+// counters left by any earlier launch (finished or stopped) never match.
+unsigned long long next_launch_tag() {
+  static std::atomic<unsigned long long> next{[] {
+    unsigned long long seed = 0x9e3779b97f4a7c15ull ^ static_cast<unsigned long long>(
+        std::chrono::steady_clock::now().time_since_epoch().count());
+    try {
+      std::random_device rd;
+      seed ^= (static_cast<unsigned long long>(rd()) << 32) ^ rd();
+    } catch (...) {
+      // no entropy source: the clock alone seeds the sequence
+    }
+    return seed;
+  }()};
+  return next.fetch_add(1, std::memory_order_relaxed);
+}
+
 // Work decomposition of one call: units are pairs of 128-row query tiles.
 struct Plan {
   int n_qtiles, n_pairs, n_units, n_kv, ctas;
@@ -199,7 +220,7 @@ Plan make_plan(int BH, int H, int W, int sms) {
   // so a unit is cut into at most two segments.
   p.split = sms > 0 && p.n_units > sms && p.n_units % sms != 0;
   p.ctas = p.split ? sms : p.n_units;
-  p.counters_bytes = align256(static_cast<size_t>(p.n_units) * 2 * sizeof(int));  // one per query tile
+  p.counters_bytes = align256(static_cast<size_t>(p.n_units) * 2 * sizeof(unsigned long long));  // one per query tile
   p.partial_bytes = static_cast<size_t>(2) * sms * 2 * kBlockM * kSlotRow * sizeof(float);
   return p;
 }
@@ -258,18 +279,16 @@ dera_status run_attention(const void* q, const void* k, const void* v, const voi
   args.n_kv = plan.n_kv;
   args.partials = nullptr;
   args.counters = nullptr;
+  args.tag = 0;
   args.scale_log2 = scale * kLog2e;
   args.in_fmt = fmt_of(in_dtype);
   args.bias_fmt = fmt_of(bias_dtype);
   args.out_fmt = fmt_of(out_dtype);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (plan.split) {
-    args.counters = static_cast<int*>(workspace);
+    args.counters = static_cast<unsigned long long*>(workspace);
+    args.tag = next_launch_tag();
     args.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.counters_bytes);
-    // the counters must start at zero; the kernel leaves them at zero too,
-    // but a launch that stopped early would not
-    if (cudaMemsetAsync(args.counters, 0, static_cast<size_t>(plan.n_units) * 2 * sizeof(int), s) != cudaSuccess)
-      return DERA_ERR_CUDA;
   }
   cudaError_t e;
   switch (WP) {

@@ -89,9 +89,9 @@ __device__ __forceinline__ void tc_fence_after() {
 // Atomic add with acquire-release semantics at GPU scope: releases every write
 // that happens before it (including other threads' writes ordered by CTA-scope
 // synchronisation) and acquires the writes released by earlier adds.
-__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
-  int old;
-  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+__device__ __forceinline__ unsigned long long atomic_exch_acq_rel_gpu(unsigned long long* p, unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.acq_rel.gpu.global.exch.b64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
   return old;
 }
 

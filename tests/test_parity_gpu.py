@@ -243,6 +243,33 @@ def test_caller_workspace_and_reuse():
     check_out(alt, oracle.fused(f["q"], f["k"], f["v"], f["rel_pos_h"], f["rel_pos_w"], w.H, w.W, w.scale))
 
 
+@pytest.mark.parametrize("entry", ["fused", "attention"])
+@pytest.mark.parametrize("name", ["global64", "ragged40"])
+def test_workspace_contents_are_ignored(name, entry):
+    """The split schedule's counters carry a per-launch tag, so a workspace
+    full of arbitrary bytes (never cleared) gives the same result as the
+    library's own workspace, call after call."""
+    w = I.WORKLOADS[name]
+    assert rpb.workspace_size(w.BH, w.H, w.W) > 0, "this workload must use the split schedule"
+    d = _dev(I.make_inputs(w))
+    if entry == "fused":
+        args = (d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W, w.scale)
+        call = rpb.fused
+    else:
+        rh, rw = rpb.project(d["q"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W)
+        args = (d["q"], d["k"], d["v"], rh, rw, w.H, w.W, w.scale)
+        call = rpb.attention
+    ref = call(*args)
+    ws = torch.empty(rpb.workspace_size(w.BH, w.H, w.W), dtype=torch.uint8, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(11)
+    for trial in range(4):
+        if trial < 3:
+            ws.random_(0, 256, generator=g)   # the last call reuses what the previous one left
+        got = call(*args, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(got, ref), f"trial {trial}"
+
+
 @pytest.mark.parametrize("name", list(I.WORKLOADS))
 def test_attention_parity_f32_bias(name):
     """Compact-bias entry fed the oracle's projection (rounded to fp32); the
