@@ -446,7 +446,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const float sl2 = args.scale_log2;
     const float2 sl2v = make_float2(sl2, sl2);
 
-    int gi = 0, seg = 0, pseg = 0;
+    int gi = 0, seg = 0;
+    int pseg = 0;  // completed phases of this warpgroup's merge-go barrier
+    int ppub = 0;  // completed phases of its partial-written barrier
     uint32_t stg_phase = 0;  // completed phases of this warpgroup's staging barrier
     // Warpgroup-wide barrier on the staging mbarrier (all 128 threads arrive, then wait).
     auto wg_sync = [&]() -> bool {
@@ -725,57 +727,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc_fence_before();
         if (FUSED) mbar_arrive(&bars[kBarEpiDone]);
       } else {
-        // Cut unit: publish this warpgroup's (O, m, l); the warpgroup that
-        // completes the unit's second segment (here or in another CTA) merges.
-        // Each query tile has its own counter, so the two warpgroups never
-        // wait for each other.  The schedule cuts a unit at most once.
+        // Cut unit: the schedule cuts a unit at most once, into two pieces
+        // that may run in different CTAs.  Each query tile has its own
+        // counter, so the two warpgroups never wait for each other, and
+        // nothing waits on another CTA.
+        //  - If the other piece has already published its (O, m, l), this
+        //    piece merges with it straight from TMEM (no publish, no atomic).
+        //  - Otherwise it publishes, then swaps this launch's tag into the
+        //    counter; the piece that finds the tag already there arrived
+        //    second and merges both published slots.  Whatever an earlier
+        //    (or stopped) launch left holds another tag, so the counters
+        //    never need clearing.
+        // Both merges combine the pieces in the same order (the unit's first
+        // piece, then its second) from the same fp32 values, so the result
+        // does not depend on which path ran.
         const int c = blockIdx.x;
         const int slot = (sg.tail == 0) ? 2 * c : 2 * c + 1;
-        float* ws = args.partials + (static_cast<size_t>(slot) * 2 + wg) * kBlockM * kSlotRow + r * kSlotRow;
-        #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t u[16];
-          tmem_ld16(tO + 16 * cc, u);
-          tmem_wait_ld();
-          #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            __stcg(reinterpret_cast<float4*>(ws + 16 * cc) + q,
-                   make_float4(__uint_as_float(u[4 * q]), __uint_as_float(u[4 * q + 1]),
-                               __uint_as_float(u[4 * q + 2]), __uint_as_float(u[4 * q + 3])));
-        }
-        __stcg(reinterpret_cast<float2*>(ws + 64), make_float2(m_used, l));
-        tc_fence_before();
-        if (FUSED) mbar_arrive(&bars[kBarEpiDone]);
-        // mbarrier arrive/wait order these writes before the elected thread's
-        // GPU-scope release below (release is cumulative)
-        mbar_arrive(&bars[kBarPartWritten + wg]);
         const long long u0 = static_cast<long long>(sg.u) * n_kv;
         const int c_first = sched.cta_of(u0);
-        if (r == 0) {
-          const bool w_ok = mbar_wait(&bars[kBarPartWritten + wg], pseg & 1, abort_flag, status);
-          int last = 0;
-          if (w_ok) {
-            // Each of the unit's two segments swaps this launch's tag in; the
-            // one that finds the tag already there arrived second.  Whatever
-            // an earlier (or stopped) launch left holds another tag, so the
-            // counters never need clearing.
-            unsigned long long* counter = args.counters + 2 * static_cast<size_t>(sg.u) + wg;
-            last = atomic_exch_acq_rel_gpu(counter, args.tag) == args.tag;
-          }
-          merge_flag[wg] = last;
-          mbar_arrive(&bars[kBarMergeGo + wg]);
-        }
-        ok = warp_all(mbar_wait(&bars[kBarMergeGo + wg], pseg & 1, abort_flag, status));
-        ++pseg;
-        if (!ok) break;
-        if (merge_flag[wg]) {
-          // the unit's two segments, rescaled to the larger running max
-          const int sl0 = (sched.begin(c_first) == u0) ? 2 * c_first : 2 * c_first + 1;
-          const int sl1 = 2 * (c_first + 1);
-          const float* pa = args.partials + (static_cast<size_t>(sl0) * 2 + wg) * kBlockM * kSlotRow + r * kSlotRow;
-          const float* pb = args.partials + (static_cast<size_t>(sl1) * 2 + wg) * kBlockM * kSlotRow + r * kSlotRow;
-          const float2 ma = __ldcg(reinterpret_cast<const float2*>(pa + 64));
-          const float2 mb = __ldcg(reinterpret_cast<const float2*>(pb + 64));
+        const int sl0 = (sched.begin(c_first) == u0) ? 2 * c_first : 2 * c_first + 1;
+        const int sl1 = 2 * (c_first + 1);
+        auto slot_row = [&](int s_) {
+          return args.partials + (static_cast<size_t>(s_) * 2 + wg) * kBlockM * kSlotRow + r * kSlotRow;
+        };
+        // out = (fa O_a + fb O_b) / (fa l_a + fb l_b), rescaled to the larger running max
+        auto merge_store = [&](const float4 (&xa)[16], float2 ma, const float4 (&xb)[16], float2 mb) {
           const float mstar = fmaxf(ma.x, mb.x);
           const float fa = ex2_approx(ma.x - mstar), fb = ex2_approx(mb.x - mstar);
           const float inv_l = 1.0f / (fa * ma.y + fb * mb.y);
@@ -784,14 +760,86 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             float v[16];
             #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const float4 xa = __ldcg(reinterpret_cast<const float4*>(pa + 16 * cc) + q);
-              const float4 xb = __ldcg(reinterpret_cast<const float4*>(pb + 16 * cc) + q);
-              v[4 * q] = fa * xa.x + fb * xb.x;
-              v[4 * q + 1] = fa * xa.y + fb * xb.y;
-              v[4 * q + 2] = fa * xa.z + fb * xb.z;
-              v[4 * q + 3] = fa * xa.w + fb * xb.w;
+              const float4 a = xa[4 * cc + q], b = xb[4 * cc + q];
+              v[4 * q] = fa * a.x + fb * b.x;
+              v[4 * q + 1] = fa * a.y + fb * b.y;
+              v[4 * q + 2] = fa * a.z + fb * b.z;
+              v[4 * q + 3] = fa * a.w + fb * b.w;
             }
             store16(16 * cc, v, inv_l);
+          }
+        };
+        unsigned long long* counter = args.counters + 2 * static_cast<size_t>(sg.u) + wg;
+        if (r == 0) {
+          merge_flag[wg] = ld_acquire_gpu(counter) == args.tag;
+          mbar_arrive(&bars[kBarMergeGo + wg]);
+        }
+        ok = warp_all(mbar_wait(&bars[kBarMergeGo + wg], pseg & 1, abort_flag, status));
+        ++pseg;
+        if (!ok) break;
+        if (merge_flag[wg]) {
+          const float* po = slot_row(slot == sl0 ? sl1 : sl0);
+          float4 xo[16];
+          #pragma unroll
+          for (int q = 0; q < 16; ++q) xo[q] = __ldcg(reinterpret_cast<const float4*>(po) + q);
+          const float2 mo = __ldcg(reinterpret_cast<const float2*>(po + 64));
+          uint32_t oa[64];
+          tmem_ld32(tO, *reinterpret_cast<uint32_t(*)[32]>(&oa[0]));
+          tmem_ld32(tO + 32, *reinterpret_cast<uint32_t(*)[32]>(&oa[32]));
+          tmem_wait_ld();
+          tc_fence_before();
+          if (FUSED) mbar_arrive(&bars[kBarEpiDone]);
+          const bool first = slot == sl0;  // warp-uniform
+          float4 xa[16], xb[16];
+          #pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const float4 own = make_float4(__uint_as_float(oa[4 * q]), __uint_as_float(oa[4 * q + 1]),
+                                           __uint_as_float(oa[4 * q + 2]), __uint_as_float(oa[4 * q + 3]));
+            xa[q] = first ? own : xo[q];
+            xb[q] = first ? xo[q] : own;
+          }
+          const float2 mown = make_float2(m_used, l);
+          merge_store(xa, first ? mown : mo, xb, first ? mo : mown);
+        } else {
+          float* ws = slot_row(slot);
+          #pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t u[16];
+            tmem_ld16(tO + 16 * cc, u);
+            tmem_wait_ld();
+            #pragma unroll
+            for (int q = 0; q < 4; ++q)
+              __stcg(reinterpret_cast<float4*>(ws + 16 * cc) + q,
+                     make_float4(__uint_as_float(u[4 * q]), __uint_as_float(u[4 * q + 1]),
+                                 __uint_as_float(u[4 * q + 2]), __uint_as_float(u[4 * q + 3])));
+          }
+          __stcg(reinterpret_cast<float2*>(ws + 64), make_float2(m_used, l));
+          tc_fence_before();
+          if (FUSED) mbar_arrive(&bars[kBarEpiDone]);
+          // mbarrier arrive/wait order these writes before the elected thread's
+          // GPU-scope release below (release is cumulative).  Every thread has
+          // read merge_flag above before it arrives here, so r == 0 may reuse it.
+          mbar_arrive(&bars[kBarPartWritten + wg]);
+          const int pw = ppub++;
+          if (r == 0) {
+            const bool w_ok = mbar_wait(&bars[kBarPartWritten + wg], pw & 1, abort_flag, status);
+            merge_flag[wg] = w_ok && atomic_exch_acq_rel_gpu(counter, args.tag) == args.tag;
+            mbar_arrive(&bars[kBarMergeGo + wg]);
+          }
+          ok = warp_all(mbar_wait(&bars[kBarMergeGo + wg], pseg & 1, abort_flag, status));
+          ++pseg;
+          if (!ok) break;
+          if (merge_flag[wg]) {
+            const float* pa = slot_row(sl0);
+            const float* pb = slot_row(sl1);
+            float4 xa[16], xb[16];
+            #pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              xa[q] = __ldcg(reinterpret_cast<const float4*>(pa) + q);
+              xb[q] = __ldcg(reinterpret_cast<const float4*>(pb) + q);
+            }
+            merge_store(xa, __ldcg(reinterpret_cast<const float2*>(pa + 64)), xb,
+                        __ldcg(reinterpret_cast<const float2*>(pb + 64)));
           }
         }
       }

@@ -89,6 +89,11 @@ __device__ __forceinline__ void tc_fence_after() {
 // Atomic add with acquire-release semantics at GPU scope: releases every write
 // that happens before it (including other threads' writes ordered by CTA-scope
 // synchronisation) and acquires the writes released by earlier adds.
+__device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
 __device__ __forceinline__ unsigned long long atomic_exch_acq_rel_gpu(unsigned long long* p, unsigned long long v) {
   unsigned long long old;
   asm volatile("atom.acq_rel.gpu.global.exch.b64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
