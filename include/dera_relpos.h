@@ -171,9 +171,9 @@ DERA_API dera_status dera_relpos_workspace_size(int BH, int H, int W, int head_d
  *   - Limit: problems whose split schedule needs more scratch than the
  *     buffer holds are rejected with DERA_ERR_SCRATCH before anything is
  *     enqueued.  The need is what dera_relpos_workspace_size reports: on a
- *     152-SM GB300, 21 168 128 bytes of partial-result slots plus 16 bytes per
+ *     152-SM GB300, 20 545 536 bytes of partial-result slots plus 16 bytes per
  *     work unit (a pair of 128-row query tiles of one head), so problems of
- *     up to about 249 000 units fit.  Problems that need no scratch always run.
+ *     up to about 288 000 units fit.  Problems that need no scratch always run.
  *   - Sharing: every call on a device uses the same buffer and leaves its
  *     contents behind; like a caller's workspace, the buffer needs no
  *     clearing between calls (see dera_relpos_workspace_size).  Calls that overlap on

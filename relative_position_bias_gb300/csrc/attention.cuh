@@ -747,9 +747,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int c_first = sched.cta_of(u0);
         const int sl0 = (sched.begin(c_first) == u0) ? 2 * c_first : 2 * c_first + 1;
         const int sl1 = 2 * (c_first + 1);
-        auto slot_row = [&](int s_) {
-          return args.partials + (static_cast<size_t>(s_) * 2 + wg) * kBlockM * kSlotRow + r * kSlotRow;
-        };
+        // a slot of this query tile; this thread's row is O chunk q at
+        // float4 index q * 128 + r, and (m, l) at float2 index r after the
+        // 64 * 128 floats of O
+        auto slot_of = [&](int s_) { return args.partials + (static_cast<size_t>(s_) * 2 + wg) * kSlotFloats; };
+        auto ld_chunk = [&](const float* sl, int q) { return __ldcg(reinterpret_cast<const float4*>(sl) + q * kBlockM + r); };
+        auto ld_ml = [&](const float* sl) { return __ldcg(reinterpret_cast<const float2*>(sl + 64 * kBlockM) + r); };
         // out = (fa O_a + fb O_b) / (fa l_a + fb l_b), rescaled to the larger running max
         auto merge_store = [&](const float4 (&xa)[16], float2 ma, const float4 (&xb)[16], float2 mb) {
           const float mstar = fmaxf(ma.x, mb.x);
@@ -778,11 +781,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         ++pseg;
         if (!ok) break;
         if (merge_flag[wg]) {
-          const float* po = slot_row(slot == sl0 ? sl1 : sl0);
+          const float* po = slot_of(slot == sl0 ? sl1 : sl0);
           float4 xo[16];
           #pragma unroll
-          for (int q = 0; q < 16; ++q) xo[q] = __ldcg(reinterpret_cast<const float4*>(po) + q);
-          const float2 mo = __ldcg(reinterpret_cast<const float2*>(po + 64));
+          for (int q = 0; q < 16; ++q) xo[q] = ld_chunk(po, q);
+          const float2 mo = ld_ml(po);
           uint32_t oa[64];
           tmem_ld32(tO, *reinterpret_cast<uint32_t(*)[32]>(&oa[0]));
           tmem_ld32(tO + 32, *reinterpret_cast<uint32_t(*)[32]>(&oa[32]));
@@ -801,7 +804,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const float2 mown = make_float2(m_used, l);
           merge_store(xa, first ? mown : mo, xb, first ? mo : mown);
         } else {
-          float* ws = slot_row(slot);
+          float* ws = slot_of(slot);
           #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
             uint32_t u[16];
@@ -809,11 +812,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tmem_wait_ld();
             #pragma unroll
             for (int q = 0; q < 4; ++q)
-              __stcg(reinterpret_cast<float4*>(ws + 16 * cc) + q,
+              __stcg(reinterpret_cast<float4*>(ws) + (4 * cc + q) * kBlockM + r,
                      make_float4(__uint_as_float(u[4 * q]), __uint_as_float(u[4 * q + 1]),
                                  __uint_as_float(u[4 * q + 2]), __uint_as_float(u[4 * q + 3])));
           }
-          __stcg(reinterpret_cast<float2*>(ws + 64), make_float2(m_used, l));
+          __stcg(reinterpret_cast<float2*>(ws + 64 * kBlockM) + r, make_float2(m_used, l));
           tc_fence_before();
           if (FUSED) mbar_arrive(&bars[kBarEpiDone]);
           // mbarrier arrive/wait order these writes before the elected thread's
@@ -830,16 +833,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           ++pseg;
           if (!ok) break;
           if (merge_flag[wg]) {
-            const float* pa = slot_row(sl0);
-            const float* pb = slot_row(sl1);
+            const float* pa = slot_of(sl0);
+            const float* pb = slot_of(sl1);
             float4 xa[16], xb[16];
             #pragma unroll
             for (int q = 0; q < 16; ++q) {
-              xa[q] = __ldcg(reinterpret_cast<const float4*>(pa) + q);
-              xb[q] = __ldcg(reinterpret_cast<const float4*>(pb) + q);
+              xa[q] = ld_chunk(pa, q);
+              xb[q] = ld_chunk(pb, q);
             }
-            merge_store(xa, __ldcg(reinterpret_cast<const float2*>(pa + 64)), xb,
-                        __ldcg(reinterpret_cast<const float2*>(pb + 64)));
+            merge_store(xa, ld_ml(pa), xb, ld_ml(pb));
           }
         }
       }

@@ -14,7 +14,10 @@ constexpr int kBlockM = 128;      // query rows per tile (one TMEM lane per row)
 constexpr int kRowBytes = 128;    // one 64-element 16-bit row
 constexpr int kTileBytes = 128 * kRowBytes;  // a 128-row operand tile (16 KB)
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kSlotRow = 68;      // floats per row of a partial-result slot: O[64], m, l, pad
+// One partial-result slot of a query tile: O as 16 column chunks of 4 floats,
+// chunk-major ([16][128] float4, so a warp's 32 rows of one chunk are 512
+// contiguous bytes), then (m, l) per row ([128] float2).
+constexpr int kSlotFloats = 128 * 66;
 
 // Key tiles cover KHT whole grid rows of WP (>= W) padded columns, so the
 // column of a key inside its tile fixes kw at compile time.  The padded
@@ -36,7 +39,7 @@ struct AttnArgs {
   const void* rel_w;   // [BH, N, W]
   void* out;           // [BH, N, 64]
   int* status;         // device status word
-  float* partials;     // [2 * gridDim.x][2][128][kSlotRow] partial results (split units only)
+  float* partials;     // [2 * gridDim.x][2][kSlotFloats] partial results (split units only)
   unsigned long long* counters;  // [n_units][2] arrival tags per unit and query tile (split units only)
   unsigned long long tag;        // this launch's arrival tag: no earlier launch of the process used it
   int BH, H, W, N;

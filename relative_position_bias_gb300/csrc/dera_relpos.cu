@@ -221,7 +221,7 @@ Plan make_plan(int BH, int H, int W, int sms) {
   p.split = sms > 0 && p.n_units > sms && p.n_units % sms != 0;
   p.ctas = p.split ? sms : p.n_units;
   p.counters_bytes = align256(static_cast<size_t>(p.n_units) * 2 * sizeof(unsigned long long));  // one per query tile
-  p.partial_bytes = static_cast<size_t>(2) * sms * 2 * kBlockM * kSlotRow * sizeof(float);
+  p.partial_bytes = static_cast<size_t>(2) * sms * 2 * kSlotFloats * sizeof(float);
   return p;
 }
 
