@@ -487,6 +487,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_arrive(&bars[kBarGFree]);
         if (!ok) break;
       } else {
+        // every warp has stored the previous segment's output rows, which
+        // leave through the same area, before any row is copied in
+        if (seg > 0) ok = wg_sync() && ok;
         // The tile's rows of rel_w, then of rel_h, are one contiguous block
         // each: every warp copies a quarter of the rows into the staging area,
         // a row per pass with the lanes along it (coalesced), scaled by log2e.
@@ -692,25 +695,43 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const float l = lsum.x + lsum.y;
-      uint8_t* orow = reinterpret_cast<uint8_t*>(args.out) +
-                      (static_cast<size_t>(bh) * N + (row_valid ? n : 0)) * kHeadDim * (args.out_fmt == kF32 ? 4 : 2);
-      auto store16 = [&](int c0, const float (&v)[16], float scale) {
-        if (!row_valid) return;
-        if (args.out_fmt == kF32) {
-          float4* dst = reinterpret_cast<float4*>(orow) + c0 / 4;
+      // Output rows leave through this warp's quarter of the bias area (no
+      // warp of the warpgroup reads its bias rows once O is complete): each
+      // lane stages its row, 16-byte chunks XOR-swizzled by row so neither
+      // side has bank conflicts, then the warp stores runs of 512 contiguous
+      // bytes (4 bf16/f16 rows or 2 fp32 rows per instruction).
+      const bool out32 = args.out_fmt == kF32;
+      const int row_bytes = out32 ? 256 : 128;
+      uint8_t* ostage = reinterpret_cast<uint8_t*>(area + wq * 32 * kBiasStride);
+      auto chunk_at = [&](int row, int k) { return ostage + row * row_bytes + ((k ^ (row & 7)) << 4); };
+      auto stage16 = [&](int c0, const float (&v)[16], float scale) {
+        if (out32) {
           #pragma unroll
           for (int q = 0; q < 4; ++q)
-            dst[q] = make_float4(v[4 * q] * scale, v[4 * q + 1] * scale, v[4 * q + 2] * scale, v[4 * q + 3] * scale);
+            *reinterpret_cast<float4*>(chunk_at(lane, c0 / 4 + q)) =
+                make_float4(v[4 * q] * scale, v[4 * q + 1] * scale, v[4 * q + 2] * scale, v[4 * q + 3] * scale);
         } else {
           uint32_t w[8];
           #pragma unroll
           for (int k = 0; k < 8; ++k)
             w[k] = args.out_fmt == kBF16 ? pack_bf16x2(v[2 * k] * scale, v[2 * k + 1] * scale)
                                          : pack_f16x2(v[2 * k] * scale, v[2 * k + 1] * scale);
-          uint4* dst = reinterpret_cast<uint4*>(orow) + c0 / 8;
-          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          *reinterpret_cast<uint4*>(chunk_at(lane, c0 / 8)) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(chunk_at(lane, c0 / 8 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
         }
+      };
+      auto flush_rows = [&]() {
+        __syncwarp();
+        const int n0 = qt * kBlockM + wq * 32;  // this warp's first row
+        uint8_t* obase = reinterpret_cast<uint8_t*>(args.out) + (static_cast<size_t>(bh) * N + n0) * row_bytes;
+        const int per = out32 ? 2 : 4;           // rows per 512-byte run
+        const int kc = out32 ? 16 : 8;           // chunks per row
+        for (int i = 0; i < 32 / per; ++i) {
+          const int row = per * i + lane / kc, k = lane % kc;
+          if (n0 + row < N)
+            *reinterpret_cast<uint4*>(obase + row * row_bytes + (k << 4)) = *reinterpret_cast<const uint4*>(chunk_at(row, k));
+        }
+        __syncwarp();
       };
       if (sg.full(n_kv)) {
         const float inv_l = 1.0f / l;
@@ -722,10 +743,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           float v[16];
           #pragma unroll
           for (int k = 0; k < 16; ++k) v[k] = __uint_as_float(u[k]);
-          store16(16 * c, v, inv_l);
+          stage16(16 * c, v, inv_l);
         }
         tc_fence_before();
         if (FUSED) mbar_arrive(&bars[kBarEpiDone]);
+        flush_rows();
       } else {
         // Cut unit: the schedule cuts a unit at most once, into two pieces
         // that may run in different CTAs.  Each query tile has its own
@@ -769,8 +791,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
               v[4 * q + 2] = fa * a.z + fb * b.z;
               v[4 * q + 3] = fa * a.w + fb * b.w;
             }
-            store16(16 * cc, v, inv_l);
+            stage16(16 * cc, v, inv_l);
           }
+          flush_rows();
         };
         unsigned long long* counter = args.counters + 2 * static_cast<size_t>(sg.u) + wg;
         if (r == 0) {
