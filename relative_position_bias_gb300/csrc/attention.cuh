@@ -10,14 +10,17 @@
 // K/V tile the CTA streams.  The kernel is persistent: CTA c runs the
 // contiguous range [c*T/G, (c+1)*T/G) of the T = units x key-tiles iteration
 // space (stream-K), so all CTAs get the same number of key tiles whatever the
-// unit count.  A unit cut between CTAs leaves partial results (unnormalised O,
-// row max, row sum) in the caller's workspace; the CTA that finishes a unit
-// last merges them.  With one CTA per unit (no workspace) every segment is a
-// whole unit and nothing is written to the workspace.
+// unit count.  A unit cut between two CTAs: the piece that finishes first
+// publishes its partial results (unnormalised O, row max, row sum) to the
+// caller's workspace; the piece that finishes second merges them with its own
+// O straight from TMEM (or, if both had to publish, from both slots).  With
+// one CTA per unit (no workspace) every segment is a whole unit and nothing
+// is written to the workspace.
 //
-// Warp roles (384 threads):
+// Warp roles (384 threads; warps 0-3 run with 104 registers, the softmax
+// warpgroups with 200, set by setmaxnreg):
 //   warp 0      TMA producer: Q pair, [tables,] K/V ring (3 stages)
-//   warp 1      tcgen05.mma issuer (one thread)
+//   warp 1      tcgen05.mma issuer (the warp walks the loop, an elected lane issues)
 //   warp 2      TMEM allocator; with warp 3, converts bf16 V tiles to fp16
 //   warps 4-7   softmax / epilogue of query tile 0 (one thread per row)
 //   warps 8-11  softmax / epilogue of query tile 1
