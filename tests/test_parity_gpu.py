@@ -225,6 +225,19 @@ def test_split_schedule_ragged(entry, BH):
     check_out(_select(o32, heads_s, rows), want, what=f"split {entry} {w.BH} heads")
 
 
+@pytest.mark.parametrize("name", list(I.WORKLOADS))
+def test_workspace_size_formula(name):
+    """The reported scratch is the documented layout: an 8-byte counter per query tile of each
+    unit (256-byte aligned), then two 66-float-per-row slots per CTA and query tile; zero when the
+    units fill whole waves of one CTA per SM."""
+    w = I.WORKLOADS[name]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    units = w.BH * ((-(-w.N // 128) + 1) // 2)
+    split = units > sms and units % sms != 0
+    want = ((16 * units + 255) // 256 * 256 + 2 * sms * 2 * 128 * 66 * 4) if split else 0
+    assert rpb.workspace_size(w.BH, w.H, w.W) == want
+
+
 def test_caller_workspace_and_reuse():
     """A caller-owned workspace gives the same bytes as the cached one, call after call."""
     w = I.WORKLOADS["global64"]
