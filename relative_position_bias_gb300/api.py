@@ -27,7 +27,7 @@ STATUS_NAMES = {0: "DERA_OK", 1: "DERA_ERR_NULL", 2: "DERA_ERR_SHAPE", 3: "DERA_
 
 _lib = None
 _lock = threading.Lock()
-_workspaces: dict = {}    # device index -> uint8 tensor reused by every call on that device
+_workspaces: dict = {}    # (device index, stream handle) -> uint8 scratch reused by the calls on that stream
 
 
 class DeraError(RuntimeError):
@@ -107,8 +107,13 @@ def workspace_size(BH: int, H: int, W: int, head_dim: int = 64) -> int:
     return n.value
 
 
-def _workspace(device: torch.device, BH: int, H: int, W: int, d: int, workspace):
-    """(pointer, bytes) of the scratch for one call: the caller's tensor, none, or a cached per-device buffer."""
+def _workspace(device: torch.device, BH: int, H: int, W: int, d: int, workspace, stream_handle):
+    """(pointer, bytes) of the scratch for one call: the caller's tensor, none, or a cached buffer.
+
+    The cached buffer is kept per (device, stream): calls on one stream are ordered by it, and
+    calls on different streams, which may overlap on the GPU, never share scratch.  A buffer used
+    on a stream other than the one current at its allocation is recorded on that stream, so the
+    allocator does not hand its memory out again before that stream's work is done."""
     if workspace is False or device.type != "cuda" or BH == 0:
         return None, 0
     if isinstance(workspace, torch.Tensor):
@@ -118,10 +123,14 @@ def _workspace(device: torch.device, BH: int, H: int, W: int, d: int, workspace)
     if need == 0:
         return None, 0
     idx = device.index if device.index is not None else torch.cuda.current_device()
-    buf = _workspaces.get(idx)
-    if buf is None or buf.numel() < need:
-        buf = torch.empty(need, dtype=torch.uint8, device=device)
-        _workspaces[idx] = buf
+    key = (idx, int(stream_handle or 0))
+    with _lock:
+        buf = _workspaces.get(key)
+        if buf is None or buf.numel() < need:
+            buf = torch.empty(need, dtype=torch.uint8, device=device)
+            if int(stream_handle or 0) != torch.cuda.current_stream(device).cuda_stream:
+                buf.record_stream(torch.cuda.ExternalStream(int(stream_handle or 0), device=device))
+            _workspaces[key] = buf
     return buf.data_ptr(), buf.numel()
 
 
@@ -159,8 +168,8 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, rel_h: torch.Te
               out: torch.Tensor | None = None, stream=None, workspace=None) -> torch.Tensor:
     """Attention with a compact bias via ``dera_relpos_attention``.
 
-    ``workspace``: None = a cached per-device scratch buffer (allocated once),
-    False = no scratch (one CTA per unit), or a caller-owned uint8 tensor."""
+    ``workspace``: None = a cached scratch buffer per (device, stream), False = no scratch (one
+    CTA per unit), or a caller-owned uint8 tensor, which no other call in flight may use."""
     BH, N, d = q.shape
     scale = d ** -0.5 if scale is None else scale
     if out is None:
@@ -174,10 +183,11 @@ def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, rel_h: torch.Te
     if rel_h.dtype != rel_w.dtype:
         raise TypeError("rel_h and rel_w must share a dtype")
     lib = load_library()
-    ws, ws_bytes = _workspace(q.device, BH, H, W, d, workspace)
+    st = _stream(q.device, stream)
+    ws, ws_bytes = _workspace(q.device, BH, H, W, d, workspace, st)
     _check(lib.dera_relpos_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(rel_h), _ptr(rel_w), _ptr(out), BH, H, W, d,
                                      float(scale), _code(q.dtype), _code(rel_h.dtype), _code(out.dtype), ws,
-                                     ws_bytes, _stream(q.device, stream)))
+                                     ws_bytes, st))
     return out
 
 
@@ -197,10 +207,10 @@ def fused(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, rel_pos_h: torch.Te
         if t.dtype != q.dtype:
             raise TypeError("q, k, v and the tables must share a dtype")
     lib = load_library()
-    ws, ws_bytes = _workspace(q.device, BH, H, W, d, workspace)
+    st = _stream(q.device, stream)
+    ws, ws_bytes = _workspace(q.device, BH, H, W, d, workspace, st)
     _check(lib.dera_relpos_fused(_ptr(q), _ptr(k), _ptr(v), _ptr(rel_pos_h), _ptr(rel_pos_w), _ptr(out), BH, H, W,
-                                 d, float(scale), _code(q.dtype), _code(out.dtype), ws, ws_bytes,
-                                 _stream(q.device, stream)))
+                                 d, float(scale), _code(q.dtype), _code(out.dtype), ws, ws_bytes, st))
     return out
 
 

@@ -33,6 +33,7 @@
 namespace dera {
 
 constexpr int kStages = 3;
+constexpr int kTilesPerUnit = 2;  // 128-row query tiles per work unit
 constexpr int kAttnThreads = 384;
 // Largest accepted row sum of a speculative tile: with the sum at most this,
 // every p rounds to at most 65504, the largest finite fp16.

@@ -165,10 +165,12 @@ bool map_table(CUtensorMap* m, const void* p, dera_dtype t, int L) {
 int padded_width(int W) { return W <= 16 ? 16 : (W <= 32 ? 32 : (W <= 40 ? 40 : 64)); }
 int rows_per_tile(int WP) { return WP <= 16 ? 8 : (WP <= 32 ? 4 : 2); }
 
-// Streaming-multiprocessor count of a device (cached).
+// Streaming-multiprocessor count of a device (cached; 0 if the query fails).
 int sm_count(int dev) {
   static int counts[kMaxDevices] = {};
+  static std::mutex mu;
   if (dev < 0 || dev >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lock(mu);
   if (counts[dev] == 0) {
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
@@ -458,10 +460,14 @@ dera_status dera_relpos_fused_noalloc(const void* q, const void* k, const void* 
   DERA_TRY(check_host({q, k, v, rel_pos_h, rel_pos_w, out}));
   int dev = 0;
   DERA_TRY(current_device(&dev));
+  // The size limit is decided before any pointer is examined, and a device whose SM count
+  // cannot be read is refused (that count sizes the schedule and its scratch).
+  const int sms = sm_count(dev);
+  if (sms <= 0) return DERA_ERR_CUDA;
+  const size_t need = workspace_bytes_for(make_plan(BH, H, W, sms));
+  if (need > DERA_NOALLOC_SCRATCH_BYTES) return DERA_ERR_SCRATCH;
   for (const void* p : {q, k, v, rel_pos_h, rel_pos_w, static_cast<const void*>(out)})
     DERA_TRY(check_ptr(p, dev));
-  const size_t need = workspace_bytes_for(make_plan(BH, H, W, sm_count(dev)));
-  if (need > DERA_NOALLOC_SCRATCH_BYTES) return DERA_ERR_SCRATCH;
   void* scratch = nullptr;
   if (need > 0) {
     scratch = noalloc_scratch(dev);

@@ -16,12 +16,16 @@ relative L2 1e-2 against the float64 oracle):
 """
 from __future__ import annotations
 
+import re
+from pathlib import Path
+
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import relative_position_bias_gb300 as rpb
+from conftest import record_margin
 from relative_position_bias_gb300 import build as rbuild
 from relative_position_bias_gb300 import inputs as I
 
@@ -58,6 +62,7 @@ def check_out(got32: torch.Tensor, want: np.ndarray, got16: torch.Tensor | None 
     assert np.isfinite(g).all(), f"{what}: non-finite output"
     err = np.abs(g - want)
     rl2 = np.linalg.norm(g - want) / max(np.linalg.norm(want), 1e-300)
+    record_margin(what, err.max(), rl2)
     assert err.max() <= ABS_TOL, f"{what}: max-abs {err.max():.3e}"
     assert rl2 <= RL2_TOL, f"{what}: rel-L2 {rl2:.3e}"
     if got16 is not None:
@@ -69,13 +74,40 @@ def check_out(got32: torch.Tensor, want: np.ndarray, got16: torch.Tensor | None 
     return float(err.max()), float(rl2)
 
 
-def sample_rows(w: I.Workload, n_heads: int = 4, n_rows: int = 96, seed: int = 0):
-    """Heads and token rows for sampled checks: first/last tile rows, ragged tail and random rows."""
+_ATTN_SRC = Path(__file__).resolve().parents[1] / "relative_position_bias_gb300" / "csrc" / "attention.cuh"
+
+
+def query_tiles_per_unit() -> int:
+    """Query tiles (of 128 rows) in one work unit of the attention kernel's schedule."""
+    m = re.search(r"constexpr int kTilesPerUnit = (\d+);", _ATTN_SRC.read_text())
+    assert m, "kTilesPerUnit not found"
+    return int(m.group(1))
+
+
+def tail_heads(w: I.Workload) -> set[int]:
+    """Heads with a unit in the stream-K tail of the default (workspace) schedule, restated from
+    the host plan: units are groups of query tiles of one head, the tail is the last one and a
+    fraction waves of units when they do not fill whole waves of one CTA per SM.  Cut units only
+    occur there."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    per = query_tiles_per_unit()
+    units_per_head = (-(-w.N // 128) + per - 1) // per
+    U = w.BH * units_per_head
+    if not (U > sms and U % sms != 0):
+        return set()
+    first_tail = max(U // sms - 1, 0) * sms
+    return {u // units_per_head for u in range(first_tail, U)}
+
+
+def dense_heads(w: I.Workload, at_least: int = 16, seed: int = 0) -> list[int]:
+    """Heads checked on every row: the first and last heads, every head holding a tail (possibly
+    cut) unit, and random others up to `at_least`."""
     r = np.random.default_rng(seed)
-    heads = sorted({0, w.BH - 1, *r.choice(w.BH, size=min(n_heads, w.BH), replace=False).tolist()})
-    fixed = [0, 1, 127, 128, 255, 256, w.N - 129, w.N - 128, w.N - 2, w.N - 1]
-    rows = sorted({x for x in fixed if 0 <= x < w.N} | set(r.choice(w.N, size=n_rows, replace=False).tolist()))
-    return heads, np.array(rows)
+    heads = {0, 1, w.BH - 1} | tail_heads(w)
+    heads = {h for h in heads if 0 <= h < w.BH}
+    rest = [h for h in r.permutation(w.BH).tolist() if h not in heads]
+    heads |= set(rest[:max(0, at_least - len(heads))])
+    return sorted(heads)
 
 
 # --------------------------------------------------------------------------- projection
@@ -105,28 +137,19 @@ def test_project_16bit_bias(bias_dtype):
 
 
 # --------------------------------------------------------------------------- full workloads
-def _oracle_full_or_rows(w, f, entry, rel=None):
-    """Whole oracle output when it is cheap, else (heads, rows, values) sampled."""
-    if w.BH * w.N * w.N <= 12 * 4096 * 4096:
-        if entry == "fused":
-            return None, None, oracle.fused(f["q"], f["k"], f["v"], f["rel_pos_h"], f["rel_pos_w"], w.H, w.W, w.scale)
-        return None, None, oracle.attention(f["q"], f["k"], f["v"], rel[0], rel[1], w.H, w.W, w.scale)
-    heads, rows = sample_rows(w)
-    vals = []
-    for b in heads:
-        if entry == "fused":
-            vals.append(oracle.fused_rows(f["q"], f["k"], f["v"], f["rel_pos_h"], f["rel_pos_w"], b, rows, w.H, w.W,
-                                          w.scale))
-        else:
-            vals.append(oracle.attention_rows(f["q"], f["k"], f["v"], rel[0][b][rows], rel[1][b][rows], b, rows,
-                                              w.H, w.W, w.scale))
-    return heads, rows, np.stack(vals)
+def _oracle_full_or_heads(w, f, entry, rel=None):
+    """Whole oracle output when it is cheap, else every row of the heads `dense_heads` picks."""
+    heads = None if w.BH * w.N * w.N <= 12 * 4096 * 4096 else dense_heads(w)
+    sel = (lambda a: a) if heads is None else (lambda a: a[heads])
+    if entry == "fused":
+        want = oracle.fused(sel(f["q"]), sel(f["k"]), sel(f["v"]), f["rel_pos_h"], f["rel_pos_w"], w.H, w.W, w.scale)
+    else:
+        want = oracle.attention(sel(f["q"]), sel(f["k"]), sel(f["v"]), sel(rel[0]), sel(rel[1]), w.H, w.W, w.scale)
+    return heads, want
 
 
-def _select(t: torch.Tensor, heads, rows):
-    if heads is None:
-        return t
-    return t[heads][:, rows]
+def _select(t: torch.Tensor, heads):
+    return t if heads is None else t[heads]
 
 
 @pytest.mark.parametrize("split", [True, False], ids=["workspace", "no-workspace"])
@@ -144,8 +167,9 @@ def test_fused_parity(name, split):
     torch.cuda.synchronize()
     # every row, not only the sampled ones, must be finite
     assert bool(torch.isfinite(o32).all()) and bool(torch.isfinite(o16).all()), f"fused {name}: non-finite output"
-    heads, rows, want = _oracle_full_or_rows(w, _f64(x), "fused")
-    check_out(_select(o32, heads, rows), want, _select(o16, heads, rows), what=f"fused {name}")
+    heads, want = _oracle_full_or_heads(w, _f64(x), "fused")
+    check_out(_select(o32, heads), want, _select(o16, heads),
+              what=f"fused {name} {'workspace' if split else 'no-workspace'}" + ("" if heads is None else f" ({len(heads)} heads)"))
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
@@ -214,15 +238,15 @@ def test_split_schedule_ragged(entry, BH):
         o32 = rpb.fused(d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W, w.scale,
                         out_dtype=torch.float32)
         torch.cuda.synchronize()
-        heads_s, rows, want = _oracle_full_or_rows(w, f, "fused")
+        heads_s, want = _oracle_full_or_heads(w, f, "fused")
     else:
         rh, rw = oracle.project(f["q"], f["rel_pos_h"], f["rel_pos_w"], w.H, w.W)
         rh32, rw32 = torch.from_numpy(rh).float(), torch.from_numpy(rw).float()
         o32 = rpb.attention(d["q"], d["k"], d["v"], rh32.cuda(), rw32.cuda(), w.H, w.W, w.scale,
                             out_dtype=torch.float32)
         torch.cuda.synchronize()
-        heads_s, rows, want = _oracle_full_or_rows(w, f, "attention", (rh32.double().numpy(), rw32.double().numpy()))
-    check_out(_select(o32, heads_s, rows), want, what=f"split {entry} {w.BH} heads")
+        heads_s, want = _oracle_full_or_heads(w, f, "attention", (rh32.double().numpy(), rw32.double().numpy()))
+    check_out(_select(o32, heads_s), want, what=f"split {entry} {w.BH} heads")
 
 
 @pytest.mark.parametrize("name", list(I.WORKLOADS))
@@ -253,7 +277,31 @@ def test_caller_workspace_and_reuse():
     alt = rpb.fused(*args, out_dtype=torch.float32, workspace=small)
     torch.cuda.synchronize()
     f = _f64(I.make_inputs(w))
-    check_out(alt, oracle.fused(f["q"], f["k"], f["v"], f["rel_pos_h"], f["rel_pos_w"], w.H, w.W, w.scale))
+    check_out(alt, oracle.fused(f["q"], f["k"], f["v"], f["rel_pos_h"], f["rel_pos_w"], w.H, w.W, w.scale),
+              what="fused global64 workspace too small")
+
+
+def test_default_workspace_per_stream():
+    """Calls on two streams that overlap on the GPU each get their own cached scratch, so both
+    match a serial call bit for bit."""
+    w = I.WORKLOADS["global64"]
+    assert rpb.workspace_size(w.BH, w.H, w.W) > 0, "this workload must use the split schedule"
+    d = _dev(I.make_inputs(w))
+    d2 = _dev(I.make_inputs(w, seed=1))
+    ref1 = rpb.fused(d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W, w.scale)
+    ref2 = rpb.fused(d2["q"], d2["k"], d2["v"], d2["rel_pos_h"], d2["rel_pos_w"], w.H, w.W, w.scale)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    for _ in range(3):
+        with torch.cuda.stream(s1):
+            a = rpb.fused(d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W, w.scale)
+        with torch.cuda.stream(s2):
+            b = rpb.fused(d2["q"], d2["k"], d2["v"], d2["rel_pos_h"], d2["rel_pos_w"], w.H, w.W, w.scale)
+        outs.append((a, b))
+    torch.cuda.synchronize()
+    for a, b in outs:
+        assert torch.equal(a, ref1) and torch.equal(b, ref2)
 
 
 @pytest.mark.parametrize("entry", ["fused", "attention"])
@@ -298,8 +346,9 @@ def test_attention_parity_f32_bias(name):
     o16 = rpb.attention(d["q"], d["k"], d["v"], rh32.cuda(), rw32.cuda(), w.H, w.W, w.scale)
     torch.cuda.synchronize()
     rel = (rh32.double().numpy(), rw32.double().numpy())
-    heads, rows, want = _oracle_full_or_rows(w, f, "attention", rel)
-    check_out(_select(o32, heads, rows), want, _select(o16, heads, rows), what=f"attention {name}")
+    heads, want = _oracle_full_or_heads(w, f, "attention", rel)
+    check_out(_select(o32, heads), want, _select(o16, heads),
+              what=f"attention {name}" + ("" if heads is None else f" ({len(heads)} heads)"))
 
 
 @pytest.mark.parametrize("bias_dtype", [torch.bfloat16, torch.float16])
@@ -441,4 +490,5 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     out = rpb.fused(d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W, w.scale, out_dtype=torch.float32)
     torch.cuda.synchronize()
     f = _f64(x)
-    check_out(out, oracle.fused(f["q"], f["k"], f["v"], f["rel_pos_h"], f["rel_pos_w"], w.H, w.W, w.scale))
+    check_out(out, oracle.fused(f["q"], f["k"], f["v"], f["rel_pos_h"], f["rel_pos_w"], w.H, w.W, w.scale),
+              what="fused grid16 after a timed-out wait")

@@ -44,7 +44,6 @@ def test_noalloc_matches_fused_on_two_calls():
     lib = rpb.load_library()
     fn = _noalloc(lib)
     w = I.WORKLOADS["global64"]
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert rpb.workspace_size(w.BH, w.H, w.W) > 0, "this workload must use the split schedule"
     x = I.make_inputs(w)
     d = {k: t.cuda() for k, t in x.items()}
@@ -66,23 +65,25 @@ def test_noalloc_matches_fused_on_two_calls():
         assert err.max() <= ABS_TOL, f"call {call}: max-abs {err.max():.3e} vs dera_relpos_fused"
         assert np.linalg.norm(got - refn) / np.linalg.norm(refn) <= RL2_TOL
     assert rpb.device_status() == 0
-    del sms
 
 
 def test_noalloc_rejects_problems_beyond_its_buffer():
     rbuild.build()
     lib = rpb.load_library()
     fn = _noalloc(lib)
-    # Valid device pointers, but a head count whose unit counters alone exceed
-    # the 24 MiB buffer: refused before anything is enqueued.
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    BH = 9_000_001   # 64x64 grid: 16 units per head -> 144 M units
-    while (16 * BH) % sms == 0:
+    # A head count whose unit counters alone exceed the 24 MiB buffer: refused before anything
+    # is enqueued.  The pointers are 16-byte aligned pinned HOST memory, so even if the size
+    # check ever stopped firing, the device-memory check would still refuse the call
+    # (DERA_ERR_DEVICE) and nothing could be launched on them.
+    BH = 9_000_001   # 64x64 grid: millions of units
+    need = rpb.workspace_size(BH, 64, 64)
+    if need == 0:    # whole waves on this device: nudge the count so the split schedule applies
         BH += 1
-    # The call must be refused, never launched: its pointers cover 32 bytes.
-    assert rpb.workspace_size(BH, 64, 64) > 24 * 1024 * 1024
-    t = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
+        need = rpb.workspace_size(BH, 64, 64)
+    assert need > 24 * 1024 * 1024
+    t = torch.zeros(64, dtype=torch.bfloat16).pin_memory()
     p = t.data_ptr()
+    assert p % 16 == 0
     st = fn(p, p, p, p, p, p, BH, 64, 64, 64, 0.125, DERA_BF16, DERA_BF16, torch.cuda.current_stream().cuda_stream)
     assert st == DERA_ERR_SCRATCH, lib.dera_status_string(st).decode()
     assert "scratch" in lib.dera_status_string(st).decode()
