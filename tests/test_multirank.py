@@ -1,19 +1,26 @@
-"""Host logic of the multi-rank benchmark, on CPU with gloo (world size 2).
+"""Multi-rank host logic on CPU with gloo (world sizes 2 and 3).
 
-The path shards into independent replicas (one workload per GPU, no data
-exchange); the only cross-rank operations are the barrier and the max over
-ranks of the timed duration, which these tests exercise."""
+One call's (batch, head) problems are independent, so they are split into
+contiguous ranges, one per rank, with no exchange while computing; a consumer
+that needs the whole output gathers the slices afterwards.  These tests check
+the partition (every problem exactly once, uneven counts), that the gathered
+result equals a single-rank computation of the whole call, and the benchmark's
+cross-rank steps (barrier, max over ranks of the timed duration)."""
 from __future__ import annotations
 
 import json
 import os
 import socket
 
+import numpy as np
 import pytest
+import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
 
 import bench
+import oracle
+from relative_position_bias_gb300 import shard
 
 
 def _free_port() -> int:
@@ -66,3 +73,67 @@ def test_reference_arm_other_ranks_exit_quietly(capsys, monkeypatch):
     monkeypatch.setenv("WORLD_SIZE", "2")
     assert bench.main(["--impl", "reference", "--steps", "3", "--warmup", "3", "--workload", "grid16"]) == 0
     assert capsys.readouterr().out.strip() == ""
+
+
+# --------------------------------------------------------------------------- BH partition of one call
+@pytest.mark.parametrize("world", [1, 2, 3, 4, 5, 8])
+def test_bh_ranges_tile_the_call(world):
+    for BH in list(range(0, 40)) + [96, 192, 1001]:
+        seen = []
+        sizes = []
+        for r in range(world):
+            lo, hi = shard.bh_range(BH, r, world)
+            assert 0 <= lo <= hi <= BH
+            seen.extend(range(lo, hi))
+            sizes.append(hi - lo)
+        assert seen == list(range(BH))            # every (batch, head) exactly once, in order
+        assert max(sizes) - min(sizes) <= 1
+
+
+def test_bh_range_rejects_bad_ranks():
+    with pytest.raises(ValueError):
+        shard.bh_range(8, 2, 2)
+    with pytest.raises(ValueError):
+        shard.bh_range(8, 0, 0)
+    with pytest.raises(ValueError):
+        shard.bh_range(-1, 0, 1)
+
+
+def _oracle_compute(q, k, v, th, tw, H, W, scale, **_):
+    """CPU stand-in for one rank's device computation (the float64 oracle on the slice)."""
+    out = oracle.fused(q.double().numpy(), k.double().numpy(), v.double().numpy(), th.double().numpy(),
+                       tw.double().numpy(), H, W, scale)
+    return torch.from_numpy(out)
+
+
+def _shard_case(BH, H=3, W=4, d=8, seed=5):
+    g = torch.Generator().manual_seed(seed)
+    N = H * W
+    q, k, v = (torch.randn(BH, N, d, generator=g) for _ in range(3))
+    th, tw = 0.5 * torch.randn(2 * H - 1, d, generator=g), 0.5 * torch.randn(2 * W - 1, d, generator=g)
+    return q, k, v, th, tw, H, W, d ** -0.5
+
+
+def _shard_worker(rank: int, world: int, port: int, out_dir: str, BH: int):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    q, k, v, th, tw, H, W, scale = _shard_case(BH)
+    part = shard.fused_shard(q, k, v, th, tw, H, W, scale, compute=_oracle_compute)
+    full = shard.fused_shard(q, k, v, th, tw, H, W, scale, gather=True, compute=_oracle_compute)
+    lo, hi = shard.bh_range(BH, rank, world)
+    torch.save({"lo": lo, "hi": hi, "part": part, "full": full}, os.path.join(out_dir, f"s{rank}.pt"))
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world,BH", [(2, 7), (3, 7), (3, 2), (2, 12)])
+def test_sharded_call_gathers_to_the_single_rank_result(tmp_path, world, BH):
+    mp.spawn(_shard_worker, args=(world, _free_port(), str(tmp_path), BH), nprocs=world, join=True)
+    q, k, v, th, tw, H, W, scale = _shard_case(BH)
+    want = _oracle_compute(q, k, v, th, tw, H, W, scale)
+    got = [torch.load(tmp_path / f"s{r}.pt") for r in range(world)]
+    covered = []
+    for r, rec in enumerate(got):
+        assert torch.equal(rec["full"], want), f"rank {r}: gathered output differs from the single-rank call"
+        assert torch.equal(rec["part"], want[rec["lo"]:rec["hi"]])
+        covered.extend(range(rec["lo"], rec["hi"]))
+    assert covered == list(range(BH))

@@ -224,11 +224,11 @@ def test_late_large_scores(entry, case, dtype):
 @pytest.mark.parametrize("BH", [None, 1, 2, 3], ids=["sms+1", "sms+sms/2", "2sms+1", "3sms-1"])
 def test_split_schedule_ragged(entry, BH):
     """Unit counts just past whole waves of the device, on a ragged 40x40 grid
-    (7 query-tile pairs per head), so most units are cut between two CTAs."""
+    (13 query tiles per head), so most units are cut between two CTAs."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    pairs = 7
+    per_head = (-(-1600 // 128) + query_tiles_per_unit() - 1) // query_tiles_per_unit()
     units = {None: sms + 1, 1: sms + sms // 2, 2: 2 * sms + 1, 3: 3 * sms - 1}[BH]
-    heads = -(-units // pairs)
+    heads = -(-units // per_head)
     w = I.WORKLOADS["ragged40"].with_grid(40, 40, B=1, heads=heads)
     assert rpb.workspace_size(w.BH, w.H, w.W) > 0
     x = I.make_inputs(w, seed=heads)
@@ -251,14 +251,15 @@ def test_split_schedule_ragged(entry, BH):
 
 @pytest.mark.parametrize("name", list(I.WORKLOADS))
 def test_workspace_size_formula(name):
-    """The reported scratch is the documented layout: an 8-byte counter per query tile of each
-    unit (256-byte aligned), then two 66-float-per-row slots per CTA and query tile; zero when the
-    units fill whole waves of one CTA per SM."""
+    """The reported scratch is the documented layout: an 8-byte counter per unit (256-byte
+    aligned), then two 66-float-per-row slots of one query tile per CTA; zero when the units fill
+    whole waves of one CTA per SM."""
     w = I.WORKLOADS[name]
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    units = w.BH * ((-(-w.N // 128) + 1) // 2)
+    per = query_tiles_per_unit()
+    units = w.BH * ((-(-w.N // 128) + per - 1) // per)
     split = units > sms and units % sms != 0
-    want = ((16 * units + 255) // 256 * 256 + 2 * sms * 2 * 128 * 66 * 4) if split else 0
+    want = ((8 * units + 255) // 256 * 256 + 2 * sms * 128 * 66 * 4) if split else 0
     assert rpb.workspace_size(w.BH, w.H, w.W) == want
 
 
