@@ -6,43 +6,27 @@
 // 实现拆解 item 1 and 关键源码片段).  The softmax is online, in base 2, with
 // fp32 statistics (section 风险与影响).
 //
-// Work unit: one 128-row query tile of one head.  The kernel is persistent:
-// all but the last one-and-a-fraction waves of units run as data-parallel
-// rounds, the rest as a stream-K tail of (unit, key tile) iterations cut into
-// one equal-cost range per CTA.  A unit cut between two CTAs: the piece that
-// finishes first publishes its partial result (unnormalised O, row max, row
-// sum) to the caller's workspace; the piece that finishes second merges.
-//
-// Every key tile is split by columns into two halves of whole grid rows.  Each
-// half is an independent online softmax over its keys, run by its own four
-// warps (one thread per row), with its own running maximum, row sum and O
-// accumulator in TMEM; the two are merged once, at the end of the segment.  So
-// the eight softmax warps share every tile without exchanging anything per tile.
+// Work unit: a pair of 128-row query tiles of one head; both tiles share every
+// K/V tile the CTA streams.  The kernel is persistent: CTA c runs the
+// contiguous range [c*T/G, (c+1)*T/G) of the T = units x key-tiles iteration
+// space (stream-K), so all CTAs get the same number of key tiles whatever the
+// unit count.  A unit cut between two CTAs: the piece that finishes first
+// publishes its partial results (unnormalised O, row max, row sum) to the
+// caller's workspace; the piece that finishes second merges them with its own
+// O straight from TMEM (or, if both had to publish, from both slots).  With
+// one CTA per unit (no workspace) every segment is a whole unit and nothing
+// is written to the workspace.
 //
 // Warp roles (384 threads; warps 0-3 run with 104 registers, the softmax
-// warps with 200, set by setmaxnreg):
-//   warp 0      TMA producer: Q tile, [tables,] K ring and V ring
+// warpgroups with 200, set by setmaxnreg):
+//   warp 0      TMA producer: Q pair, [tables,] K/V ring (3 stages)
 //   warp 1      tcgen05.mma issuer (the warp walks the loop, an elected lane issues)
 //   warp 2      TMEM allocator; with warp 3, converts bf16 V tiles to fp16
-//   warps 4-7   softmax of column half 0 (grid rows 0 .. KHT/2 - 1 of each tile)
-//   warps 8-11  softmax of column half 1
-// TMEM (512 columns): S0 [0,128) S1 [128,256)   scores of key tiles t (t even / odd)
-//                     P0 [256,320) P1 [320,384) fp16 P of tiles t (even / odd), half h at +HALF/2*h
-//                     O_0 [384,448) O_1 [448,512) unnormalised output of half 0 / half 1
-// S and P are double-buffered, so QK^T of tile t + 2 is issued as soon as both
-// halves have read S(t), never behind a P.V product; the fused prologue's
-// q.table^T products use S0 and S1 before the segment's first QK^T.
-//
-// Softmax range: each tile is exponentiated against the half's running
-// maximum and P is rounded to fp16.  A segment's first tile starts the maximum
-// from a rel_h-aware estimate that may sit up to kStartCap above the exact
-// maximum; later tiles are exponentiated at once and redone exactly only if
-// their row sum passes kSpecSumLimit.  At the end of a segment the merged row
-// sum l (in units of the final maximum) bounds the error that fp16 rounding
-// and flushing of P can cause: at most 2^-11 relative, plus 2^-25 per key
-// over l.  A segment whose l falls below kMinRowSum on any row is not stored;
-// it is run again at the end of the CTA's work with no overshoot (cap 0),
-// which keeps l >= 1, and the CTA's later segments use cap 0 as well.
+//   warps 4-7   softmax / epilogue of query tile 0 (one thread per row)
+//   warps 8-11  softmax / epilogue of query tile 1
+// TMEM (512 columns): S0 [0,128) S1 [128,256) P0 [256,320) P1 [320,384)
+//                     O0 [384,448) O1 [448,512); the fused prologue uses all
+//                     512 columns for G_i = Q_i [T_h ; T_w]^T before each segment.
 #pragma once
 #include <cfloat>
 
@@ -50,24 +34,27 @@
 
 namespace dera {
 
-constexpr int kTilesPerUnit = 1;  // 128-row query tiles per work unit
-constexpr int kRing = 5;          // depth of the K ring and of the V ring
+constexpr int kStages = 3;
+constexpr int kTilesPerUnit = 2;  // 128-row query tiles per work unit
 constexpr int kAttnThreads = 384;
 // Largest accepted row sum of a speculative tile: with the sum at most this,
 // every p rounds to at most 65504, the largest finite fp16.
 constexpr float kSpecSumLimit = 65000.0f;
 // Starting row maximum of a segment (base 2): at most kStartCap above the
-// exact maximum of its first key tile; kStartMargin below the estimate.
+// exact maximum of its first key tile, which keeps that tile's largest p at or
+// above 2^-12, inside the fp16 normal range; kStartMargin below the estimate.
 constexpr float kStartCap = 12.0f;
 constexpr float kStartMargin = 4.0f;
-// Smallest accepted merged row sum at the end of a segment (see above).
-constexpr float kMinRowSum = 0.25f;
-constexpr int kBiasStride = 66;       // floats per row of the bias staging area
+// Row-sum check at the end of a segment: the row sum l, in units of the
+// running maximum, must be at least the segment's valid key count times
+// 2^kMinRowSumLog2 (see the epilogue).
+constexpr int kMinRowSumLog2 = -16;
+constexpr int kBiasStride = 66;       // floats per row of a bias staging area
 // Register split: the producer / MMA / V-conversion warpgroup gives registers
-// back and the softmax warps take them.  The block launches with kLaunchRegs
-// per thread (the most that 384 threads get); the host checks the compiled
-// count before the first launch, since a split larger than the launch pool
-// would block forever.
+// back and the two softmax warpgroups take them, which removes the softmax's
+// spills.  The block launches with kLaunchRegs per thread (the most that 384
+// threads get); the host checks the compiled count before the first launch,
+// since a split larger than the launch pool would block forever.
 constexpr int kLaunchRegs = 168;
 constexpr int kRegsCtl = 104;
 constexpr int kRegsSmx = 200;
@@ -75,18 +62,16 @@ static_assert(kRegsCtl * 128 + kRegsSmx * 256 <= kLaunchRegs * kAttnThreads, "re
 static_assert(kRegsCtl % 8 == 0 && kRegsSmx % 8 == 0, "setmaxnreg counts are multiples of 8");
 
 struct AttnSmem {
-  static constexpr int kQ = 0;                                    // 16 KB
-  static constexpr int kK = kTileBytes;                           // kRing x 16 KB
-  static constexpr int kV = kK + kRing * kTileBytes;              // kRing x 16 KB
-  static constexpr int kBias = kV + kRing * kTileBytes;           // 128 x 66 floats
-  static constexpr int kBiasBytes = kBlockM * kBiasStride * 4;
-  static constexpr int kXchg = kBias + kBiasBytes;                // [2 halves][128] float2 (m, l)
-  static constexpr int kXchgBytes = 2 * kBlockM * 8;
-  static constexpr int kBars = kXchg + kXchgBytes;
-  static constexpr int kNumBars = 48;
-  static constexpr int kMisc = kBars + kNumBars * 8;              // flags and the replay segment
-  static constexpr int kTotal = kMisc + 64;
-  static constexpr int kAlloc = kTotal + 1024;                    // slack for 1 KB alignment
+  static constexpr int kQ = 0;                                   // 2 x 16 KB
+  static constexpr int kRing = 2 * kTileBytes;                   // stages: [K 16 KB][V 16 KB]
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kBias = kRing + kStages * kStageBytes;    // 2 x 128 x 66 floats
+  static constexpr int kBiasBytes = 2 * kBlockM * kBiasStride * 4;
+  static constexpr int kBars = kBias + kBiasBytes;
+  static constexpr int kNumBars = 32;
+  static constexpr int kMisc = kBars + kNumBars * 8;             // tmem slot, flags, replay records
+  static constexpr int kTotal = kMisc + 96;
+  static constexpr int kAlloc = kTotal + 1024;                   // slack for 1 KB alignment
 };
 static_assert(AttnSmem::kAlloc <= 232448, "shared memory budget");
 
@@ -94,21 +79,19 @@ static_assert(AttnSmem::kAlloc <= 232448, "shared memory budget");
 enum : int {
   kBarQFull = 0,
   kBarQEmpty = 1,
-  kBarKFull = 2,                        // + ring slot
-  kBarKEmpty = kBarKFull + kRing,
-  kBarVFull = kBarKEmpty + kRing,
-  kBarVEmpty = kBarVFull + kRing,
-  kBarVReady = kBarVEmpty + kRing,
-  kBarSFull = kBarVReady + kRing,       // + S buffer
-  kBarPFull = kBarSFull + 2,            // + 2 * half + P buffer
-  kBarODone = kBarPFull + 4,            // + 2 * half + P buffer
-  kBarGFull = kBarODone + 4,
+  kBarKVFull = 2,                     // + stage
+  kBarKVEmpty = kBarKVFull + kStages,
+  kBarVReady = kBarKVEmpty + kStages,
+  kBarSFull = kBarVReady + kStages,   // + tile
+  kBarPFull = kBarSFull + 2,
+  kBarODone = kBarPFull + 2,
+  kBarGFull = kBarODone + 2,
   kBarGFree = kBarGFull + 1,
   kBarEpiDone = kBarGFree + 1,
-  kBarXchg = kBarEpiDone + 1,
-  kBarMergeGo = kBarXchg + 1,
-  kBarPartWritten = kBarMergeGo + 1,
-  kBarDecision = kBarPartWritten + 1,
+  kBarStg = kBarEpiDone + 1,          // + tile
+  kBarPartWritten = kBarStg + 2,     // + tile
+  kBarMergeGo = kBarPartWritten + 2,  // + tile
+  kBarDecision = kBarMergeGo + 2,
   kBarMmaDone = kBarDecision + 1,
   kBarCount = kBarMmaDone + 1
 };
@@ -119,16 +102,18 @@ static_assert(kBarCount <= AttnSmem::kNumBars, "barrier slots");
 // round r, so the CTAs active together work on consecutive units, i.e. on the
 // same heads, and share those heads' K/V in L2); the remaining G + (U mod G)
 // units form a stream-K tail whose (unit, key tile) iterations are cut into G
-// contiguous ranges.  With U a multiple of G the tail is one whole unit per
-// CTA and nothing is cut.  Iterations are numbered globally:
-// t = unit * n_kv + key tile.
+// equal contiguous ranges.  Every tail range holds at least one unit's worth
+// of key tiles, so a unit is cut into at most two segments.  With U a
+// multiple of G the tail is one whole unit per CTA and nothing is cut.
+// Iterations are numbered globally: t = unit * n_kv + key tile.
 //
 // The tail ranges are equal in cost rather than in key tiles: each segment
 // a CTA starts costs about kSegCost key tiles (prologue, epilogue, pipeline
 // refill), so the tail is cut evenly in a virtual space where every unit is
-// kSegCost slots of "segment start" followed by its n_kv key tiles.  Each
-// range still spans at least n_kv + kSegCost virtual slots, so no unit is cut
-// into more than two segments.
+// kSegCost slots of "segment start" followed by its n_kv key tiles.  A range
+// then holds fewer key tiles the more unit starts it contains.  Each range
+// still spans at least n_kv + kSegCost virtual slots, so no unit is cut into
+// more than two segments.
 struct Schedule {
   static constexpr int kSegCost = 8;
   int G, n_kv, dp_rounds;
@@ -200,9 +185,10 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   return pack_f16x2(lo, hi);
 }
 
-// Shared-memory record of the segment a CTA has to run again (see the header).
+// A segment whose row-sum check failed for one query tile (see the epilogue):
+// the CTA runs it again after its other work, storing only that tile.
 struct ReplayRecord {
-  int pending;   // 1 if a segment failed the row-sum check
+  int pending;
   Segment sg;
 };
 
@@ -214,8 +200,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   using KT = KeyTile<WP>;
   constexpr int KHT = KT::KHT;
   constexpr int BN = KT::BN;
-  constexpr int HALF = KT::HALF;
-  constexpr int GH = KT::GH;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u = smem_u32(smem_raw);
@@ -223,9 +207,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + AttnSmem::kBars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + AttnSmem::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + AttnSmem::kMisc + 4);
-  volatile int* merge_flag = reinterpret_cast<volatile int*>(smem + AttnSmem::kMisc + 8);
-  volatile int* bad_flag = reinterpret_cast<volatile int*>(smem + AttnSmem::kMisc + 12);   // [2], by segment parity
-  ReplayRecord* replay = reinterpret_cast<ReplayRecord*>(smem + AttnSmem::kMisc + 32);
+  volatile int* merge_flag = reinterpret_cast<volatile int*>(smem + AttnSmem::kMisc + 8);  // [2]
+  volatile int* bad_flag = reinterpret_cast<volatile int*>(smem + AttnSmem::kMisc + 16);   // [2 tiles][2 parities]
+  ReplayRecord* replay = reinterpret_cast<ReplayRecord*>(smem + AttnSmem::kMisc + 32);     // [2 tiles]
   int* status = args.status;
 
   const int warp = threadIdx.x >> 5;
@@ -234,39 +218,38 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const Schedule sched(args.n_units, static_cast<int>(gridDim.x), n_kv);
   constexpr bool convert_v = BF16;  // P is fp16, so bf16 V tiles are converted to fp16 on chip
 
-  auto sQ = [&]() { return smem + AttnSmem::kQ; };
-  auto sK = [&](int s) { return smem + AttnSmem::kK + s * kTileBytes; };
-  auto sV = [&](int s) { return smem + AttnSmem::kV + s * kTileBytes; };
+  auto sQ = [&](int i) { return smem + AttnSmem::kQ + i * kTileBytes; };
+  auto sK = [&](int s) { return smem + AttnSmem::kRing + s * AttnSmem::kStageBytes; };
+  auto sV = [&](int s) { return smem + AttnSmem::kRing + s * AttnSmem::kStageBytes + kTileBytes; };
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    *merge_flag = 0;
-    bad_flag[0] = 0;
-    bad_flag[1] = 0;
-    replay->pending = 0;
+    merge_flag[0] = 0;
+    merge_flag[1] = 0;
+    for (int i = 0; i < 4; ++i) bad_flag[i] = 0;
+    replay[0].pending = 0;
+    replay[1].pending = 0;
     mbar_init(&bars[kBarQFull], 1);
     mbar_init(&bars[kBarQEmpty], 1);
-    for (int s = 0; s < kRing; ++s) {
-      mbar_init(&bars[kBarKFull + s], 1);
-      mbar_init(&bars[kBarKEmpty + s], 1);
-      mbar_init(&bars[kBarVFull + s], 1);
-      mbar_init(&bars[kBarVEmpty + s], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars[kBarKVFull + s], 1);
+      mbar_init(&bars[kBarKVEmpty + s], 1);
       mbar_init(&bars[kBarVReady + s], 64);
     }
-    for (int i = 0; i < 2; ++i) mbar_init(&bars[kBarSFull + i], 1);
-    // P-ready and P.V-done barriers exist per P buffer: a half may finish tile
-    // t + 1 before the MMA warp has looked at tile t, and a parity wait only
-    // tolerates one completed phase it has not seen
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[kBarSFull + i], 1);
       mbar_init(&bars[kBarPFull + i], kBlockM);
       mbar_init(&bars[kBarODone + i], 1);
     }
     mbar_init(&bars[kBarGFull], 1);
     mbar_init(&bars[kBarGFree], 2 * kBlockM);
     mbar_init(&bars[kBarEpiDone], 2 * kBlockM);
-    mbar_init(&bars[kBarXchg], 2 * kBlockM);
-    mbar_init(&bars[kBarMergeGo], 1);
-    mbar_init(&bars[kBarPartWritten], 2 * kBlockM);
+    mbar_init(&bars[kBarStg + 0], kBlockM);
+    mbar_init(&bars[kBarStg + 1], kBlockM);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[kBarPartWritten + i], kBlockM);
+      mbar_init(&bars[kBarMergeGo + i], 1);
+    }
     mbar_init(&bars[kBarDecision], 2 * kBlockM);
     mbar_init(&bars[kBarMmaDone], 1);
     fence_mbar_init();
@@ -280,13 +263,40 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
-  // Waits (bounded) until the softmax warps have decided whether a segment
-  // must run again, then returns that segment (or false).
-  auto replay_decision = [&](bool ok, Segment& sg) -> bool {
+  // After the softmax warps have finished their segments (bounded wait), the
+  // k-th segment to run again, if any: a failed segment of query tile k, run
+  // once for both tiles when both failed in the same segment.  `mask` holds
+  // the tiles whose result that run stores.
+  auto replay_decision = [&](bool ok, int k, Segment& sg, int& mask) -> bool {
     if (!mbar_wait(&bars[kBarDecision], 0, abort_flag, status) || !ok) return false;
-    if (!replay->pending) return false;
-    sg = replay->sg;
+    if (!replay[k].pending) return false;
+    const Segment a = replay[k].sg;
+    const bool same = replay[0].pending && replay[1].pending && replay[0].sg.u == replay[1].sg.u &&
+                      replay[0].sg.j0 == replay[1].sg.j0 && replay[0].sg.j1 == replay[1].sg.j1;
+    if (k == 1 && same) return false;   // already run for both tiles
+    sg = a;
+    mask = same ? 3 : (1 << k);
     return true;
+  };
+  // The segments of a role, in order: the CTA's own (mask -1), then those to
+  // run again.  Every role walks the same list through this one function, so
+  // each role's segment body has a single call site.  The softmax warps
+  // arrive on the decision barrier when their own segments are done.
+  auto next_segment = [&](Cursor& cur, int& phase, bool ok, bool softmax, Segment& sg, int& mask) -> bool {
+    if (phase == 0) {
+      if (ok && cur.next(sched, sg)) {
+        mask = -1;
+        return true;
+      }
+      phase = 1;
+      if (softmax) mbar_arrive(&bars[kBarDecision]);
+    }
+    while (phase <= 2) {
+      const int k = phase - 1;
+      ++phase;
+      if (replay_decision(ok, k, sg, mask)) return true;
+    }
+    return false;
   };
 
   if (warp < 4) {
@@ -299,151 +309,143 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tma_prefetch_desc(&tm_v);
       int rg = 0, seg = 0;
       bool ok = true;
-      // ring slot rg % kRing; K and V of one tile share the index
-      auto load_kv = [&](bool table, int j, int bh) -> bool {
-        const int s = rg % kRing;
-        const uint32_t ph = ((rg / kRing) & 1) ^ 1;
-        if (!mbar_wait(&bars[kBarKEmpty + s], ph, abort_flag, status)) return false;
-        if (table) {
-          mbar_arrive_expect_tx(&bars[kBarKFull + s], kTileBytes);
-          tma_load_2d(sK(s), &tm_th, &bars[kBarKFull + s], 0, 0);
-        } else {
-          mbar_arrive_expect_tx(&bars[kBarKFull + s], BN * kRowBytes);
-          tma_load_4d(sK(s), &tm_k, &bars[kBarKFull + s], 0, 0, j * KHT, bh);
-        }
-        if (!mbar_wait(&bars[kBarVEmpty + s], ph, abort_flag, status)) return false;
-        if (table) {
-          mbar_arrive_expect_tx(&bars[kBarVFull + s], kTileBytes);
-          tma_load_2d(sV(s), &tm_tw, &bars[kBarVFull + s], 0, 0);
-        } else {
-          mbar_arrive_expect_tx(&bars[kBarVFull + s], BN * kRowBytes);
-          tma_load_4d(sV(s), &tm_v, &bars[kBarVFull + s], 0, 0, j * KHT, bh);
-        }
-        ++rg;
-        return true;
-      };
       auto run_seg = [&](const Segment& sg) -> bool {
-        const int bh = sg.u / args.n_qtiles;
-        const int qt = sg.u - bh * args.n_qtiles;
+        const int bh = sg.u / args.n_pairs;
+        const int qt0 = 2 * (sg.u - bh * args.n_pairs);
         if (seg > 0 && !mbar_wait(&bars[kBarQEmpty], (seg - 1) & 1, abort_flag, status)) return false;
-        mbar_arrive_expect_tx(&bars[kBarQFull], kTileBytes);
-        tma_load_3d(sQ(), &tm_q, &bars[kBarQFull], 0, qt * kBlockM, bh);
+        mbar_arrive_expect_tx(&bars[kBarQFull], 2 * kTileBytes);
+        tma_load_3d(sQ(0), &tm_q, &bars[kBarQFull], 0, qt0 * kBlockM, bh);
+        tma_load_3d(sQ(1), &tm_q, &bars[kBarQFull], 0, (qt0 + 1) * kBlockM, bh);
         ++seg;
-        if (FUSED && !load_kv(true, 0, 0)) return false;
-        for (int j = sg.j0; j < sg.j1; ++j)
-          if (!load_kv(false, j, bh)) return false;
+        if (FUSED) {
+          const int s = rg % kStages;
+          if (!mbar_wait(&bars[kBarKVEmpty + s], ((rg / kStages) & 1) ^ 1, abort_flag, status)) return false;
+          mbar_arrive_expect_tx(&bars[kBarKVFull + s], 2 * kTileBytes);
+          tma_load_2d(sK(s), &tm_th, &bars[kBarKVFull + s], 0, 0);
+          tma_load_2d(sV(s), &tm_tw, &bars[kBarKVFull + s], 0, 0);
+          ++rg;
+        }
+        for (int j = sg.j0; j < sg.j1; ++j, ++rg) {
+          const int s = rg % kStages;
+          if (!mbar_wait(&bars[kBarKVEmpty + s], ((rg / kStages) & 1) ^ 1, abort_flag, status)) return false;
+          mbar_arrive_expect_tx(&bars[kBarKVFull + s], 2 * BN * kRowBytes);
+          tma_load_4d(sK(s), &tm_k, &bars[kBarKVFull + s], 0, 0, j * KHT, bh);
+          tma_load_4d(sV(s), &tm_v, &bars[kBarKVFull + s], 0, 0, j * KHT, bh);
+        }
         return true;
       };
       Cursor cur(sched, blockIdx.x);
       Segment sg;
-      while (ok && cur.next(sched, sg)) ok = run_seg(sg);
-      if (replay_decision(ok, sg)) ok = run_seg(sg);
+      int phase = 0, mask;
+      while (next_segment(cur, phase, ok, false, sg, mask)) ok = run_seg(sg) && ok;
       if (!ok) {
         // Let the copies already in flight land before the CTA exits.
         if (seg > 0) mbar_wait_budget(&bars[kBarQFull], (seg - 1) & 1, kWaitBudgetCycles);
-        for (int r = max(0, rg - kRing); r < rg; ++r) {
-          mbar_wait_budget(&bars[kBarKFull + r % kRing], (r / kRing) & 1, kWaitBudgetCycles);
-          mbar_wait_budget(&bars[kBarVFull + r % kRing], (r / kRing) & 1, kWaitBudgetCycles);
-        }
+        for (int r = max(0, rg - kStages); r < rg; ++r)
+          mbar_wait_budget(&bars[kBarKVFull + r % kStages], (r / kStages) & 1, kWaitBudgetCycles);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp walks the loop (waits and operand arithmetic are
     // warp-uniform); one elected lane issues each tcgen05 instruction.
-    constexpr uint32_t fmt = BF16 ? kBF16 : kF16;
-    constexpr uint32_t id_qk = idesc_f16(kBlockM, BN, fmt, fmt, 0, 0);
-    constexpr uint32_t id_pv = idesc_f16(kBlockM, kHeadDim, kF16, kF16, 0, 1);
-    constexpr uint32_t id_g = idesc_f16(kBlockM, 128, fmt, fmt, 0, 0);
-    // Descriptors differ only in their 14-bit start-address field (address / 16),
-    // which stays below 2^14 for any shared-memory address, so offsets are
-    // added to one base descriptor per operand.
-    const uint64_t d_q = sdesc_sw128(smem_u32(sQ()), 16, 1024);
-    const uint64_t d_k = sdesc_sw128(smem_u32(sK(0)), 16, 1024);
-    const uint64_t d_v = sdesc_sw128(smem_u32(sV(0)), 16, 1024);
-    constexpr uint32_t kSlotStep = kTileBytes >> 4;
-    int rg = 0, gt = 0, seg = 0;
-    bool ok = true;
-    // S(t) = Q K(t)^T into S buffer t % 2
-    auto issue_qk = [&](int t_local, bool last) -> bool {
-      const int s = (rg + t_local) % kRing;
-      if (!warp_all(mbar_wait(&bars[kBarKFull + s], ((rg + t_local) / kRing) & 1, abort_flag, status))) return false;
-      tc_fence_after();
-      const uint32_t d = tbase + 128 * ((gt + t_local) & 1);
-      const uint64_t b = d_k + s * kSlotStep;
-      #pragma unroll
-      for (int k = 0; k < 4; ++k) umma_ss_w(d, d_q + 2 * k, b + 2 * k, id_qk, k > 0);
-      umma_commit_w(&bars[kBarSFull + ((gt + t_local) & 1)]);
-      umma_commit_w(&bars[kBarKEmpty + s]);
-      if (last) umma_commit_w(&bars[kBarQEmpty]);  // no more reads of this segment's Q
-      return true;
-    };
-    // O_h (+)= P_h(t) V_h(t): half h's keys are rows [h*HALF, (h+1)*HALF) of the V tile
-    auto issue_pv = [&](int h, int s, int b, bool acc) {
-      const uint64_t vb = d_v + s * kSlotStep + ((h * HALF * kRowBytes) >> 4);
-      const uint32_t pa = tbase + 256 + 64 * b + h * (HALF / 2);
-      #pragma unroll
-      for (int k = 0; k < HALF / 16; ++k)
-        umma_ts_w(tbase + 384 + 64 * h, pa + 8 * k, vb + 128 * k, id_pv, (acc || k > 0) ? 1u : 0u);
-      umma_commit_w(&bars[kBarODone + 2 * h + b]);
-    };
-    auto run_seg = [&](const Segment& sg) -> bool {
-      const int len = sg.j1 - sg.j0;
-      if (!warp_all(mbar_wait(&bars[kBarQFull], seg & 1, abort_flag, status))) return false;
-      if (FUSED) {
-        // G = Q [T_h ; T_w]^T into S0 | S1; both S buffers are free: every
-        // earlier QK^T has been read by both halves (their P arrivals came first)
-        const int s = rg % kRing;
-        const uint32_t ph = (rg / kRing) & 1;
-        if (!warp_all(mbar_wait(&bars[kBarKFull + s], ph, abort_flag, status))) return false;
-        if (!warp_all(mbar_wait(&bars[kBarVFull + s], ph, abort_flag, status))) return false;
-        tc_fence_after();
+    {
+      constexpr uint32_t fmt = BF16 ? kBF16 : kF16;
+      constexpr uint32_t id_qk = idesc_f16(kBlockM, BN, fmt, fmt, 0, 0);
+      constexpr uint32_t id_pv = idesc_f16(kBlockM, kHeadDim, kF16, kF16, 0, 1);
+      constexpr uint32_t id_g = idesc_f16(kBlockM, 256, fmt, fmt, 0, 0);
+      // Descriptors differ only in their 14-bit start-address field (address / 16),
+      // which stays below 2^14 for any shared-memory address, so offsets are
+      // added to one base descriptor per operand.
+      const uint64_t d_q = sdesc_sw128(smem_u32(sQ(0)), 16, 1024);
+      const uint64_t d_k = sdesc_sw128(smem_u32(sK(0)), 16, 1024);
+      const uint64_t d_v = sdesc_sw128(smem_u32(sV(0)), 16, 1024);
+      constexpr uint32_t kQStep = kTileBytes >> 4, kStageStep = AttnSmem::kStageBytes >> 4;
+      auto issue_qk = [&](int i, int s) {
+        const uint64_t a = d_q + i * kQStep, b = d_k + s * kStageStep;
         #pragma unroll
-        for (int k = 0; k < 4; ++k) umma_ss_w(tbase, d_q + 2 * k, d_k + s * kSlotStep + 2 * k, id_g, k > 0);
+        for (int k = 0; k < 4; ++k) umma_ss_w(tbase + 128 * i, a + 2 * k, b + 2 * k, id_qk, k > 0);
+      };
+      auto issue_pv = [&](int i, int s, bool acc) {
+        const uint64_t b = d_v + s * kStageStep;
         #pragma unroll
-        for (int k = 0; k < 4; ++k) umma_ss_w(tbase + 128, d_q + 2 * k, d_v + s * kSlotStep + 2 * k, id_g, k > 0);
-        umma_commit_w(&bars[kBarGFull]);
-        umma_commit_w(&bars[kBarKEmpty + s]);
-        umma_commit_w(&bars[kBarVEmpty + s]);
-        ++rg;
-        if (!warp_all(mbar_wait(&bars[kBarGFree], seg & 1, abort_flag, status))) return false;
-        tc_fence_after();
-      }
-      if (!issue_qk(0, len == 1)) return false;
-      if (len > 1 && !issue_qk(1, len == 2)) return false;
-      for (int jj = 0; jj < len; ++jj) {
-        const int t = gt + jj, s = (rg + jj) % kRing, b = t & 1;
-        const uint32_t ph = ((rg + jj) / kRing) & 1;
-        if (!warp_all(mbar_wait(&bars[convert_v ? kBarVReady + s : kBarVFull + s], ph, abort_flag, status)))
-          return false;
-        if (!warp_all(mbar_wait(&bars[kBarPFull + b], (t >> 1) & 1, abort_flag, status))) return false;
-        if (jj == 0 && seg > 0) {
-          // the first P.V of a segment overwrites O: the previous epilogue must have read it
-          if (!warp_all(mbar_wait(&bars[kBarEpiDone], (seg - 1) & 1, abort_flag, status))) return false;
+        for (int k = 0; k < BN / 16; ++k)
+          umma_ts_w(tbase + 384 + 64 * i, tbase + 256 + 64 * i + 8 * k, b + 128 * k, id_pv,
+                    (acc || k > 0) ? 1u : 0u);
+      };
+      int rg = 0, gi = 0, seg = 0;
+      bool ok = true;
+      auto run_seg = [&](const Segment& sg) -> bool {
+        const int len = sg.j1 - sg.j0;
+        if (!warp_all(mbar_wait(&bars[kBarQFull], seg & 1, abort_flag, status))) return false;
+        if (FUSED) {
+          if (seg > 0 && !warp_all(mbar_wait(&bars[kBarEpiDone], (seg - 1) & 1, abort_flag, status))) return false;
+          const int s = rg % kStages;
+          if (!warp_all(mbar_wait(&bars[kBarKVFull + s], (rg / kStages) & 1, abort_flag, status))) return false;
+          tc_fence_after();
+          for (int i = 0; i < 2; ++i) {
+            const uint64_t a = d_q + i * kQStep, b = d_k + s * kStageStep;
+            #pragma unroll
+            for (int k = 0; k < 4; ++k) umma_ss_w(tbase + 256 * i, a + 2 * k, b + 2 * k, id_g, k > 0);
+          }
+          umma_commit_w(&bars[kBarGFull]);
+          umma_commit_w(&bars[kBarKVEmpty + s]);
+          ++rg;
+          if (!warp_all(mbar_wait(&bars[kBarGFree], seg & 1, abort_flag, status))) return false;
+          tc_fence_after();
         }
-        tc_fence_after();
-        issue_pv(0, s, b, jj > 0);
-        if (!warp_all(mbar_wait(&bars[kBarPFull + 2 + b], (t >> 1) & 1, abort_flag, status))) return false;
-        tc_fence_after();
-        // both halves have read S(t): its buffer takes S(t + 2)
-        if (jj + 2 < len && !issue_qk(jj + 2, jj + 3 == len)) return false;
-        issue_pv(1, s, b, jj > 0);
-        umma_commit_w(&bars[kBarVEmpty + s]);
-      }
-      gt += len;
-      rg += len;
-      ++seg;
-      return true;
-    };
-    Cursor cur(sched, blockIdx.x);
-    Segment sg;
-    while (ok && cur.next(sched, sg)) ok = run_seg(sg);
-    if (replay_decision(warp_all(ok), sg)) ok = run_seg(sg);
-    // Drain: every MMA issued above completes before TMEM is released.
-    umma_commit_w(&bars[kBarMmaDone]);
-    mbar_wait_budget(&bars[kBarMmaDone], 0, kWaitBudgetCycles);
-    __syncwarp();
-  } else {
+        ++seg;
+        {
+          const int s = rg % kStages;
+          if (!warp_all(mbar_wait(&bars[kBarKVFull + s], (rg / kStages) & 1, abort_flag, status))) return false;
+          tc_fence_after();
+          issue_qk(0, s);
+          umma_commit_w(&bars[kBarSFull + 0]);
+          issue_qk(1, s);
+          umma_commit_w(&bars[kBarSFull + 1]);
+        }
+        for (int jj = 0; jj < len; ++jj, ++rg, ++gi) {
+          const int s = rg % kStages, ph = (rg / kStages) & 1;
+          const int sn = (rg + 1) % kStages, phn = ((rg + 1) / kStages) & 1;
+          const bool more = jj + 1 < len;
+          if (convert_v && !warp_all(mbar_wait(&bars[kBarVReady + s], ph, abort_flag, status))) return false;
+          // Once softmax i has written P_i(j) (and so finished reading S_i),
+          // the next S_i goes first: the softmax can start on it while PV_i(j)
+          // runs, and waits for PV_i(j) only before it next writes P_i or O_i.
+          if (!warp_all(mbar_wait(&bars[kBarPFull + 0], gi & 1, abort_flag, status))) return false;
+          tc_fence_after();
+          if (more) {
+            if (!warp_all(mbar_wait(&bars[kBarKVFull + sn], phn, abort_flag, status))) return false;
+            tc_fence_after();
+            issue_qk(0, sn);
+            umma_commit_w(&bars[kBarSFull + 0]);
+          }
+          issue_pv(0, s, jj > 0);
+          umma_commit_w(&bars[kBarODone + 0]);
+          if (!warp_all(mbar_wait(&bars[kBarPFull + 1], gi & 1, abort_flag, status))) return false;
+          tc_fence_after();
+          if (more) {
+            issue_qk(1, sn);
+            umma_commit_w(&bars[kBarSFull + 1]);
+          } else {
+            umma_commit_w(&bars[kBarQEmpty]);  // no more reads of this segment's Q
+          }
+          issue_pv(1, s, jj > 0);
+          umma_commit_w(&bars[kBarODone + 1]);
+          umma_commit_w(&bars[kBarKVEmpty + s]);
+        }
+        return true;
+      };
+      Cursor cur(sched, blockIdx.x);
+      Segment sg;
+      int phase = 0, mask;
+      while (next_segment(cur, phase, warp_all(ok), false, sg, mask)) ok = run_seg(sg) && ok;
+      // Drain: every MMA issued above completes before TMEM is released.
+      umma_commit_w(&bars[kBarMmaDone]);
+      mbar_wait_budget(&bars[kBarMmaDone], 0, kWaitBudgetCycles);
+      __syncwarp();
+    }
+  } else if (warp < 4) {
     // ------------------------------------------------------------ bf16 -> fp16 V conversion
     // The fused kernel's table slots are passed through unconverted, so that
     // v_ready completes once per ring index.
@@ -453,8 +455,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       bool ok = true;
       auto run_seg = [&](const Segment& sg) -> bool {
         for (int j = FUSED ? sg.j0 - 1 : sg.j0; j < sg.j1; ++j, ++rg) {
-          const int s = rg % kRing;
-          if (!mbar_wait(&bars[kBarVFull + s], (rg / kRing) & 1, abort_flag, status)) return false;
+          const int s = rg % kStages;
+          if (!mbar_wait(&bars[kBarKVFull + s], (rg / kStages) & 1, abort_flag, status)) return false;
           if (j >= sg.j0) {
             uint4* vp = reinterpret_cast<uint4*>(sV(s));
             for (int idx = ct; idx < BN * kRowBytes / 16; idx += 64) {
@@ -473,170 +475,175 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       };
       Cursor cur(sched, blockIdx.x);
       Segment sg;
-      while (ok && cur.next(sched, sg)) ok = run_seg(sg);
-      if (replay_decision(ok, sg)) run_seg(sg);
+      int phase = 0, mask;
+      while (next_segment(cur, phase, ok, false, sg, mask)) ok = run_seg(sg) && ok;
     }
   }
   } else {
     regs_claim<kRegsSmx>();
     // ------------------------------------------------------------ softmax / epilogue
-    const int h = (warp - 4) >> 2;           // column half of this warp
+    const int wg = (warp - 4) >> 2;          // query tile of this warpgroup
     const int wq = warp & 3;                 // TMEM lane quarter
-    const int r = wq * 32 + lane;            // row inside the query tile
+    const int r = wq * 32 + lane;            // row inside the tile
     const int H = args.H, W = args.W, N = args.N;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tO0 = tbase + lane_off + 384;
-    float* area = reinterpret_cast<float*>(smem + AttnSmem::kBias);
-    float2* xchg = reinterpret_cast<float2*>(smem + AttnSmem::kXchg);   // [2][128] (m, l)
+    const uint32_t tS = tbase + lane_off + 128 * wg;
+    const uint32_t tP = tbase + lane_off + 256 + 64 * wg;
+    const uint32_t tO = tbase + lane_off + 384 + 64 * wg;
+    float* area = reinterpret_cast<float*>(smem + AttnSmem::kBias) + wg * kBlockM * kBiasStride;
     const int Hpad = n_kv * KHT;
     const int HS = Hpad + 1;
     float* bh_row = area + r * HS;
     const float NEG_INF = -__int_as_float(0x7f800000);
     const float sl2 = args.scale_log2;
     const float2 sl2v = make_float2(sl2, sl2);
-    const bool leader = warp == 4 && lane == 0;
 
-    int gt = 0, seg = 0;
-    uint32_t xph = 0;   // completed phases of the softmax-wide exchange barrier
-    int pmerge = 0;     // completed phases of the merge-go barrier
-    int ppub = 0;       // completed phases of the partial-written barrier
-    float cap = kStartCap;
-    bool ok = true;
-    // Barrier of the 256 softmax threads (all arrive, then wait).
-    auto sm_sync = [&]() -> bool {
-      mbar_arrive(&bars[kBarXchg]);
-      const bool w = mbar_wait(&bars[kBarXchg], xph & 1, abort_flag, status);
-      ++xph;
+    int gi = 0, seg = 0;
+    float cap = kStartCap;  // overshoot allowed to the starting maximum; 0 after a failed check
+    int pseg = 0;  // completed phases of this warpgroup's merge-go barrier
+    int ppub = 0;  // completed phases of its partial-written barrier
+    uint32_t stg_phase = 0;  // completed phases of this warpgroup's staging barrier
+    // Warpgroup-wide barrier on the staging mbarrier (all 128 threads arrive, then wait).
+    auto wg_sync = [&]() -> bool {
+      mbar_arrive(&bars[kBarStg + wg]);
+      const bool w = mbar_wait(&bars[kBarStg + wg], stg_phase & 1, abort_flag, status);
+      ++stg_phase;
       return warp_all(w);
     };
-
-    auto run_seg = [&](const Segment& sg, bool is_replay) -> bool {
-      const int bh = sg.u / args.n_qtiles;
-      const int qt = sg.u - bh * args.n_qtiles;
+    bool ok = true;
+    auto run_seg = [&](const Segment& sg, int store_mask) -> bool {
+      const int bh = sg.u / args.n_pairs;
+      const int qt = 2 * (sg.u - bh * args.n_pairs) + wg;
       const int n = qt * kBlockM + r;
       const bool row_valid = n < N;
       const int qh = row_valid ? n / W : 0;
       const int qw = row_valid ? n - qh * W : 0;
-      const int len = sg.j1 - sg.j0;
 
-      // ---------------------------------------------------------------- prologue
-      // every thread has finished with the previous segment's output staging
-      // in the bias area before any row is written into it again
-      if (seg > 0 && !sm_sync()) return false;
       float bw[WP];
       if (FUSED) {
-        if (!warp_all(mbar_wait(&bars[kBarGFull], seg & 1, abort_flag, status))) return false;
+        ok = warp_all(mbar_wait(&bars[kBarGFull], seg & 1, abort_flag, status));
         tc_fence_after();
         float* stg = area + r * kBiasStride;
-        // rel_w row from G_w (TMEM columns 128..255), skewed into the staging
-        // row; the row's two threads take alternate 32-column chunks
-        skew_row_to_smem(tbase + lane_off + 128, qw, W, stg, kLog2e, h, 2);
-        if (!sm_sync()) return false;
+        if (ok) skew_row_to_smem(tbase + lane_off + 256 * wg + 128, qw, W, stg, kLog2e);
         #pragma unroll
-        for (int kw = 0; kw < WP; ++kw) bw[kw] = kw < W ? stg[kw] : NEG_INF;
+        for (int kw = 0; kw < WP; ++kw) bw[kw] = (ok && kw < W) ? stg[kw] : NEG_INF;
         // the staging rows (stride kBiasStride) overlap the bias rows (stride HS):
-        // every thread has its rel_w row before any rel_h row is written
-        if (!sm_sync()) return false;
-        skew_row_to_smem(tbase + lane_off, qh, H, bh_row, kLog2e, h, 2);
-        if (h == 0)
+        // every thread of the warpgroup has read its staged row before any bias row is written
+        ok = wg_sync() && ok;
+        if (ok) {
+          skew_row_to_smem(tbase + lane_off + 256 * wg, qh, H, bh_row, kLog2e);
           for (int kh = H; kh < Hpad; ++kh) bh_row[kh] = NEG_INF;
+        }
         tc_fence_before();
         mbar_arrive(&bars[kBarGFree]);
-        if (!sm_sync()) return false;
+        if (!ok) return false;
       } else {
+        // every warp has stored the previous segment's output rows, which
+        // leave through the same area, before any row is copied in
+        if (seg > 0) ok = wg_sync() && ok;
         // The tile's rows of rel_w, then of rel_h, are one contiguous block
-        // each: each of the eight warps copies every eighth row into the
-        // staging area, a row per pass with the lanes along it (coalesced),
-        // scaled by log2e.  Rows past N read as 0.
+        // each: every warp copies a quarter of the rows into the staging area,
+        // a row per pass with the lanes along it (coalesced), scaled by log2e.
+        // Rows past N read as 0.
         const size_t row0 = static_cast<size_t>(bh) * N + static_cast<size_t>(qt) * kBlockM;
         const int nrows = min(kBlockM, N - qt * kBlockM);
-        const int cw = warp - 4;   // copy warp 0..7
-        // Loads for 4 rows go out together before any store (the stores could
+        // Loads for 8 rows go out together before any store (the stores could
         // alias the source as far as the compiler knows).
-        auto copy_rows = [&](const void* src, int rlen, int stride) {
-          for (int rb = cw; rb < kBlockM; rb += 32) {
-            float v[4][2];
+        auto copy_rows = [&](const void* src, int len, int stride) {
+          for (int rb = wq; rb < kBlockM; rb += 32) {
+            float v[8][2];
             #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int rr = rb + 8 * u;
+            for (int u = 0; u < 8; ++u) {
+              const int rr = rb + 4 * u;
               #pragma unroll
-              for (int k = 0; k < 2; ++k) {
-                const int c = lane + 32 * k;
-                v[u][k] = (rr < nrows && c < rlen)
-                              ? load_elem(src, (row0 + rr) * static_cast<size_t>(rlen) + c, args.bias_fmt)
+              for (int h = 0; h < 2; ++h) {
+                const int c = lane + 32 * h;
+                v[u][h] = (rr < nrows && c < len)
+                              ? load_elem(src, (row0 + rr) * static_cast<size_t>(len) + c, args.bias_fmt)
                               : 0.f;
               }
             }
             #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < 8; ++u) {
               #pragma unroll
-              for (int k = 0; k < 2; ++k) {
-                const int c = lane + 32 * k;
-                if (c < rlen) area[(rb + 8 * u) * stride + c] = kLog2e * v[u][k];
+              for (int h = 0; h < 2; ++h) {
+                const int c = lane + 32 * h;
+                if (c < len) area[(rb + 4 * u) * stride + c] = kLog2e * v[u][h];
               }
             }
           }
         };
         copy_rows(args.rel_w, W, kBiasStride);
-        if (!sm_sync()) return false;
+        ok = wg_sync() && ok;
         const float* stg = area + r * kBiasStride;
         #pragma unroll
         for (int kw = 0; kw < WP; ++kw) bw[kw] = kw < W ? stg[kw] : NEG_INF;
         // every thread has its rel_w row before the area is reused for rel_h
-        if (!sm_sync()) return false;
+        ok = wg_sync() && ok;
         copy_rows(args.rel_h, H, HS);
-        if (h == 0)
-          for (int kh = H; kh < Hpad; ++kh) bh_row[kh] = NEG_INF;
-        if (!sm_sync()) return false;
+        ok = wg_sync() && ok;
+        for (int kh = H; kh < Hpad; ++kh) bh_row[kh] = NEG_INF;
+        if (!ok) return false;
       }
+      ++seg;
 
-      // S is processed in blocks of 16 columns (one TMEM load and one wait each).
-      // Exact maximum over this half of x = s*scale*log2e + rel_w*log2e + rel_h*log2e;
+      // S is processed in blocks of kBlk columns (one TMEM load and one wait
+      // each); narrow grids, with more grid rows per tile, use 16 to keep
+      // their per-row bias terms in registers.
+      constexpr int kBlk = WP <= 16 ? 16 : 32;
+      auto load_block = [&](int cb, uint32_t (&u)[kBlk]) {
+        if (kBlk == 32 && BN - cb >= 32) tmem_ld32(tS + cb, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+        else tmem_ld16(tS + cb, *reinterpret_cast<uint32_t(*)[16]>(&u[0]));
+        tmem_wait_ld();
+      };
+      // Exact tile maximum of x = s*scale*log2e + rel_w*log2e + rel_h*log2e;
       // base = the same without the rel_h term.
-      auto tile_max = [&](uint32_t tS, const float (&bhv)[GH], float& base) -> float {
-        float gm[GH];
+      auto tile_max = [&](const float (&bhv)[KHT], float& base) -> float {
+        float gm[KHT];
         #pragma unroll
-        for (int g = 0; g < GH; ++g) gm[g] = NEG_INF;
+        for (int g = 0; g < KHT; ++g) gm[g] = NEG_INF;
         #pragma unroll
-        for (int cb = 0; cb < HALF; cb += 16) {
-          uint32_t u[16];
-          tmem_ld16(tS + cb, u);
-          tmem_wait_ld();
+        for (int cb = 0; cb < BN; cb += kBlk) {
+          uint32_t u[kBlk];
+          load_block(cb, u);
           #pragma unroll
-          for (int k = 0; k < 16; k += 2) {
+          for (int k = 0; k < kBlk; k += 2) {
             const int col = cb + k;
-            const int g = col / WP, kw = col % WP;
-            const float2 t = ffma2(make_float2(__uint_as_float(u[k]), __uint_as_float(u[k + 1])), sl2v,
-                                   make_float2(bw[kw], bw[kw + 1]));
-            gm[g] = fmax3(gm[g], t.x, t.y);
+            if (col < BN) {
+              const int g = col / WP, kw = col % WP;
+              const float2 t = ffma2(make_float2(__uint_as_float(u[k]), __uint_as_float(u[k + 1])), sl2v,
+                                     make_float2(bw[kw], bw[kw + 1]));
+              gm[g] = fmax3(gm[g], t.x, t.y);
+            }
           }
         }
         float mt = NEG_INF;
         base = NEG_INF;
         #pragma unroll
-        for (int g = 0; g < GH; ++g) {
+        for (int g = 0; g < KHT; ++g) {
           mt = fmaxf(mt, gm[g] + bhv[g]);
           base = fmaxf(base, gm[g]);
         }
         return mt;
       };
-      // p = 2^(x - m) for this half of the tile into P (fp16, TMEM); returns the
-      // row sum.  S is read in 16-column blocks with the next block always in
-      // flight; four partial sums keep the dependency chains short.  Before the
-      // first P store, P.V of tile t - 2 (the last reader of this P buffer) has
-      // completed.
-      bool pfree_pending = false;
-      auto wait_pfree = [&](int t) {
-        if (pfree_pending) {
-          ok = warp_all(mbar_wait(&bars[kBarODone + 2 * h + (t & 1)], ((t - 2) >> 1) & 1, abort_flag, status)) && ok;
+      // Waits (once, warp-uniformly) until PV of the previous key tile has
+      // read P and written O; needed before P or O is next written.
+      bool pv_pending = false;
+      auto wait_pv = [&]() {
+        if (pv_pending) {
+          ok = warp_all(mbar_wait(&bars[kBarODone + wg], (gi - 1) & 1, abort_flag, status)) && ok;
           tc_fence_after();
-          pfree_pending = false;
+          pv_pending = false;
         }
       };
-      auto exp_pass = [&](uint32_t tS, uint32_t tP, int t, const float (&bhv)[GH], float m) -> float2 {
-        float2 off[GH];
+      // p = 2^(x - m) for the whole tile into P (fp16, TMEM); returns the row sum.
+      // S is read in 16-column blocks with the next block always in flight,
+      // so the TMEM load latency overlaps the arithmetic of the current one;
+      // four partial sums keep the dependency chains short.
+      auto exp_pass = [&](const float (&bhv)[KHT], float m) -> float2 {
+        float2 off[KHT];
         #pragma unroll
-        for (int g = 0; g < GH; ++g) off[g] = make_float2(bhv[g] - m, bhv[g] - m);
+        for (int g = 0; g < KHT; ++g) off[g] = make_float2(bhv[g] - m, bhv[g] - m);
         float2 ts[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                         make_float2(0.f, 0.f)};
         uint32_t ua[16], ub[16];
@@ -646,306 +653,307 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           for (int k = 0; k < 16; k += 2) {
             const int col = cb + k;
             const int g = col / WP, kw = col % WP;
-            float2 x = ffma2(make_float2(__uint_as_float(u[k]), __uint_as_float(u[k + 1])), sl2v,
+            float2 t = ffma2(make_float2(__uint_as_float(u[k]), __uint_as_float(u[k + 1])), sl2v,
                              make_float2(bw[kw], bw[kw + 1]));
-            x = fadd2(x, off[g]);
-            const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            t = fadd2(t, off[g]);
+            const float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
             ts[(k / 2) & 3] = fadd2(ts[(k / 2) & 3], p);
             pk[k / 2] = pack_f16x2(p.x, p.y);
           }
-          if (cb == 0) wait_pfree(t);
+          if (cb == 0) wait_pv();
           tmem_st8(tP + cb / 2, pk);
         };
         tmem_ld16(tS, ua);
         #pragma unroll
-        for (int cb = 0; cb < HALF; cb += 32) {
+        for (int cb = 0; cb < BN; cb += 32) {
           tmem_wait_ld();
-          if (cb + 16 < HALF) tmem_ld16(tS + cb + 16, ub);
+          if (cb + 16 < BN) tmem_ld16(tS + cb + 16, ub);
           block(cb, ua);
-          if (cb + 16 < HALF) {
+          if (cb + 16 < BN) {
             tmem_wait_ld();
-            if (cb + 32 < HALF) tmem_ld16(tS + cb + 32, ua);
+            if (cb + 32 < BN) tmem_ld16(tS + cb + 32, ua);
             block(cb + 16, ub);
           }
         }
         return fadd2(fadd2(ts[0], ts[1]), fadd2(ts[2], ts[3]));
       };
 
-      // Largest rel_h term (base 2) over this half's grid rows of the segment.
-      float mbh = NEG_INF;
-      for (int j = sg.j0; j < sg.j1; ++j) {
-        #pragma unroll
-        for (int g = 0; g < GH; ++g) mbh = fmaxf(mbh, bh_row[j * KHT + h * GH + g]);
-      }
-
-      // ---------------------------------------------------------------- tiles
       // Online softmax over the segment's key tiles.  The first tile takes the
-      // exact maximum (raised by the rel_h estimate, at most `cap` above it);
-      // later tiles exponentiate against the running maximum at once and are
-      // redone exactly only if their row sum exceeds kSpecSumLimit.  The final
-      // O / l uses the same running maximum, so skipping rescales changes nothing.
+      // exact maximum (raised by the rel_h estimate below); later tiles
+      // exponentiate against the running maximum
+      // at once and are redone exactly only if their row sum exceeds
+      // kSpecSumLimit (so every p stays within fp16).  The final O / l uses the
+      // same running maximum, so skipping rescales changes nothing.
       float m_used = 0.f;
       float2 lsum = make_float2(0.f, 0.f);
-      for (int jj = 0; jj < len; ++jj) {
-        const int t = gt + jj;
-        const int b = t & 1;
-        const uint32_t tS = tbase + lane_off + 128 * b + h * HALF;
-        const uint32_t tP = tbase + lane_off + 256 + 64 * b + h * (HALF / 2);
-        if (!warp_all(mbar_wait(&bars[kBarSFull + b], (t >> 1) & 1, abort_flag, status))) return false;
+      // largest rel_h term (base 2) over the grid rows this segment covers
+      float mbh = NEG_INF;
+      for (int kh = sg.j0 * KHT; kh < min(sg.j1 * KHT, H); ++kh) mbh = fmaxf(mbh, bh_row[kh]);
+      for (int j = sg.j0; j < sg.j1; ++j, ++gi) {
+        ok = warp_all(mbar_wait(&bars[kBarSFull + wg], gi & 1, abort_flag, status));
+        if (!ok) break;
         tc_fence_after();
-        pfree_pending = t >= 2;
-        const int kh0 = (sg.j0 + jj) * KHT + h * GH;
-        float bhv[GH];
+        pv_pending = j > sg.j0;
+        const int kh0 = j * KHT;
+        float bhv[KHT];
         #pragma unroll
-        for (int g = 0; g < GH; ++g) bhv[g] = bh_row[kh0 + g];
+        for (int g = 0; g < KHT; ++g) bhv[g] = bh_row[kh0 + g];
 
         float2 ts = make_float2(0.f, 0.f);
-        bool exact = jj == 0;
+        bool exact = j == sg.j0;
         if (!exact) {
-          ts = exp_pass(tS, tP, t, bhv, m_used);
+          ts = exp_pass(bhv, m_used);
           exact = __any_sync(0xffffffffu, !(ts.x + ts.y <= kSpecSumLimit));
         }
         if (exact) {
           float base;
-          const float mt = tile_max(tS, bhv, base);
-          // rel_h is the term that moves the row maximum most between key
-          // tiles, so start from this tile's largest s*scale + rel_w plus the
-          // half's largest rel_h (less a margin), at most `cap` above the
-          // exact maximum of this tile
-          const float est = fminf(mt + cap, base + mbh - kStartMargin);
-          if (jj == 0) {
-            // A half can hold no valid key at all (the grid rows of a last,
-            // partly padded tile); -FLT_MAX instead of -inf keeps x - m at
-            // -inf there (p = 0), and the merge then weighs the half with 0.
-            m_used = fmaxf(fmaxf(mt, est), -FLT_MAX);
+          const float mt = tile_max(bhv, base);
+          if (j == sg.j0) {
+            // rel_h is the term that moves the row maximum most between key
+            // tiles, so start from this tile's largest s*scale + rel_w plus the
+            // row's largest rel_h (less a margin), capped above the exact
+            // maximum of this tile: later tiles then seldom pass the row-sum
+            // bound and need an exact redo
+            m_used = fmaxf(fmaxf(mt, fminf(mt + cap, base + mbh - kStartMargin)), -FLT_MAX);
           } else {
-            const float m_new = fmaxf(fmaxf(m_used, mt), est);
+            wait_pv();
+            // the same estimate, capped above this tile's exact maximum
+            const float m_new = fmaxf(fmaxf(m_used, mt), fminf(mt + cap, base + mbh - kStartMargin));
             const float alpha = ex2_approx(m_used - m_new);
             m_used = m_new;
             lsum.x *= alpha;
             lsum.y *= alpha;
-            // P.V of tile t - 1 (the last one into O_h) has completed
-            ok = warp_all(mbar_wait(&bars[kBarODone + 2 * h + ((t - 1) & 1)], ((t - 1) >> 1) & 1, abort_flag,
-                                    status)) && ok;
-            tc_fence_after();
-            const uint32_t tOh = tO0 + 64 * h;
             #pragma unroll
             for (int c = 0; c < 2; ++c) {
               uint32_t o[32];
-              tmem_ld32(tOh + 32 * c, o);
+              tmem_ld32(tO + 32 * c, o);
               tmem_wait_ld();
               #pragma unroll
               for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-              tmem_st32(tOh + 32 * c, o);
+              tmem_st32(tO + 32 * c, o);
             }
           }
-          ts = exp_pass(tS, tP, t, bhv, m_used);
+          ts = exp_pass(bhv, m_used);
         }
         lsum = fadd2(lsum, ts);
-        if (!ok) return false;
+        if (!ok) break;
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&bars[kBarPFull + 2 * h + b]);
+        mbar_arrive(&bars[kBarPFull + wg]);
       }
+      if (!ok) return false;
 
-      // ---------------------------------------------------------------- epilogue
-      // Both halves' last P.V products have completed (this thread reads both O halves).
-      const int tl = gt + len - 1;
-      for (int x = 0; x < 2; ++x)
-        if (!warp_all(mbar_wait(&bars[kBarODone + 2 * x + (tl & 1)], (tl >> 1) & 1, abort_flag, status)))
-          return false;
+      // epilogue: O (fp32, unnormalised) streamed out of TMEM 16 columns at a time
+      ok = warp_all(mbar_wait(&bars[kBarODone + wg], (gi - 1) & 1, abort_flag, status));
+      if (!ok) return false;
       tc_fence_after();
-      // merge the halves: m* = max(m_0, m_1), l = f_0 l_0 + f_1 l_1 with f_x = 2^(m_x - m*)
-      xchg[h * kBlockM + r] = make_float2(m_used, lsum.x + lsum.y);
-      if (!sm_sync()) return false;
-      const float2 ml0 = xchg[r], ml1 = xchg[kBlockM + r];
-      const float mstar = fmaxf(ml0.x, ml1.x);
-      const float f0 = ex2_approx(ml0.x - mstar), f1 = ex2_approx(ml1.x - mstar);
-      const float l = f0 * ml0.y + f1 * ml1.y;
-      volatile int* bad = bad_flag + (seg & 1);
-      if (row_valid && !(l >= kMinRowSum)) *bad = 1;
-      // this thread's 32 output columns [32h, 32h + 32) of both O halves
-      uint32_t o0[32], o1[32];
-      tmem_ld32(tO0 + 32 * h, o0);
-      tmem_ld32(tO0 + 64 + 32 * h, o1);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&bars[kBarEpiDone]);
-      if (!sm_sync()) return false;
-      const bool seg_bad = *bad != 0;
-      // every thread has read this segment's flag; the next segment's is cleared
-      if (leader) bad_flag[(seg + 1) & 1] = 0;
-      gt += len;
-      ++seg;
-      if (seg_bad && !is_replay) {
-        // Too little of the row's mass above the fp16 range: nothing of this
-        // segment is stored or published; the CTA runs it again at the end
-        // with no overshoot, and its later segments use none either.  (With
-        // no overshoot l >= 1 on every row of finite inputs, so the run again
-        // always stores.)
-        if (leader && !replay->pending) {
-          replay->pending = 1;
-          replay->sg = sg;
+      const float l = lsum.x + lsum.y;
+      // Row-sum check.  Rounding P to fp16 moves each p by at most 2^-11 of
+      // itself, or by 2^-25 (in units of the running maximum) for the p that
+      // fall below the fp16 normal range, so the output moves by at most
+      // max|v| (2^-11 + n 2^-25 / l) for the segment's n valid keys.  The
+      // estimated starting maximum may overshoot the row's true maximum and
+      // leave l small; a tile with l < n 2^-16 on any row (which keeps the
+      // second term at most 2^-9) is neither stored nor published but computed
+      // again at the end of the CTA's work with no overshoot (cap 0, l >= 1).
+      const int n_keys = (min(sg.j1 * KHT, H) - sg.j0 * KHT) * W;
+      volatile int* bad = bad_flag + 2 * wg + (seg & 1);
+      if (row_valid && !(l >= ldexpf(static_cast<float>(n_keys), kMinRowSumLog2))) *bad = 1;
+      if (!wg_sync()) return false;
+      const bool tile_bad = *bad != 0;
+      if (r == 0) bad_flag[2 * wg + ((seg + 1) & 1)] = 0;   // every thread has read this segment's flag
+      const bool store = store_mask < 0 ? !tile_bad : ((store_mask >> wg) & 1) != 0;
+      if (store_mask < 0 && tile_bad) {
+        if (r == 0) {
+          replay[wg].sg = sg;
+          replay[wg].pending = 1;
         }
         cap = 0.f;
+      }
+      if (!store) {
+        tc_fence_before();
+        if (FUSED) mbar_arrive(&bars[kBarEpiDone]);
         return true;
       }
-      float v[32];
-      #pragma unroll
-      for (int k = 0; k < 32; ++k) v[k] = f0 * __uint_as_float(o0[k]) + f1 * __uint_as_float(o1[k]);
-
-      // Output rows leave through the bias area (no thread reads bias rows
-      // any more): each lane stages its 32 columns, 16-byte chunks XOR-swizzled
-      // by row so neither side has bank conflicts, then the warp stores runs of
-      // 512 contiguous bytes.
+      // Output rows leave through this warp's quarter of the bias area (no
+      // warp of the warpgroup reads its bias rows once O is complete): each
+      // lane stages its row, 16-byte chunks XOR-swizzled by row so neither
+      // side has bank conflicts, then the warp stores runs of 512 contiguous
+      // bytes (4 bf16/f16 rows or 2 fp32 rows per instruction).
       const bool out32 = args.out_fmt == kF32;
-      const int row_bytes = out32 ? 256 : 128;     // a whole output row in global memory
-      const int part_bytes = row_bytes / 2;        // this thread's 32 columns
-      uint8_t* ostage = reinterpret_cast<uint8_t*>(area) + (h * 4 + wq) * 32 * 128;
-      // 128-byte row parts: chunk k ^ (row & 7); 64-byte row parts (two per 128 bytes): k ^ ((row >> 1) & 3)
-      auto chunk_at = [&](int row, int k) {
-        const int sw = out32 ? (row & 7) : ((row >> 1) & 3);
-        return ostage + row * part_bytes + ((k ^ sw) << 4);
-      };
-      auto stage_out = [&](const float (&vv)[32], float scale) {
+      const int row_bytes = out32 ? 256 : 128;
+      uint8_t* ostage = reinterpret_cast<uint8_t*>(area + wq * 32 * kBiasStride);
+      auto chunk_at = [&](int row, int k) { return ostage + row * row_bytes + ((k ^ (row & 7)) << 4); };
+      auto stage16 = [&](int c0, const float (&v)[16], float scale) {
         if (out32) {
           #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<float4*>(chunk_at(lane, q)) =
-                make_float4(vv[4 * q] * scale, vv[4 * q + 1] * scale, vv[4 * q + 2] * scale, vv[4 * q + 3] * scale);
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<float4*>(chunk_at(lane, c0 / 4 + q)) =
+                make_float4(v[4 * q] * scale, v[4 * q + 1] * scale, v[4 * q + 2] * scale, v[4 * q + 3] * scale);
         } else {
+          uint32_t w[8];
           #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t w4[4];
-            #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float a = vv[8 * q + 2 * k] * scale, c = vv[8 * q + 2 * k + 1] * scale;
-              w4[k] = args.out_fmt == kBF16 ? pack_bf16x2(a, c) : pack_f16x2(a, c);
-            }
-            *reinterpret_cast<uint4*>(chunk_at(lane, q)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-          }
+          for (int k = 0; k < 8; ++k)
+            w[k] = args.out_fmt == kBF16 ? pack_bf16x2(v[2 * k] * scale, v[2 * k + 1] * scale)
+                                         : pack_f16x2(v[2 * k] * scale, v[2 * k + 1] * scale);
+          *reinterpret_cast<uint4*>(chunk_at(lane, c0 / 8)) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(chunk_at(lane, c0 / 8 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
         }
       };
       auto flush_rows = [&]() {
         __syncwarp();
         const int n0 = qt * kBlockM + wq * 32;  // this warp's first row
-        uint8_t* obase =
-            reinterpret_cast<uint8_t*>(args.out) + (static_cast<size_t>(bh) * N + n0) * row_bytes + h * part_bytes;
-        const int kc = part_bytes / 16;          // chunks per row part (8 or 4)
-        const int per = 32 / kc;                 // row parts per warp instruction
+        uint8_t* obase = reinterpret_cast<uint8_t*>(args.out) + (static_cast<size_t>(bh) * N + n0) * row_bytes;
+        const int per = out32 ? 2 : 4;           // rows per 512-byte run
+        const int kc = out32 ? 16 : 8;           // chunks per row
         for (int i = 0; i < 32 / per; ++i) {
           const int row = per * i + lane / kc, k = lane % kc;
           if (n0 + row < N)
-            *reinterpret_cast<uint4*>(obase + row * row_bytes + (k << 4)) =
-                *reinterpret_cast<const uint4*>(chunk_at(row, k));
+            *reinterpret_cast<uint4*>(obase + row * row_bytes + (k << 4)) = *reinterpret_cast<const uint4*>(chunk_at(row, k));
         }
         __syncwarp();
       };
       if (sg.full(n_kv)) {
-        stage_out(v, 1.0f / l);
-        flush_rows();
-        return true;
-      }
-      // Cut unit: the schedule cuts a unit at most once, into two pieces that
-      // may run in different CTAs; nothing waits on another CTA.
-      //  - If the other piece has already published its (O, m, l), this piece
-      //    merges with it straight away (no publish, no atomic).
-      //  - Otherwise it publishes, then swaps this launch's tag into the
-      //    unit's counter; the piece that finds the tag already there arrived
-      //    second and merges both published slots.  Whatever an earlier (or
-      //    stopped) launch left holds another tag, so the counters never need
-      //    clearing.
-      // Both merges combine the pieces in the same order (the unit's first
-      // piece, then its second) from the same fp32 values, so the result does
-      // not depend on which path ran.
-      const int c = blockIdx.x;
-      const int slot = (sg.tail == 0) ? 2 * c : 2 * c + 1;
-      const long long u0 = static_cast<long long>(sg.u) * n_kv;
-      const int c_first = sched.cta_of(u0);
-      const int sl0 = (sched.begin(c_first) == u0) ? 2 * c_first : 2 * c_first + 1;
-      const int sl1 = 2 * (c_first + 1);
-      // a slot holds O as [16 chunks][128 rows] float4 (this thread's chunks
-      // are 8h .. 8h + 7), then (m, l) per row as [128] float2
-      auto slot_of = [&](int s_) { return args.partials + static_cast<size_t>(s_) * kSlotFloats; };
-      auto ld_chunk = [&](const float* sl, int q) { return __ldcg(reinterpret_cast<const float4*>(sl) + q * kBlockM + r); };
-      auto ld_ml = [&](const float* sl) { return __ldcg(reinterpret_cast<const float2*>(sl + 64 * kBlockM) + r); };
-      // out = (fa O_a + fb O_b) / (fa l_a + fb l_b), rescaled to the larger running max
-      auto merge_store = [&](const float4 (&xa)[8], float2 ma, const float4 (&xb)[8], float2 mb) {
-        const float ms = fmaxf(ma.x, mb.x);
-        const float fa = ex2_approx(ma.x - ms), fb = ex2_approx(mb.x - ms);
-        const float inv_l = 1.0f / (fa * ma.y + fb * mb.y);
-        float vv[32];
+        const float inv_l = 1.0f / l;
         #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          vv[4 * q] = fa * xa[q].x + fb * xb[q].x;
-          vv[4 * q + 1] = fa * xa[q].y + fb * xb[q].y;
-          vv[4 * q + 2] = fa * xa[q].z + fb * xb[q].z;
-          vv[4 * q + 3] = fa * xa[q].w + fb * xb[q].w;
+        for (int c = 0; c < 4; ++c) {
+          uint32_t u[16];
+          tmem_ld16(tO + 16 * c, u);
+          tmem_wait_ld();
+          float v[16];
+          #pragma unroll
+          for (int k = 0; k < 16; ++k) v[k] = __uint_as_float(u[k]);
+          stage16(16 * c, v, inv_l);
         }
-        stage_out(vv, inv_l);
+        tc_fence_before();
+        if (FUSED) mbar_arrive(&bars[kBarEpiDone]);
         flush_rows();
-      };
-      unsigned long long* counter = args.counters + static_cast<size_t>(sg.u);
-      const float2 mown = make_float2(mstar, l);
-      float4 own[8];
-      #pragma unroll
-      for (int q = 0; q < 8; ++q) own[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-      if (leader) {
-        *merge_flag = ld_acquire_gpu(counter) == args.tag;
-        mbar_arrive(&bars[kBarMergeGo]);
-      }
-      if (!warp_all(mbar_wait(&bars[kBarMergeGo], pmerge & 1, abort_flag, status))) return false;
-      ++pmerge;
-      const bool first = slot == sl0;  // warp-uniform
-      if (*merge_flag) {
-        const float* po = slot_of(slot == sl0 ? sl1 : sl0);
-        float4 xo[8];
-        #pragma unroll
-        for (int q = 0; q < 8; ++q) xo[q] = ld_chunk(po, 8 * h + q);
-        const float2 mo = ld_ml(po);
-        if (first) merge_store(own, mown, xo, mo);
-        else merge_store(xo, mo, own, mown);
-        return true;
-      }
-      float* ws = slot_of(slot);
-      #pragma unroll
-      for (int q = 0; q < 8; ++q) __stcg(reinterpret_cast<float4*>(ws) + (8 * h + q) * kBlockM + r, own[q]);
-      if (h == 0) __stcg(reinterpret_cast<float2*>(ws + 64 * kBlockM) + r, mown);
-      // mbarrier arrive/wait order these writes before the leader's GPU-scope
-      // release below (release is cumulative).  Every thread has read
-      // merge_flag above before it arrives here, so the leader may reuse it.
-      mbar_arrive(&bars[kBarPartWritten]);
-      const int pw = ppub++;
-      if (leader) {
-        const bool w_ok = mbar_wait(&bars[kBarPartWritten], pw & 1, abort_flag, status);
-        *merge_flag = w_ok && atomic_exch_acq_rel_gpu(counter, args.tag) == args.tag;
-        mbar_arrive(&bars[kBarMergeGo]);
-      }
-      if (!warp_all(mbar_wait(&bars[kBarMergeGo], pmerge & 1, abort_flag, status))) return false;
-      ++pmerge;
-      // the leader writes merge_flag again only in a later segment's epilogue,
-      // after the prologue barrier that every thread passes once it has read it here
-      if (*merge_flag) {
-        const float* pa = slot_of(sl0);
-        const float* pb = slot_of(sl1);
-        float4 xa[8], xb[8];
-        #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          xa[q] = ld_chunk(pa, 8 * h + q);
-          xb[q] = ld_chunk(pb, 8 * h + q);
+      } else {
+        // Cut unit: the schedule cuts a unit at most once, into two pieces
+        // that may run in different CTAs.  Each query tile has its own
+        // counter, so the two warpgroups never wait for each other, and
+        // nothing waits on another CTA.
+        //  - If the other piece has already published its (O, m, l), this
+        //    piece merges with it straight from TMEM (no publish, no atomic).
+        //  - Otherwise it publishes, then swaps this launch's tag into the
+        //    counter; the piece that finds the tag already there arrived
+        //    second and merges both published slots.  Whatever an earlier
+        //    (or stopped) launch left holds another tag, so the counters
+        //    never need clearing.
+        // Both merges combine the pieces in the same order (the unit's first
+        // piece, then its second) from the same fp32 values, so the result
+        // does not depend on which path ran.
+        const int c = blockIdx.x;
+        const int slot = (sg.tail == 0) ? 2 * c : 2 * c + 1;
+        const long long u0 = static_cast<long long>(sg.u) * n_kv;
+        const int c_first = sched.cta_of(u0);
+        const int sl0 = (sched.begin(c_first) == u0) ? 2 * c_first : 2 * c_first + 1;
+        const int sl1 = 2 * (c_first + 1);
+        // a slot of this query tile; this thread's row is O chunk q at
+        // float4 index q * 128 + r, and (m, l) at float2 index r after the
+        // 64 * 128 floats of O
+        auto slot_of = [&](int s_) { return args.partials + (static_cast<size_t>(s_) * 2 + wg) * kSlotFloats; };
+        auto ld_chunk = [&](const float* sl, int q) { return __ldcg(reinterpret_cast<const float4*>(sl) + q * kBlockM + r); };
+        auto ld_ml = [&](const float* sl) { return __ldcg(reinterpret_cast<const float2*>(sl + 64 * kBlockM) + r); };
+        // out = (fa O_a + fb O_b) / (fa l_a + fb l_b), rescaled to the larger running max
+        auto merge_store = [&](const float4 (&xa)[16], float2 ma, const float4 (&xb)[16], float2 mb) {
+          const float mstar = fmaxf(ma.x, mb.x);
+          const float fa = ex2_approx(ma.x - mstar), fb = ex2_approx(mb.x - mstar);
+          const float inv_l = 1.0f / (fa * ma.y + fb * mb.y);
+          #pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            float v[16];
+            #pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float4 a = xa[4 * cc + q], b = xb[4 * cc + q];
+              v[4 * q] = fa * a.x + fb * b.x;
+              v[4 * q + 1] = fa * a.y + fb * b.y;
+              v[4 * q + 2] = fa * a.z + fb * b.z;
+              v[4 * q + 3] = fa * a.w + fb * b.w;
+            }
+            stage16(16 * cc, v, inv_l);
+          }
+          flush_rows();
+        };
+        unsigned long long* counter = args.counters + 2 * static_cast<size_t>(sg.u) + wg;
+        if (r == 0) {
+          merge_flag[wg] = ld_acquire_gpu(counter) == args.tag;
+          mbar_arrive(&bars[kBarMergeGo + wg]);
         }
-        merge_store(xa, ld_ml(pa), xb, ld_ml(pb));
+        ok = warp_all(mbar_wait(&bars[kBarMergeGo + wg], pseg & 1, abort_flag, status));
+        ++pseg;
+        if (!ok) return false;
+        if (merge_flag[wg]) {
+          const float* po = slot_of(slot == sl0 ? sl1 : sl0);
+          float4 xo[16];
+          #pragma unroll
+          for (int q = 0; q < 16; ++q) xo[q] = ld_chunk(po, q);
+          const float2 mo = ld_ml(po);
+          uint32_t oa[64];
+          tmem_ld32(tO, *reinterpret_cast<uint32_t(*)[32]>(&oa[0]));
+          tmem_ld32(tO + 32, *reinterpret_cast<uint32_t(*)[32]>(&oa[32]));
+          tmem_wait_ld();
+          tc_fence_before();
+          if (FUSED) mbar_arrive(&bars[kBarEpiDone]);
+          const bool first = slot == sl0;  // warp-uniform
+          float4 xa[16], xb[16];
+          #pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const float4 own = make_float4(__uint_as_float(oa[4 * q]), __uint_as_float(oa[4 * q + 1]),
+                                           __uint_as_float(oa[4 * q + 2]), __uint_as_float(oa[4 * q + 3]));
+            xa[q] = first ? own : xo[q];
+            xb[q] = first ? xo[q] : own;
+          }
+          const float2 mown = make_float2(m_used, l);
+          merge_store(xa, first ? mown : mo, xb, first ? mo : mown);
+        } else {
+          float* ws = slot_of(slot);
+          #pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t u[16];
+            tmem_ld16(tO + 16 * cc, u);
+            tmem_wait_ld();
+            #pragma unroll
+            for (int q = 0; q < 4; ++q)
+              __stcg(reinterpret_cast<float4*>(ws) + (4 * cc + q) * kBlockM + r,
+                     make_float4(__uint_as_float(u[4 * q]), __uint_as_float(u[4 * q + 1]),
+                                 __uint_as_float(u[4 * q + 2]), __uint_as_float(u[4 * q + 3])));
+          }
+          __stcg(reinterpret_cast<float2*>(ws + 64 * kBlockM) + r, make_float2(m_used, l));
+          tc_fence_before();
+          if (FUSED) mbar_arrive(&bars[kBarEpiDone]);
+          // mbarrier arrive/wait order these writes before the elected thread's
+          // GPU-scope release below (release is cumulative).  Every thread has
+          // read merge_flag above before it arrives here, so r == 0 may reuse it.
+          mbar_arrive(&bars[kBarPartWritten + wg]);
+          const int pw = ppub++;
+          if (r == 0) {
+            const bool w_ok = mbar_wait(&bars[kBarPartWritten + wg], pw & 1, abort_flag, status);
+            merge_flag[wg] = w_ok && atomic_exch_acq_rel_gpu(counter, args.tag) == args.tag;
+            mbar_arrive(&bars[kBarMergeGo + wg]);
+          }
+          ok = warp_all(mbar_wait(&bars[kBarMergeGo + wg], pseg & 1, abort_flag, status));
+          ++pseg;
+          if (!ok) return false;
+          if (merge_flag[wg]) {
+            const float* pa = slot_of(sl0);
+            const float* pb = slot_of(sl1);
+            float4 xa[16], xb[16];
+            #pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              xa[q] = ld_chunk(pa, q);
+              xb[q] = ld_chunk(pb, q);
+            }
+            merge_store(xa, ld_ml(pa), xb, ld_ml(pb));
+          }
+        }
       }
       return true;
     };
-
     Cursor cur(sched, blockIdx.x);
     Segment sg;
-    while (ok && cur.next(sched, sg)) ok = run_seg(sg, false);
-    // every softmax thread has finished its segments; tell the other roles
-    // whether one must run again
-    mbar_arrive(&bars[kBarDecision]);
-    if (replay_decision(ok, sg)) run_seg(sg, true);
+    int phase = 0, mask;
+    while (next_segment(cur, phase, ok, true, sg, mask)) ok = run_seg(sg, mask) && ok;
   }
 
   tc_fence_before();

@@ -1,0 +1,6 @@
+// Attention kernels for key tiles padded to 40 grid columns.
+#include "attention_inst.cuh"
+
+namespace dera {
+template cudaError_t launch_attention<40>(const AttnMaps&, const AttnArgs&, int, bool, cudaStream_t);
+}  // namespace dera

@@ -22,17 +22,12 @@ constexpr int kSlotFloats = 128 * 66;
 // Key tiles cover KHT whole grid rows of WP (>= W) padded columns, so the
 // column of a key inside its tile fixes kw at compile time.  The padded
 // columns (kw >= W) and padded rows (kh >= H) are zero-filled by TMA and get
-// a -inf bias, which removes them from the softmax.  Each tile splits into two
-// halves of KHT / 2 grid rows (HALF columns); each half is a multiple of 16
-// keys, the K extent of one tcgen05.mma step.
+// a -inf bias, which removes them from the softmax.
 template <int WP>
 struct KeyTile {
   static constexpr int KHT = WP <= 16 ? 8 : (WP <= 32 ? 4 : 2);
   static constexpr int BN = KHT * WP;
-  static constexpr int HALF = BN / 2;
-  static constexpr int GH = KHT / 2;   // grid rows per half
-  static_assert(BN % 32 == 0 && BN <= 128, "tcgen05 N constraint");
-  static_assert(HALF % 16 == 0 && HALF % WP == 0, "a half is whole grid rows and whole MMA K steps");
+  static_assert(BN % 16 == 0 && BN <= 128, "tcgen05 N constraint");
   static_assert(WP % 2 == 0, "packed pairs must not straddle a grid row");
 };
 
@@ -44,12 +39,13 @@ struct AttnArgs {
   const void* rel_w;   // [BH, N, W]
   void* out;           // [BH, N, 64]
   int* status;         // device status word
-  float* partials;     // [2 * gridDim.x][kSlotFloats] partial results (split units only)
-  unsigned long long* counters;  // [n_units] arrival tags per unit (split units only)
+  float* partials;     // [2 * gridDim.x][2][kSlotFloats] partial results (split units only)
+  unsigned long long* counters;  // [n_units][2] arrival tags per unit and query tile (split units only)
   unsigned long long tag;        // this launch's arrival tag: no earlier launch of the process used it
   int BH, H, W, N;
-  int n_qtiles;        // ceil(N / 128): query tiles (work units) per head
-  int n_units;         // BH * n_qtiles
+  int n_qtiles;        // ceil(N / 128)
+  int n_pairs;         // ceil(n_qtiles / 2): query-tile pairs per head
+  int n_units;         // BH * n_pairs
   int n_kv;            // ceil(H / KHT)
   float scale_log2;    // scale * log2(e)
   int in_fmt;          // kF16 | kBF16
@@ -85,11 +81,8 @@ __device__ __forceinline__ float load_elem(const void* p, size_t i, int fmt) {
 // dst[r * stride + (len - 1 - j)] = scale * G[r, first + j] for j in [0, len),
 // i.e. dst[r][k] = scale * G[r, first + len - 1 - k].  With first = qh and
 // len = H this gives dst[r][kh] = scale * rel_h[n, kh].
-// Two threads may share a row: with nparts = 2, the thread with part p only
-// handles the 32-column chunks whose index (within the warp's chunk range)
-// has parity p, so the two threads write disjoint entries of the row.
 __device__ __forceinline__ void skew_row_to_smem(uint32_t tmem_row_base, int first, int len, float* dst_row,
-                                                 float scale, int part = 0, int nparts = 1) {
+                                                 float scale) {
   // Columns [first, first + len) of this row; chunks of 32 are loaded
   // warp-wide (every lane must take part in tcgen05.ld), so the chunk range
   // is the warp's union.
@@ -99,7 +92,7 @@ __device__ __forceinline__ void skew_row_to_smem(uint32_t tmem_row_base, int fir
     lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, off));
     hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, off));
   }
-  for (int cb = (lo & ~31) + 32 * part; cb < hi; cb += 32 * nparts) {
+  for (int cb = lo & ~31; cb < hi; cb += 32) {
     uint32_t u[32];
     tmem_ld32(tmem_row_base + static_cast<uint32_t>(cb), u);
     tmem_wait_ld();

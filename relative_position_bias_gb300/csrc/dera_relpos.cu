@@ -95,9 +95,9 @@ int fmt_of(dera_dtype t) { return t == DERA_F16 ? kF16 : (t == DERA_BF16 ? kBF16
 dera_status check_shape(int BH, int H, int W, int head_dim) {
   if (head_dim != kHeadDim) return DERA_ERR_HEAD_DIM;
   if (BH < 0 || H < 1 || W < 1 || H > 64 || W > 64) return DERA_ERR_SHAPE;
-  // work units: ceil(N/128) query tiles per head must fit 2^31 - 1 in total
-  const long long tiles = (static_cast<long long>(H) * W + kBlockM - 1) / kBlockM;
-  if (tiles * BH > 0x7fffffffLL) return DERA_ERR_SHAPE;
+  // grid size: ceil(N/256) CTAs per head must fit 2^31 - 1 in total
+  const long long pairs = (static_cast<long long>(H) * W + 255) / 256;
+  if (pairs * BH > 0x7fffffffLL) return DERA_ERR_SHAPE;
   return DERA_OK;
 }
 
@@ -162,7 +162,7 @@ bool map_table(CUtensorMap* m, const void* p, dera_dtype t, int L) {
   return make_map(m, p, tma_type(t), 2, dims, strides, box);
 }
 
-int padded_width(int W) { return W <= 16 ? 16 : (W <= 32 ? 32 : (W <= 48 ? 48 : 64)); }
+int padded_width(int W) { return W <= 16 ? 16 : (W <= 32 ? 32 : (W <= 40 ? 40 : 64)); }
 int rows_per_tile(int WP) { return WP <= 16 ? 8 : (WP <= 32 ? 4 : 2); }
 
 // Streaming-multiprocessor count of a device (cached; 0 if the query fails).
@@ -202,9 +202,9 @@ unsigned long long next_launch_tag() {
   return next.fetch_add(1, std::memory_order_relaxed);
 }
 
-// Work decomposition of one call: a unit is one 128-row query tile of one head.
+// Work decomposition of one call: units are pairs of 128-row query tiles.
 struct Plan {
-  int n_qtiles, n_units, n_kv, ctas;
+  int n_qtiles, n_pairs, n_units, n_kv, ctas;
   bool split;              // stream-K over `ctas` persistent CTAs (needs the workspace)
   size_t counters_bytes, partial_bytes;
 };
@@ -214,15 +214,16 @@ Plan make_plan(int BH, int H, int W, int sms) {
   const int N = H * W;
   const int KHT = rows_per_tile(padded_width(W));
   p.n_qtiles = (N + kBlockM - 1) / kBlockM;
-  p.n_units = BH * p.n_qtiles;
+  p.n_pairs = (p.n_qtiles + 1) / 2;
+  p.n_units = BH * p.n_pairs;
   p.n_kv = (H + KHT - 1) / KHT;
   // Split only when the units do not fill whole waves of one CTA per SM; with
   // more units than CTAs every CTA range spans at least one unit's key tiles,
   // so a unit is cut into at most two segments.
   p.split = sms > 0 && p.n_units > sms && p.n_units % sms != 0;
   p.ctas = p.split ? sms : p.n_units;
-  p.counters_bytes = align256(static_cast<size_t>(p.n_units) * sizeof(unsigned long long));  // one per unit
-  p.partial_bytes = static_cast<size_t>(2) * sms * kSlotFloats * sizeof(float);              // two per CTA
+  p.counters_bytes = align256(static_cast<size_t>(p.n_units) * 2 * sizeof(unsigned long long));  // one per query tile
+  p.partial_bytes = static_cast<size_t>(2) * sms * 2 * kSlotFloats * sizeof(float);
   return p;
 }
 
@@ -275,6 +276,7 @@ dera_status run_attention(const void* q, const void* k, const void* v, const voi
   args.W = W;
   args.N = N;
   args.n_qtiles = plan.n_qtiles;
+  args.n_pairs = plan.n_pairs;
   args.n_units = plan.n_units;
   args.n_kv = plan.n_kv;
   args.partials = nullptr;
@@ -294,7 +296,7 @@ dera_status run_attention(const void* q, const void* k, const void* v, const voi
   switch (WP) {
     case 16: e = launch_attention<16>(maps, args, plan.ctas, fused, s); break;
     case 32: e = launch_attention<32>(maps, args, plan.ctas, fused, s); break;
-    case 48: e = launch_attention<48>(maps, args, plan.ctas, fused, s); break;
+    case 40: e = launch_attention<40>(maps, args, plan.ctas, fused, s); break;
     default: e = launch_attention<64>(maps, args, plan.ctas, fused, s); break;
   }
   return e == cudaSuccess ? DERA_OK : DERA_ERR_CUDA;

@@ -251,15 +251,15 @@ def test_split_schedule_ragged(entry, BH):
 
 @pytest.mark.parametrize("name", list(I.WORKLOADS))
 def test_workspace_size_formula(name):
-    """The reported scratch is the documented layout: an 8-byte counter per unit (256-byte
-    aligned), then two 66-float-per-row slots of one query tile per CTA; zero when the units fill
-    whole waves of one CTA per SM."""
+    """The reported scratch is the documented layout: an 8-byte counter per query tile of each
+    unit (256-byte aligned), then two 66-float-per-row slots per CTA and query tile of a unit;
+    zero when the units fill whole waves of one CTA per SM."""
     w = I.WORKLOADS[name]
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     per = query_tiles_per_unit()
     units = w.BH * ((-(-w.N // 128) + per - 1) // per)
     split = units > sms and units % sms != 0
-    want = ((8 * units + 255) // 256 * 256 + 2 * sms * 128 * 66 * 4) if split else 0
+    want = ((8 * per * units + 255) // 256 * 256 + 2 * sms * per * 128 * 66 * 4) if split else 0
     assert rpb.workspace_size(w.BH, w.H, w.W) == want
 
 
