@@ -110,7 +110,9 @@ DERA_API dera_status dera_relpos_project(const void* q, const void* rel_pos_h, c
  * workspace / workspace_bytes: optional scratch, see dera_relpos_workspace_size.
  * Softmax runs in base 2 with fp32 accumulation; P is rounded to fp16 for the
  * P.V product (for bf16 inputs, V tiles are converted to fp16 on chip, so
- * |v| must stay below 65504).
+ * |v| must stay below 65504).  The rounding of P moves each output by at most
+ * (2^-11 + 2^-9) max|v|: a tile whose row sums show less is computed again
+ * before anything is stored.
  */
 DERA_API dera_status dera_relpos_attention(const void* q, const void* k, const void* v, const void* rel_h,
                                   const void* rel_w, void* out, int BH, int H, int W, int head_dim, float scale,
@@ -136,12 +138,13 @@ DERA_API dera_status dera_relpos_fused(const void* q, const void* k, const void*
  * work splits evenly over the device (no scratch used).
  *
  * Scheduling (no counterpart on the pages, which give no kernel schedule):
- * the work unit is one 128-row query tile of one head.  When the number of
- * units is not a whole number of waves of one CTA per SM, the kernel runs one
- * persistent CTA per SM over equal shares of the (unit, key tile) iteration
- * space and cuts some units between two CTAs; the partial results
- * (unnormalised O, row max, row sum, fp32; two 33 792-byte slots per CTA)
- * and one 8-byte arrival counter per unit live in the caller's `workspace`.  A NULL workspace, or one smaller than this size, selects one
+ * the work unit is a pair of 128-row query tiles of one head.  When the
+ * number of units is not a whole number of waves of one CTA per SM, the
+ * kernel runs one persistent CTA per SM over equal shares of the
+ * (unit, key tile) iteration space and cuts some units between two CTAs; the
+ * partial results (unnormalised O, row max, row sum, fp32) and two 8-byte
+ * arrival counters per unit (one per query tile) live in the caller's
+ * `workspace`.  A NULL workspace, or one smaller than this size, selects one
  * CTA per unit instead (same result, no scratch, less even load).  The
  * workspace must be device memory, 256-byte aligned, owned by the caller, and
  * not used by another call in flight.  Its contents need no initialisation
@@ -174,9 +177,9 @@ DERA_API dera_status dera_relpos_workspace_size(int BH, int H, int W, int head_d
  *   - Limit: problems whose split schedule needs more scratch than the
  *     buffer holds are rejected with DERA_ERR_SCRATCH before anything is
  *     enqueued.  The need is what dera_relpos_workspace_size reports: on a
- *     152-SM GB300, 10 272 768 bytes of partial-result slots plus 8 bytes per
- *     work unit (a 128-row query tile of one head), so problems of up to about
- *     1.86 million units fit.  Problems that need no scratch always run.
+ *     152-SM GB300, 20 545 536 bytes of partial-result slots plus 16 bytes per
+ *     work unit (a pair of 128-row query tiles of one head), so problems of
+ *     up to about 288 000 units fit.  Problems that need no scratch always run.
  *   - Sharing: every call on a device uses the same buffer and leaves its
  *     contents behind; like a caller's workspace, the buffer needs no
  *     clearing between calls (see dera_relpos_workspace_size).  Calls that overlap on
