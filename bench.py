@@ -8,8 +8,9 @@ flushed (256 MiB write) between timed steps, outside each step's events.
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU float64
 oracle instead (the reference arm of this method), on a bounded sample.
-Under torchrun every rank runs its own replica of the workload (weak
-scaling; the path has no exchange step) and the slowest rank's time counts.
+Under torchrun the global batch holds N times the workload's (batch, head)
+problems and every rank computes its contiguous range of them (weak scaling;
+the path has no exchange step); the slowest rank's time counts.
 """
 from __future__ import annotations
 
@@ -223,13 +224,15 @@ def run_reference(args, w) -> dict:
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
-def workload_config(w, entry: str) -> dict:
+def workload_config(w, entry: str, world: int = 1) -> dict:
     return {"workload": f"{w.name}: DeepEncoder global attention, B={w.B} heads={w.heads} {w.H}x{w.W} grid "
                         f"(N={w.N}), head_dim {w.d}, {w.dtype}, tables [{2 * w.H - 1},{w.d}] sigma {w.sigma_table}, "
                         f"scale {w.scale:g}",
             "B": w.B, "heads": w.heads, "H": w.H, "W": w.W, "head_dim": w.d, "entry": entry,
             "l2": "flushed between timed steps (256 MiB write outside the step events)",
-            "parallelism": "replicas (one independent workload per GPU)"}
+            "global_BH": world * w.BH,
+            "parallelism": (f"dp{world}: contiguous (batch, head) ranges of the global batch, "
+                            f"{w.BH} per GPU, no data-path collective") if world > 1 else "single GPU"}
 
 
 # --------------------------------------------------------------------------- our arm
@@ -239,10 +242,15 @@ def run_ours(args, w, rank: int, world: int) -> dict | None:
     import relative_position_bias_gb300 as rpb
     from relative_position_bias_gb300 import build as rbuild
     from relative_position_bias_gb300 import inputs as I
+    from relative_position_bias_gb300.shard import bh_range
 
     rbuild.build()
     rpb.load_library()
     dev = torch.device("cuda", torch.cuda.current_device())
+    # weak scaling: the global batch holds world * BH (batch, head) problems and this rank
+    # computes the contiguous range bh_range(world * BH, rank, world), drawn with its own seed
+    lo, hi = bh_range(world * w.BH, rank, world)
+    assert hi - lo == w.BH
     x = I.make_inputs(w, seed=rank)
     d = {k: t.to(dev) for k, t in x.items()}
     out = torch.empty(w.BH, w.N, w.d, dtype=w.torch_dtype, device=dev)
@@ -390,7 +398,7 @@ def run_ours(args, w, rank: int, world: int) -> dict | None:
         "warmup": args.warmup, "ms_per_step": ms_mean, "statistic": "mean over the timed steps",
         "ms_median": ms_med, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": workload_config(w, args.entry),
+        "config": workload_config(w, args.entry, world),
         "ms_p10": percentile(ms, 0.1), "ms_p90": percentile(ms, 0.9),
         "pct_of_bf16_peak": 100.0 * achieved / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",

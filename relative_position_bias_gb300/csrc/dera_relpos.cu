@@ -29,7 +29,7 @@ cudaError_t launch_project(const CUtensorMap& q, const CUtensorMap& th, const CU
                                        ProjSmem::kAlloc);
   if (e != cudaSuccess) return e;
   const int n_qtiles = (args.N + kBlockM - 1) / kBlockM;
-  // persistent: at most max_ctas CTAs (two per SM), each walking a strided list of tiles
+  // persistent: at most max_ctas CTAs (one per SM), each walking a strided list of tiles
   const unsigned tiles = static_cast<unsigned>(n_qtiles) * static_cast<unsigned>(args.BH);
   const unsigned grid = max_ctas > 0 ? std::min(tiles, static_cast<unsigned>(max_ctas)) : tiles;
   relpos_project_kernel<<<grid, kProjThreads, ProjSmem::kAlloc, stream>>>(q, th, tw, args, in_fmt, n_qtiles);
@@ -373,7 +373,7 @@ dera_status dera_relpos_project(const void* q, const void* rel_pos_h, const void
   args.N = N;
   args.bias_fmt = fmt_of(bias_dtype);
   const cudaError_t e =
-      launch_project(mq, mh, mw, args, fmt_of(in_dtype), 2 * sm_count(dev), static_cast<cudaStream_t>(stream));
+      launch_project(mq, mh, mw, args, fmt_of(in_dtype), sm_count(dev), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DERA_OK : DERA_ERR_CUDA;
 }
 
