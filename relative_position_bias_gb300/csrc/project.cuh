@@ -7,37 +7,53 @@
 // Persistent, one CTA per SM: CTA c handles the 128-token tiles c, c + G,
 // c + 2G, ...  A tile's products with every table row, G = Q [T_h ; T_w]^T
 // (128 x 256, fp32), come from one tcgen05.mma of N = 256 into one half of
-// TMEM.  The roles run decoupled, through mbarriers:
-//   - warp 8 (one lane) keeps kProjQStages Q tiles in flight through TMA and
+// TMEM.  Three kinds of warps run decoupled, through mbarriers:
+//   - warp 16 (one lane) keeps kProjQStages Q tiles in flight through TMA and
 //     issues each tile's MMA as soon as its Q has landed and its TMEM half is
-//     free, so the loads and MMAs of later tiles overlap this tile's copy-out;
-//   - warps 0-3 skew the rel_h half of each row through shared memory (a
-//     per-row shift, see skew_row_to_smem) and store the tile's rel_h rows,
-//     which are contiguous in global memory, with coalesced stores; warps 4-7
-//     do the same for rel_w.  Each group syncs on its own named barrier.
+//     free;
+//   - skew warps 0-7 read G out of TMEM and write each row, shifted (see
+//     skew_row_to_smem), into one of two staging buffers: warps 0-3 the
+//     rel_h half, warps 4-7 the rel_w half, each warp its TMEM lane quarter;
+//   - store warps 8-15 copy a staged tile to global memory, where its rel_h
+//     rows (warps 8-11) and rel_w rows (warps 12-15) are contiguous, with
+//     coalesced stores.
+// So the MMA of tile i + 1, the skew of tile i and the stores of tile i - 1
+// run at the same time.
+//
+// Staged row strides: rel_h rows use 65 floats, so that the skew's stores
+// (one column for the whole warp when its rows share qh) fall in 32 different
+// banks; rel_w rows use 68 floats, where the skew's columns already differ
+// per lane (qw follows the lane) and rows stay 16-byte aligned, so the stores
+// read whole 16-byte chunks.
 #pragma once
 #include "common.cuh"
 
 namespace dera {
 
-constexpr int kProjCopyWarps = 8;
-constexpr int kProjThreads = 32 * (kProjCopyWarps + 1);
-constexpr int kProjQStages = 4;
+constexpr int kProjSkewWarps = 8;
+constexpr int kProjStoreWarps = 8;
+constexpr int kProjThreads = 32 * (kProjSkewWarps + kProjStoreWarps + 1);
+constexpr int kProjQStages = 3;
 
 struct ProjSmem {
+  static constexpr int kStrideH = 65;  // floats per staged rel_h row
+  static constexpr int kStrideW = 68;  // floats per staged rel_w row
+  static constexpr int kStageH = kBlockM * kStrideH * 4;
+  static constexpr int kStageW = kBlockM * kStrideW * 4;
   static constexpr int kQ = 0;                                  // kProjQStages x 16 KB
   static constexpr int kTables = kProjQStages * kTileBytes;     // T_h rows 0..127, T_w rows 128..255 (32 KB)
-  static constexpr int kStage = kTables + 2 * kTileBytes;
-  static constexpr int kStride = 65;                            // floats per staged row (>= 64 + 1)
-  static constexpr int kStageBytes = kBlockM * kStride * 4;     // one per part (rel_h, rel_w)
-  static constexpr int kBars = kStage + 2 * kStageBytes;
-  // Q full [S], Q free [S], tables full, G full [2], G free [2]
-  static constexpr int kNumBars = 2 * kProjQStages + 5;
+  static constexpr int kStagesH = kTables + 2 * kTileBytes;     // rel_h staging, 2 buffers
+  static constexpr int kStagesW = kStagesH + 2 * kStageH;       // rel_w staging, 2 buffers
+  static constexpr int kBars = kStagesW + 2 * kStageW;
+  // Q full [S], Q free [S], tables full, G full [2], G free [2],
+  // stage full [part][buffer], stage free [part][buffer]
+  static constexpr int kNumBars = 2 * kProjQStages + 5 + 8;
   static constexpr int kMisc = kBars + ((kNumBars * 8 + 15) & ~15);
   static constexpr int kTotal = kMisc + 16;
   static constexpr int kAlloc = kTotal + 1024;
 };
 static_assert(ProjSmem::kAlloc <= 232448, "shared memory budget");
+static_assert(ProjSmem::kStagesW % 16 == 0 && ProjSmem::kStageW % 16 == 0, "16-byte aligned rel_w stage rows");
 
 __device__ __forceinline__ void store_elem(void* p, size_t i, float x, int fmt) {
   if (fmt == kF32) {
@@ -62,6 +78,8 @@ __global__ void __launch_bounds__(kProjThreads, 1)
   uint64_t* t_full = bars + 2 * kProjQStages;
   uint64_t* g_full = t_full + 1;
   uint64_t* g_free = t_full + 3;
+  uint64_t* s_full = t_full + 5;  // [part * 2 + buffer]
+  uint64_t* s_free = t_full + 9;  // [part * 2 + buffer]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + ProjSmem::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + ProjSmem::kMisc + 4);
 
@@ -72,6 +90,10 @@ __global__ void __launch_bounds__(kProjThreads, 1)
   const int T = (n_tiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1;
   auto tile_of = [&](int i) { return static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x); };
   auto sQ = [&](int i) { return smem + ProjSmem::kQ + (i % kProjQStages) * kTileBytes; };
+  auto stage_of = [&](int part, int i) {
+    return reinterpret_cast<float*>(smem + (part == 0 ? ProjSmem::kStagesH + (i & 1) * ProjSmem::kStageH
+                                                      : ProjSmem::kStagesW + (i & 1) * ProjSmem::kStageW));
+  };
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -82,7 +104,11 @@ __global__ void __launch_bounds__(kProjThreads, 1)
     mbar_init(t_full, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&g_full[b], 1);
-      mbar_init(&g_free[b], kProjCopyWarps);
+      mbar_init(&g_free[b], kProjSkewWarps);
+    }
+    for (int k = 0; k < 4; ++k) {
+      mbar_init(&s_full[k], 128);  // the part's 4 skew warps, every thread
+      mbar_init(&s_free[k], 128);  // the part's 4 store warps, every thread
     }
     fence_mbar_init();
   }
@@ -95,7 +121,7 @@ __global__ void __launch_bounds__(kProjThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
-  if (warp == kProjCopyWarps) {
+  if (warp == kProjSkewWarps + kProjStoreWarps) {
     // ------------------------------------------------------- loads and MMAs
     if (lane == 0) {
       auto load_q = [&](int i) {
@@ -119,7 +145,7 @@ __global__ void __launch_bounds__(kProjThreads, 1)
           load_q(loaded++);
         }
         ok = mbar_wait(&q_full[i % kProjQStages], (i / kProjQStages) & 1, abort_flag, args.status);
-        // TMEM half i & 1 was last read by the copy-out of tile i - 2
+        // TMEM half i & 1 was last read by the skew of tile i - 2
         if (ok && i >= 2) ok = mbar_wait(&g_free[i & 1], ((i >> 1) & 1) ^ 1, abort_flag, args.status);
         if (!ok) break;
         tc_fence_after();
@@ -141,63 +167,80 @@ __global__ void __launch_bounds__(kProjThreads, 1)
           mbar_wait_budget(&g_full[k & 1], (k >> 1) & 1, kWaitBudgetCycles);
       }
     }
-  } else {
-    // ------------------------------------------------------- copy-out
+  } else if (warp < kProjSkewWarps) {
+    // ------------------------------------------------------- skew
     const int part = warp >> 2;    // 0: rel_h, 1: rel_w
     const int wq = warp & 3;       // TMEM lane quarter
-    const int bar_id = 1 + part;   // this part's named barrier
     const int r = wq * 32 + lane;  // tile row = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    float* stage = reinterpret_cast<float*>(smem + ProjSmem::kStage + part * ProjSmem::kStageBytes);
+    const int stride = part == 0 ? ProjSmem::kStrideH : ProjSmem::kStrideW;
     const int len = part == 0 ? H : W;
-    void* dst = part == 0 ? args.rel_h : args.rel_w;
-    const int pt = threadIdx.x & 127;
-    // fp32 rows with len % 4 == 0 leave as 16-byte chunks: chunk e of the tile
-    // is row e / cpr, column 4 (e % cpr); thread pt takes e = pt, pt + 128, ...
-    const int cpr = len / 4;
-    const bool vec = args.bias_fmt == kF32 && len % 4 == 0;
-    const int e_row0 = vec ? pt / cpr : 0, e_col0 = vec ? pt - e_row0 * cpr : 0;
-    const int e_drow = vec ? 128 / cpr : 0, e_dcol = vec ? 128 - e_drow * cpr : 0;
-    bool ok = true;
     for (int i = 0; i < T; ++i) {
-      const int t = tile_of(i);
-      const int qt = t % n_qtiles, bh = t / n_qtiles;
-      ok = bar_and(bar_id, 128, mbar_wait(&g_full[i & 1], (i >> 1) & 1, abort_flag, args.status) && ok);
+      const int n = (tile_of(i) % n_qtiles) * kBlockM + r;
+      // tcgen05.ld is warp-collective: the warp goes on or stops as a whole
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&g_full[i & 1], (i >> 1) & 1, abort_flag, args.status));
+      // staging buffer i & 1 was last read by the stores of tile i - 2
+      if (ok && i >= 2)
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(&s_free[part * 2 + (i & 1)], ((i >> 1) & 1) ^ 1, abort_flag, args.status));
       if (!ok) break;
       tc_fence_after();
-      const int n0 = qt * kBlockM;
-      const int n = n0 + r;
       const int qh = n < N ? n / W : 0;
       const int qw = n < N ? n - qh * W : 0;
-      const int rows = min(kBlockM, N - n0);
       skew_row_to_smem(tbase + 256 * (i & 1) + lane_off + 128 * part, part == 0 ? qh : qw, len,
-                       stage + r * ProjSmem::kStride, 1.0f);
+                       stage_of(part, i) + r * stride, 1.0f);
       tc_fence_before();  // this warp's TMEM reads of the half are done
       __syncwarp();
       if (lane == 0) mbar_arrive(&g_free[i & 1]);
-      bar_sync(bar_id, 128);  // the part's stage is complete
+      mbar_arrive(&s_full[part * 2 + (i & 1)]);  // releases this thread's staged row
+    }
+  } else {
+    // ------------------------------------------------------- stores
+    const int part = (warp - kProjSkewWarps) >> 2;  // 0: rel_h, 1: rel_w
+    const int pt = threadIdx.x & 127;               // thread within the part
+    const int len = part == 0 ? H : W;
+    const int stride = part == 0 ? ProjSmem::kStrideH : ProjSmem::kStrideW;
+    void* dst = part == 0 ? args.rel_h : args.rel_w;
+    // fp32 rows with len % 4 == 0 leave as 16-byte chunks: chunk e is row
+    // e / cpr, column 4 (e % cpr).  Otherwise element e is row e / len,
+    // column e % len.  Thread pt takes e = pt, pt + 128, ..., stepping
+    // (row, column) without a division.
+    const bool vec = args.bias_fmt == kF32 && len % 4 == 0;
+    const int per_row = vec ? len / 4 : len;
+    const int e_row0 = pt / per_row, e_col0 = pt - e_row0 * per_row;
+    const int e_drow = 128 / per_row, e_dcol = 128 - e_drow * per_row;
+    for (int i = 0; i < T; ++i) {
+      if (!mbar_wait(&s_full[part * 2 + (i & 1)], (i >> 1) & 1, abort_flag, args.status)) break;
+      const int t = tile_of(i);
+      const int n0 = (t % n_qtiles) * kBlockM, bh = t / n_qtiles;
+      const int rows = min(kBlockM, N - n0);
+      const float* stage = stage_of(part, i);
       const size_t base = (static_cast<size_t>(bh) * N + n0) * len;
+      int rr = e_row0, c = e_col0;
       if (vec) {
         float4* out4 = reinterpret_cast<float4*>(static_cast<float*>(dst) + base);
-        int rr = e_row0, c = e_col0;
-        for (int e = pt; e < rows * cpr; e += 128) {
-          const float* src = stage + rr * ProjSmem::kStride + 4 * c;
-          out4[e] = make_float4(src[0], src[1], src[2], src[3]);
+        for (int e = pt; e < rows * per_row; e += 128) {
+          const float* src = stage + rr * stride + 4 * c;
+          out4[e] = part == 1 ? *reinterpret_cast<const float4*>(src) : make_float4(src[0], src[1], src[2], src[3]);
           rr += e_drow;
           c += e_dcol;
-          if (c >= cpr) {
-            c -= cpr;
+          if (c >= per_row) {
+            c -= per_row;
             ++rr;
           }
         }
       } else {
-        // a row per warp pass, lanes along it (len <= 64)
-        for (int rr = wq; rr < rows; rr += 4)
-          for (int cc = lane; cc < len; cc += 32)
-            store_elem(dst, base + static_cast<size_t>(rr) * len + cc, stage[rr * ProjSmem::kStride + cc],
-                       args.bias_fmt);
+        for (int e = pt; e < rows * per_row; e += 128) {
+          store_elem(dst, base + static_cast<size_t>(e), stage[rr * stride + c], args.bias_fmt);
+          rr += e_drow;
+          c += e_dcol;
+          if (c >= per_row) {
+            c -= per_row;
+            ++rr;
+          }
+        }
       }
-      bar_sync(bar_id, 128);  // every thread of the part has read the stage
+      mbar_arrive(&s_free[part * 2 + (i & 1)]);  // this thread has read the stage
     }
   }
 
