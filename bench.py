@@ -225,10 +225,11 @@ def run_reference(args, w) -> dict:
 
 
 def workload_config(w, entry: str, world: int = 1) -> dict:
-    return {"workload": f"{w.name}: DeepEncoder global attention, B={w.B} heads={w.heads} {w.H}x{w.W} grid "
-                        f"(N={w.N}), head_dim {w.d}, {w.dtype}, tables [{2 * w.H - 1},{w.d}] sigma {w.sigma_table}, "
-                        f"scale {w.scale:g}",
-            "B": w.B, "heads": w.heads, "H": w.H, "W": w.W, "head_dim": w.d, "entry": entry,
+    kind = (f"DeepEncoder windowed attention, B={w.B} windows={w.windows} heads={w.heads} {w.H}x{w.W} window"
+            if w.windows > 1 else f"DeepEncoder global attention, B={w.B} heads={w.heads} {w.H}x{w.W} grid")
+    return {"workload": f"{w.name}: {kind} (N={w.N}), head_dim {w.d}, {w.dtype}, tables [{2 * w.H - 1},{w.d}] "
+                        f"sigma {w.sigma_table}, scale {w.scale:g}",
+            "B": w.B, "windows": w.windows, "heads": w.heads, "H": w.H, "W": w.W, "head_dim": w.d, "entry": entry,
             "l2": "flushed between timed steps (256 MiB write outside the step events)",
             "global_BH": world * w.BH,
             "parallelism": (f"dp{world}: contiguous (batch, head) ranges of the global batch, "

@@ -135,11 +135,13 @@ DERA_API dera_status dera_relpos_fused(const void* q, const void* k, const void*
 /*
  * Scratch needed by dera_relpos_attention / dera_relpos_fused for a problem
  * size on the current device, written to *bytes (host pointer); 0 when the
- * work splits evenly over the device (no scratch used).
+ * work splits evenly over the device or the units are too short to be worth
+ * cutting (no scratch used).
  *
  * Scheduling (no counterpart on the pages, which give no kernel schedule):
  * the work unit is a pair of 128-row query tiles of one head.  When the
- * number of units is not a whole number of waves of one CTA per SM, the
+ * number of units is not a whole number of waves of one CTA per SM and a
+ * unit spans at least 4 key tiles (grids of at least 4 x 16 or so), the
  * kernel runs one persistent CTA per SM over equal shares of the
  * (unit, key tile) iteration space and cuts some units between two CTAs; the
  * partial results (unnormalised O, row max, row sum, fp32) and two 8-byte

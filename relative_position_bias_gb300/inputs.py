@@ -5,8 +5,10 @@ arithmetic, so both the CUDA path and the CPU oracle can be fed from it.
 
 Workloads follow the DeepEncoder global-attention setting described on the
 vLLM PR #55629 page (section "功能与动机", motivation: 64x64 global attention,
-BF16) plus a small grid, a batched encoder, a ragged 40x40 grid and a wider
-16-head encoder.  Each tensor is drawn as fp32 ``sigma * randn`` from one CPU
+BF16) plus a small grid, a batched encoder, a ragged 40x40 grid, a wider
+16-head encoder, and the same encoder's windowed blocks (section 实现拆解
+item 3 keeps them on SDPA): the 64x64 grid padded to 70x70 and cut into 25
+windows of 14x14, each window an independent attention problem.  Each tensor is drawn as fp32 ``sigma * randn`` from one CPU
 generator in the fixed order q, k, v, rel_pos_h, rel_pos_w and then
 rounded-to-nearest to the workload dtype; the same rounded values go to the
 GPU and to the oracle.
@@ -35,10 +37,11 @@ class Workload:
     sigma_table: float = 0.5
     scale: float = HEAD_DIM ** -0.5
     entry: str = "attention"     # which entry point the workload is quoted on
+    windows: int = 1             # attention problems per image and head (windowed blocks)
 
     @property
     def BH(self) -> int:
-        return self.B * self.heads
+        return self.B * self.windows * self.heads
 
     @property
     def N(self) -> int:
@@ -53,7 +56,7 @@ class Workload:
                        name=f"{self.name}-{H}x{W}")
 
 
-# The five workloads.  scale = 64**-0.5 = 1/8 everywhere (the SDPA default for
+# The workloads.  scale = 64**-0.5 = 1/8 everywhere (the SDPA default for
 # head_dim 64); sigma is a standard deviation.
 WORKLOADS: dict[str, Workload] = {
     "grid16": Workload("grid16", B=1, heads=2, H=16, W=16),
@@ -62,6 +65,7 @@ WORKLOADS: dict[str, Workload] = {
     "ragged40": Workload("ragged40", B=16, heads=12, H=40, W=40, dtype="f16", sigma_q=2.0, sigma_k=2.0,
                          sigma_v=1.0, sigma_table=1.0),
     "wide64": Workload("wide64", B=4, heads=16, H=64, W=64, entry="fused"),
+    "window14": Workload("window14", B=1, heads=12, H=14, W=14, windows=25, entry="fused"),
 }
 
 

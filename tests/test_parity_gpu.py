@@ -84,17 +84,27 @@ def query_tiles_per_unit() -> int:
     return int(m.group(1))
 
 
-def tail_heads(w: I.Workload) -> set[int]:
-    """Heads with a unit in the stream-K tail of the default (workspace) schedule, restated from
-    the host plan: units are groups of query tiles of one head, the tail is the last one and a
-    fraction waves of units when they do not fill whole waves of one CTA per SM.  Cut units only
-    occur there."""
+def default_plan(w: I.Workload) -> tuple[bool, int, int]:
+    """(split, units, units per head) of the default (workspace) schedule, restated from the host
+    plan: units are groups of query tiles of one head; the work is split when the units do not
+    fill whole waves of one CTA per SM and a unit spans at least 4 key tiles (128 keys each:
+    whole grid rows of the padded width 16, 32, 40 or 64)."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     per = query_tiles_per_unit()
     units_per_head = (-(-w.N // 128) + per - 1) // per
     U = w.BH * units_per_head
-    if not (U > sms and U % sms != 0):
+    wp = next(x for x in (16, 32, 40, 64) if x >= w.W)
+    n_kv = -(-w.H // {16: 8, 32: 4, 40: 2, 64: 2}[wp])
+    return (n_kv >= 4 and U > sms and U % sms != 0), U, units_per_head
+
+
+def tail_heads(w: I.Workload) -> set[int]:
+    """Heads with a unit in the stream-K tail of the default schedule: the last one and a fraction
+    waves of units when the work is split.  Cut units only occur there."""
+    split, U, units_per_head = default_plan(w)
+    if not split:
         return set()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
     first_tail = max(U // sms - 1, 0) * sms
     return {u // units_per_head for u in range(first_tail, U)}
 
@@ -253,12 +263,11 @@ def test_split_schedule_ragged(entry, BH):
 def test_workspace_size_formula(name):
     """The reported scratch is the documented layout: an 8-byte counter per query tile of each
     unit (256-byte aligned), then two 66-float-per-row slots per CTA and query tile of a unit;
-    zero when the units fill whole waves of one CTA per SM."""
+    zero when the units fill whole waves of one CTA per SM or span fewer than 4 key tiles."""
     w = I.WORKLOADS[name]
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     per = query_tiles_per_unit()
-    units = w.BH * ((-(-w.N // 128) + per - 1) // per)
-    split = units > sms and units % sms != 0
+    split, units, _ = default_plan(w)
     want = ((8 * per * units + 255) // 256 * 256 + 2 * sms * per * 128 * 66 * 4) if split else 0
     assert rpb.workspace_size(w.BH, w.H, w.W) == want
 
