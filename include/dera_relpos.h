@@ -32,7 +32,8 @@
  *       q, k, v, out : [BH, N, head_dim], N = H*W, token n = qh*W + qw
  *       rel_pos_h    : [2H-1, head_dim]      rel_pos_w : [2W-1, head_dim]
  *       rel_h        : [BH, N, H]            rel_w     : [BH, N, W]
- *   - head_dim must be 64.  q, k, v, tables share one dtype: DERA_F16 or
+ *   - head_dim is 64 or 128 (the pages' kernel fixes 64; 128 is this
+ *     library's extension).  q, k, v, tables share one dtype: DERA_F16 or
  *     DERA_BF16.  1 <= H, W <= 64.  BH >= 0 (BH == 0 is a no-op).
  *   - Buffer lengths are the caller's precondition: the ABI takes no length
  *     arguments, so a table must hold exactly 2H-1 (2W-1) rows and every
@@ -75,7 +76,7 @@ typedef enum dera_status {
   DERA_ERR_NULL = 1,        /* a required pointer is NULL */
   DERA_ERR_SHAPE = 2,       /* H, W, BH out of range, or N overflow */
   DERA_ERR_DTYPE = 3,       /* dtype not supported for that argument */
-  DERA_ERR_HEAD_DIM = 4,    /* head_dim != 64 */
+  DERA_ERR_HEAD_DIM = 4,    /* head_dim is neither 64 nor 128 */
   DERA_ERR_ALIGN = 5,       /* a pointer is not 16-byte aligned */
   DERA_ERR_DEVICE = 6,      /* a pointer is not device memory of the current device */
   DERA_ERR_TIMEOUT = 7,     /* (device status only) a bounded wait expired */
@@ -139,10 +140,10 @@ DERA_API dera_status dera_relpos_fused(const void* q, const void* k, const void*
  * cutting (no scratch used).
  *
  * Scheduling (no counterpart on the pages, which give no kernel schedule):
- * the work unit is a pair of 128-row query tiles of one head.  When the
- * number of units is not a whole number of waves of one CTA per SM and a
- * unit spans at least 4 key tiles (grids of at least 4 x 16 or so), the
- * kernel runs one persistent CTA per SM over equal shares of the
+ * the work unit is a pair of 128-row query tiles of one head.  When
+ * head_dim is 64, the number of units is not a whole number of waves of one
+ * CTA per SM and a unit spans at least 4 key tiles (grids of at least 4 x 16
+ * or so), the kernel runs one persistent CTA per SM over equal shares of the
  * (unit, key tile) iteration space and cuts some units between two CTAs; the
  * partial results (unnormalised O, row max, row sum, fp32) and two 8-byte
  * arrival counters per unit (one per query tile) live in the caller's

@@ -24,9 +24,11 @@
 //   warp 2      TMEM allocator; with warp 3, converts bf16 V tiles to fp16
 //   warps 4-7   softmax / epilogue of query tile 0 (one thread per row)
 //   warps 8-11  softmax / epilogue of query tile 1
-// TMEM (512 columns): S0 [0,128) S1 [128,256) P0 [256,320) P1 [320,384)
-//                     O0 [384,448) O1 [448,512); the fused prologue uses all
-//                     512 columns for G_i = Q_i [T_h ; T_w]^T before each segment.
+// TMEM (512 columns), head_dim 64: S0 [0,128) S1 [128,256) P0 [256,320)
+//   P1 [320,384) O0 [384,448) O1 [448,512); head_dim 128 (key tiles of at most
+//   80 keys): S_i [128i, 128i+80) P_i [128i+88, 128i+128) O_i [256+128i, 384+128i).
+//   The fused prologue uses all 512 columns for G_i = Q_i [T_h ; T_w]^T before
+//   each segment.
 #pragma once
 #include <cfloat>
 
@@ -34,7 +36,7 @@
 
 namespace dera {
 
-constexpr int kStages = 3;
+constexpr int kMaxStages = 3;     // K/V ring depth (head_dim 64; 2 for head_dim 128)
 constexpr int kTilesPerUnit = 2;  // 128-row query tiles per work unit
 constexpr int kAttnThreads = 384;
 // Largest accepted row sum of a speculative tile: with the sum at most this,
@@ -49,7 +51,6 @@ constexpr float kStartMargin = 4.0f;
 // running maximum, must be at least the segment's valid key count times
 // 2^kMinRowSumLog2 (see the epilogue).
 constexpr int kMinRowSumLog2 = -16;
-constexpr int kBiasStride = 66;       // floats per row of a bias staging area
 // Register split: the producer / MMA / V-conversion warpgroup gives registers
 // back and the two softmax warpgroups take them, which removes the softmax's
 // spills.  The block launches with kLaunchRegs per thread (the most that 384
@@ -61,28 +62,54 @@ constexpr int kRegsSmx = 200;
 static_assert(kRegsCtl * 128 + kRegsSmx * 256 <= kLaunchRegs * kAttnThreads, "register split exceeds the launch pool");
 static_assert(kRegsCtl % 8 == 0 && kRegsSmx % 8 == 0, "setmaxnreg counts are multiples of 8");
 
+// Shapes that depend on the head dimension D (64 or 128) and the key-tile
+// width BN.
+template <int D, int BN>
+struct AttnDims {
+  static constexpr int kAtoms = atoms_of<D>();
+  static constexpr int kQTile = kBlockM * 2 * D;                 // one 128-row query tile
+  // K (and V) region of a ring stage: BN rows of 2D bytes (at most 128 x 128 B
+  // for head_dim 64; 64 or 80 x 256 B for head_dim 128)
+  static constexpr int kKVBytes = D == 64 ? kTileBytes : BN * 2 * D;
+  static constexpr int kStageBytes = 2 * kKVBytes;
+  // K/V ring depth: three stages, except for head_dim 128 with 80-key tiles,
+  // where three do not fit beside the query tiles and the bias areas
+  static constexpr int kStages = kStageBytes <= 32 * 1024 ? 3 : 2;
+  // floats per row of a bias staging area (65 where a third stage has to fit)
+  static constexpr int kBiasStride = D == 64 ? 66 : 65;
+  // ring stages the fused prologue's tables take: [T_h | T_w] in one stage,
+  // or T_h and T_w (32 KB each) in one stage apiece
+  static constexpr int kTableSlots = D == 64 ? 1 : 2;
+  // TMEM columns of query tile i
+  static constexpr uint32_t tmS(int i) { return 128u * i; }
+  static constexpr uint32_t tmP(int i) { return D == 64 ? 256u + 64u * i : 128u * i + 88u; }
+  static constexpr uint32_t tmO(int i) { return D == 64 ? 384u + 64u * i : 256u + 128u * i; }
+  static_assert(kMaxStages >= kStages, "barrier slots");
+};
+
+template <int D, int BN>
 struct AttnSmem {
-  static constexpr int kQ = 0;                                   // 2 x 16 KB
-  static constexpr int kRing = 2 * kTileBytes;                   // stages: [K 16 KB][V 16 KB]
-  static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kBias = kRing + kStages * kStageBytes;    // 2 x 128 x 66 floats
-  static constexpr int kBiasBytes = 2 * kBlockM * kBiasStride * 4;
+  using Dm = AttnDims<D, BN>;
+  static constexpr int kQ = 0;                                   // 2 query tiles
+  static constexpr int kRing = 2 * Dm::kQTile;                   // stages: [K][V]
+  static constexpr int kBias = kRing + Dm::kStages * Dm::kStageBytes;  // 2 bias areas of 128 rows
+  static constexpr int kBiasBytes = 2 * kBlockM * Dm::kBiasStride * 4;
   static constexpr int kBars = kBias + kBiasBytes;
   static constexpr int kNumBars = 32;
   static constexpr int kMisc = kBars + kNumBars * 8;             // tmem slot, flags, replay records
   static constexpr int kTotal = kMisc + 96;
   static constexpr int kAlloc = kTotal + 1024;                   // slack for 1 KB alignment
+  static_assert(kAlloc <= 232448, "shared memory budget");
 };
-static_assert(AttnSmem::kAlloc <= 232448, "shared memory budget");
 
 // barrier indices
 enum : int {
   kBarQFull = 0,
   kBarQEmpty = 1,
   kBarKVFull = 2,                     // + stage
-  kBarKVEmpty = kBarKVFull + kStages,
-  kBarVReady = kBarKVEmpty + kStages,
-  kBarSFull = kBarVReady + kStages,   // + tile
+  kBarKVEmpty = kBarKVFull + kMaxStages,
+  kBarVReady = kBarKVEmpty + kMaxStages,
+  kBarSFull = kBarVReady + kMaxStages,   // + tile
   kBarPFull = kBarSFull + 2,
   kBarODone = kBarPFull + 2,
   kBarGFull = kBarODone + 2,
@@ -95,7 +122,7 @@ enum : int {
   kBarMmaDone = kBarDecision + 1,
   kBarCount = kBarMmaDone + 1
 };
-static_assert(kBarCount <= AttnSmem::kNumBars, "barrier slots");
+static_assert(kBarCount <= AttnSmem<64, 128>::kNumBars, "barrier slots");
 
 // Work schedule over G persistent CTAs: all but the last one-and-a-fraction
 // waves of units run as data-parallel rounds (CTA c takes unit r*G + c in
@@ -192,24 +219,28 @@ struct ReplayRecord {
   Segment sg;
 };
 
-template <int WP, bool FUSED, bool BF16>
+template <int WP, bool FUSED, bool BF16, int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     relpos_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_th,
                        const __grid_constant__ CUtensorMap tm_tw, const AttnArgs args) {
-  using KT = KeyTile<WP>;
+  using KT = KeyTile<WP, D>;
+  using Dm = AttnDims<D, KT::BN>;
+  using SM = AttnSmem<D, KT::BN>;
+  constexpr int kBiasStride = Dm::kBiasStride;
   constexpr int KHT = KT::KHT;
   constexpr int BN = KT::BN;
+  constexpr int KS = Dm::kStages;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_u + 1023u) & ~1023u) - raw_u);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + AttnSmem::kBars);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + AttnSmem::kMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + AttnSmem::kMisc + 4);
-  volatile int* merge_flag = reinterpret_cast<volatile int*>(smem + AttnSmem::kMisc + 8);  // [2]
-  volatile int* bad_flag = reinterpret_cast<volatile int*>(smem + AttnSmem::kMisc + 16);   // [2 tiles][2 parities]
-  ReplayRecord* replay = reinterpret_cast<ReplayRecord*>(smem + AttnSmem::kMisc + 32);     // [2 tiles]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::kBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM::kMisc + 4);
+  volatile int* merge_flag = reinterpret_cast<volatile int*>(smem + SM::kMisc + 8);  // [2]
+  volatile int* bad_flag = reinterpret_cast<volatile int*>(smem + SM::kMisc + 16);   // [2 tiles][2 parities]
+  ReplayRecord* replay = reinterpret_cast<ReplayRecord*>(smem + SM::kMisc + 32);     // [2 tiles]
   int* status = args.status;
 
   const int warp = threadIdx.x >> 5;
@@ -218,9 +249,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const Schedule sched(args.n_units, static_cast<int>(gridDim.x), n_kv);
   constexpr bool convert_v = BF16;  // P is fp16, so bf16 V tiles are converted to fp16 on chip
 
-  auto sQ = [&](int i) { return smem + AttnSmem::kQ + i * kTileBytes; };
-  auto sK = [&](int s) { return smem + AttnSmem::kRing + s * AttnSmem::kStageBytes; };
-  auto sV = [&](int s) { return smem + AttnSmem::kRing + s * AttnSmem::kStageBytes + kTileBytes; };
+  auto sQ = [&](int i) { return smem + SM::kQ + i * Dm::kQTile; };
+  auto sK = [&](int s) { return smem + SM::kRing + s * Dm::kStageBytes; };
+  auto sV = [&](int s) { return smem + SM::kRing + s * Dm::kStageBytes + Dm::kKVBytes; };
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -231,7 +262,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     replay[1].pending = 0;
     mbar_init(&bars[kBarQFull], 1);
     mbar_init(&bars[kBarQEmpty], 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < KS; ++s) {
       mbar_init(&bars[kBarKVFull + s], 1);
       mbar_init(&bars[kBarKVEmpty + s], 1);
       mbar_init(&bars[kBarVReady + s], 64);
@@ -313,24 +344,38 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int bh = sg.u / args.n_pairs;
         const int qt0 = 2 * (sg.u - bh * args.n_pairs);
         if (seg > 0 && !mbar_wait(&bars[kBarQEmpty], (seg - 1) & 1, abort_flag, status)) return false;
-        mbar_arrive_expect_tx(&bars[kBarQFull], 2 * kTileBytes);
-        tma_load_3d(sQ(0), &tm_q, &bars[kBarQFull], 0, qt0 * kBlockM, bh);
-        tma_load_3d(sQ(1), &tm_q, &bars[kBarQFull], 0, (qt0 + 1) * kBlockM, bh);
+        mbar_arrive_expect_tx(&bars[kBarQFull], 2 * Dm::kQTile);
+        #pragma unroll
+        for (int i = 0; i < 2; ++i)
+          #pragma unroll
+          for (int a = 0; a < Dm::kAtoms; ++a)
+            tma_load_3d(sQ(i) + a * kTileBytes, &tm_q, &bars[kBarQFull], 64 * a, (qt0 + i) * kBlockM, bh);
         ++seg;
         if (FUSED) {
-          const int s = rg % kStages;
-          if (!mbar_wait(&bars[kBarKVEmpty + s], ((rg / kStages) & 1) ^ 1, abort_flag, status)) return false;
-          mbar_arrive_expect_tx(&bars[kBarKVFull + s], 2 * kTileBytes);
-          tma_load_2d(sK(s), &tm_th, &bars[kBarKVFull + s], 0, 0);
-          tma_load_2d(sV(s), &tm_tw, &bars[kBarKVFull + s], 0, 0);
-          ++rg;
+          for (int t = 0; t < Dm::kTableSlots; ++t, ++rg) {
+            const int s = rg % KS;
+            if (!mbar_wait(&bars[kBarKVEmpty + s], ((rg / KS) & 1) ^ 1, abort_flag, status)) return false;
+            mbar_arrive_expect_tx(&bars[kBarKVFull + s], 2 * kTileBytes);
+            if (D == 64) {
+              tma_load_2d(sK(s), &tm_th, &bars[kBarKVFull + s], 0, 0);
+              tma_load_2d(sV(s), &tm_tw, &bars[kBarKVFull + s], 0, 0);
+            } else {
+              // one table per stage, its two atoms back to back
+              #pragma unroll
+              for (int a = 0; a < Dm::kAtoms; ++a)
+                tma_load_2d(sK(s) + a * kTileBytes, t == 0 ? &tm_th : &tm_tw, &bars[kBarKVFull + s], 64 * a, 0);
+            }
+          }
         }
         for (int j = sg.j0; j < sg.j1; ++j, ++rg) {
-          const int s = rg % kStages;
-          if (!mbar_wait(&bars[kBarKVEmpty + s], ((rg / kStages) & 1) ^ 1, abort_flag, status)) return false;
-          mbar_arrive_expect_tx(&bars[kBarKVFull + s], 2 * BN * kRowBytes);
-          tma_load_4d(sK(s), &tm_k, &bars[kBarKVFull + s], 0, 0, j * KHT, bh);
-          tma_load_4d(sV(s), &tm_v, &bars[kBarKVFull + s], 0, 0, j * KHT, bh);
+          const int s = rg % KS;
+          if (!mbar_wait(&bars[kBarKVEmpty + s], ((rg / KS) & 1) ^ 1, abort_flag, status)) return false;
+          mbar_arrive_expect_tx(&bars[kBarKVFull + s], 2 * BN * 2 * D);
+          #pragma unroll
+          for (int a = 0; a < Dm::kAtoms; ++a) {
+            tma_load_4d(sK(s) + a * BN * 128, &tm_k, &bars[kBarKVFull + s], 64 * a, 0, j * KHT, bh);
+            tma_load_4d(sV(s) + a * BN * 128, &tm_v, &bars[kBarKVFull + s], 64 * a, 0, j * KHT, bh);
+          }
         }
         return true;
       };
@@ -341,8 +386,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (!ok) {
         // Let the copies already in flight land before the CTA exits.
         if (seg > 0) mbar_wait_budget(&bars[kBarQFull], (seg - 1) & 1, kWaitBudgetCycles);
-        for (int r = max(0, rg - kStages); r < rg; ++r)
-          mbar_wait_budget(&bars[kBarKVFull + r % kStages], (r / kStages) & 1, kWaitBudgetCycles);
+        for (int r = max(0, rg - KS); r < rg; ++r)
+          mbar_wait_budget(&bars[kBarKVFull + r % KS], (r / KS) & 1, kWaitBudgetCycles);
       }
     }
   } else if (warp == 1) {
@@ -352,26 +397,37 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     {
       constexpr uint32_t fmt = BF16 ? kBF16 : kF16;
       constexpr uint32_t id_qk = idesc_f16(kBlockM, BN, fmt, fmt, 0, 0);
-      constexpr uint32_t id_pv = idesc_f16(kBlockM, kHeadDim, kF16, kF16, 0, 1);
-      constexpr uint32_t id_g = idesc_f16(kBlockM, 256, fmt, fmt, 0, 0);
+      // PV in 64-column halves of O (one V atom each)
+      constexpr uint32_t id_pv = idesc_f16(kBlockM, 64, kF16, kF16, 0, 1);
+      // G: [T_h ; T_w] as one N = 256 product (head_dim 64), or T_h and T_w
+      // as two N = 128 products from their own stages (head_dim 128)
+      constexpr uint32_t id_g = idesc_f16(kBlockM, D == 64 ? 256 : 128, fmt, fmt, 0, 0);
       // Descriptors differ only in their 14-bit start-address field (address / 16),
       // which stays below 2^14 for any shared-memory address, so offsets are
       // added to one base descriptor per operand.
       const uint64_t d_q = sdesc_sw128(smem_u32(sQ(0)), 16, 1024);
       const uint64_t d_k = sdesc_sw128(smem_u32(sK(0)), 16, 1024);
       const uint64_t d_v = sdesc_sw128(smem_u32(sV(0)), 16, 1024);
-      constexpr uint32_t kQStep = kTileBytes >> 4, kStageStep = AttnSmem::kStageBytes >> 4;
+      constexpr uint32_t kQStep = Dm::kQTile >> 4, kStageStep = Dm::kStageBytes >> 4;
+      // atom strides: 128 rows of a query tile or table, BN rows of a K/V tile
+      constexpr uint32_t kQAtom = kTileBytes >> 4, kKVAtom = (BN * 128) >> 4;
+      // K-step k (16 elements) of a K-major operand: atom k / 4, 32 bytes per step inside it
+      auto kstep = [](int k, uint32_t atom) { return static_cast<uint32_t>(k / 4) * atom + 2u * (k % 4); };
       auto issue_qk = [&](int i, int s) {
         const uint64_t a = d_q + i * kQStep, b = d_k + s * kStageStep;
         #pragma unroll
-        for (int k = 0; k < 4; ++k) umma_ss_w(tbase + 128 * i, a + 2 * k, b + 2 * k, id_qk, k > 0);
+        for (int k = 0; k < D / 16; ++k)
+          umma_ss_w(tbase + Dm::tmS(i), a + kstep(k, kQAtom), b + kstep(k, kKVAtom), id_qk, k > 0);
       };
       auto issue_pv = [&](int i, int s, bool acc) {
-        const uint64_t b = d_v + s * kStageStep;
         #pragma unroll
-        for (int k = 0; k < BN / 16; ++k)
-          umma_ts_w(tbase + 384 + 64 * i, tbase + 256 + 64 * i + 8 * k, b + 128 * k, id_pv,
-                    (acc || k > 0) ? 1u : 0u);
+        for (int h = 0; h < Dm::kAtoms; ++h) {
+          const uint64_t b = d_v + s * kStageStep + h * kKVAtom;
+          #pragma unroll
+          for (int k = 0; k < BN / 16; ++k)
+            umma_ts_w(tbase + Dm::tmO(i) + 64 * h, tbase + Dm::tmP(i) + 8 * k, b + 128 * k, id_pv,
+                      (acc || k > 0) ? 1u : 0u);
+        }
       };
       int rg = 0, gi = 0, seg = 0;
       bool ok = true;
@@ -380,24 +436,30 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (!warp_all(mbar_wait(&bars[kBarQFull], seg & 1, abort_flag, status))) return false;
         if (FUSED) {
           if (seg > 0 && !warp_all(mbar_wait(&bars[kBarEpiDone], (seg - 1) & 1, abort_flag, status))) return false;
-          const int s = rg % kStages;
-          if (!warp_all(mbar_wait(&bars[kBarKVFull + s], (rg / kStages) & 1, abort_flag, status))) return false;
+          for (int t = 0; t < Dm::kTableSlots; ++t) {
+            const int s = (rg + t) % KS;
+            if (!warp_all(mbar_wait(&bars[kBarKVFull + s], ((rg + t) / KS) & 1, abort_flag, status))) return false;
+          }
           tc_fence_after();
           for (int i = 0; i < 2; ++i) {
-            const uint64_t a = d_q + i * kQStep, b = d_k + s * kStageStep;
+            const uint64_t a = d_q + i * kQStep;
             #pragma unroll
-            for (int k = 0; k < 4; ++k) umma_ss_w(tbase + 256 * i, a + 2 * k, b + 2 * k, id_g, k > 0);
+            for (int t = 0; t < Dm::kTableSlots; ++t) {
+              const uint64_t b = d_k + ((rg + t) % KS) * kStageStep;
+              #pragma unroll
+              for (int k = 0; k < D / 16; ++k)
+                umma_ss_w(tbase + 256 * i + 128 * t, a + kstep(k, kQAtom), b + kstep(k, kQAtom), id_g, k > 0);
+            }
           }
           umma_commit_w(&bars[kBarGFull]);
-          umma_commit_w(&bars[kBarKVEmpty + s]);
-          ++rg;
+          for (int t = 0; t < Dm::kTableSlots; ++t, ++rg) umma_commit_w(&bars[kBarKVEmpty + rg % KS]);
           if (!warp_all(mbar_wait(&bars[kBarGFree], seg & 1, abort_flag, status))) return false;
           tc_fence_after();
         }
         ++seg;
         {
-          const int s = rg % kStages;
-          if (!warp_all(mbar_wait(&bars[kBarKVFull + s], (rg / kStages) & 1, abort_flag, status))) return false;
+          const int s = rg % KS;
+          if (!warp_all(mbar_wait(&bars[kBarKVFull + s], (rg / KS) & 1, abort_flag, status))) return false;
           tc_fence_after();
           issue_qk(0, s);
           umma_commit_w(&bars[kBarSFull + 0]);
@@ -405,8 +467,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           umma_commit_w(&bars[kBarSFull + 1]);
         }
         for (int jj = 0; jj < len; ++jj, ++rg, ++gi) {
-          const int s = rg % kStages, ph = (rg / kStages) & 1;
-          const int sn = (rg + 1) % kStages, phn = ((rg + 1) / kStages) & 1;
+          const int s = rg % KS, ph = (rg / KS) & 1;
+          const int sn = (rg + 1) % KS, phn = ((rg + 1) / KS) & 1;
           const bool more = jj + 1 < len;
           if (convert_v && !warp_all(mbar_wait(&bars[kBarVReady + s], ph, abort_flag, status))) return false;
           // Once softmax i has written P_i(j) (and so finished reading S_i),
@@ -454,12 +516,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       int rg = 0;
       bool ok = true;
       auto run_seg = [&](const Segment& sg) -> bool {
-        for (int j = FUSED ? sg.j0 - 1 : sg.j0; j < sg.j1; ++j, ++rg) {
-          const int s = rg % kStages;
-          if (!mbar_wait(&bars[kBarKVFull + s], (rg / kStages) & 1, abort_flag, status)) return false;
+        for (int j = FUSED ? sg.j0 - Dm::kTableSlots : sg.j0; j < sg.j1; ++j, ++rg) {
+          const int s = rg % KS;
+          if (!mbar_wait(&bars[kBarKVFull + s], (rg / KS) & 1, abort_flag, status)) return false;
           if (j >= sg.j0) {
             uint4* vp = reinterpret_cast<uint4*>(sV(s));
-            for (int idx = ct; idx < BN * kRowBytes / 16; idx += 64) {
+            for (int idx = ct; idx < BN * 2 * D / 16; idx += 64) {
               uint4 w = vp[idx];
               w.x = bf16x2_to_f16x2(w.x);
               w.y = bf16x2_to_f16x2(w.y);
@@ -487,10 +549,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int r = wq * 32 + lane;            // row inside the tile
     const int H = args.H, W = args.W, N = args.N;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tbase + lane_off + 128 * wg;
-    const uint32_t tP = tbase + lane_off + 256 + 64 * wg;
-    const uint32_t tO = tbase + lane_off + 384 + 64 * wg;
-    float* area = reinterpret_cast<float*>(smem + AttnSmem::kBias) + wg * kBlockM * kBiasStride;
+    const uint32_t tS = tbase + lane_off + Dm::tmS(wg);
+    const uint32_t tP = tbase + lane_off + Dm::tmP(wg);
+    const uint32_t tO = tbase + lane_off + Dm::tmO(wg);
+    float* area = reinterpret_cast<float*>(smem + SM::kBias) + wg * kBlockM * kBiasStride;
     const int Hpad = n_kv * KHT;
     const int HS = Hpad + 1;
     float* bh_row = area + r * HS;
@@ -724,7 +786,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             lsum.x *= alpha;
             lsum.y *= alpha;
             #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < D / 32; ++c) {
               uint32_t o[32];
               tmem_ld32(tO + 32 * c, o);
               tmem_wait_ld();
@@ -776,12 +838,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         return true;
       }
       // Output rows leave through this warp's quarter of the bias area (no
-      // warp of the warpgroup reads its bias rows once O is complete): each
-      // lane stages its row, 16-byte chunks XOR-swizzled by row so neither
-      // side has bank conflicts, then the warp stores runs of 512 contiguous
-      // bytes (4 bf16/f16 rows or 2 fp32 rows per instruction).
+      // warp of the warpgroup reads its bias rows once O is complete), 64
+      // columns at a time: each lane stages its row's 64 columns, 16-byte
+      // chunks XOR-swizzled by row so neither side has bank conflicts, then the
+      // warp stores runs of 512 contiguous staged bytes (4 bf16/f16 rows or 2
+      // fp32 rows per instruction; with head_dim 128 each row's half is a run
+      // of 128 or 256 bytes).
       const bool out32 = args.out_fmt == kF32;
-      const int row_bytes = out32 ? 256 : 128;
+      const int row_bytes = out32 ? 256 : 128;   // staged bytes of a row's 64 columns
+      const int out_row = row_bytes * Dm::kAtoms;  // bytes of an output row
       uint8_t* ostage = reinterpret_cast<uint8_t*>(area + wq * 32 * kBiasStride);
       auto chunk_at = [&](int row, int k) { return ostage + row * row_bytes + ((k ^ (row & 7)) << 4); };
       auto stage16 = [&](int c0, const float (&v)[16], float scale) {
@@ -800,34 +865,45 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           *reinterpret_cast<uint4*>(chunk_at(lane, c0 / 8 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
         }
       };
-      auto flush_rows = [&]() {
+      // the staged 64 columns of every row go to columns [64h, 64h + 64) of the output
+      auto flush_rows = [&](int h) {
         __syncwarp();
         const int n0 = qt * kBlockM + wq * 32;  // this warp's first row
-        uint8_t* obase = reinterpret_cast<uint8_t*>(args.out) + (static_cast<size_t>(bh) * N + n0) * row_bytes;
+        uint8_t* obase = reinterpret_cast<uint8_t*>(args.out) + (static_cast<size_t>(bh) * N + n0) * out_row +
+                         h * row_bytes;
         const int per = out32 ? 2 : 4;           // rows per 512-byte run
         const int kc = out32 ? 16 : 8;           // chunks per row
         for (int i = 0; i < 32 / per; ++i) {
           const int row = per * i + lane / kc, k = lane % kc;
           if (n0 + row < N)
-            *reinterpret_cast<uint4*>(obase + row * row_bytes + (k << 4)) = *reinterpret_cast<const uint4*>(chunk_at(row, k));
+            *reinterpret_cast<uint4*>(obase + row * out_row + (k << 4)) = *reinterpret_cast<const uint4*>(chunk_at(row, k));
         }
         __syncwarp();
       };
       if (sg.full(n_kv)) {
         const float inv_l = 1.0f / l;
         #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t u[16];
-          tmem_ld16(tO + 16 * c, u);
-          tmem_wait_ld();
-          float v[16];
+        for (int h = 0; h < Dm::kAtoms; ++h) {
           #pragma unroll
-          for (int k = 0; k < 16; ++k) v[k] = __uint_as_float(u[k]);
-          stage16(16 * c, v, inv_l);
+          for (int c = 0; c < 4; ++c) {
+            uint32_t u[16];
+            tmem_ld16(tO + 64 * h + 16 * c, u);
+            tmem_wait_ld();
+            float v[16];
+            #pragma unroll
+            for (int k = 0; k < 16; ++k) v[k] = __uint_as_float(u[k]);
+            stage16(16 * c, v, inv_l);
+          }
+          if (h == Dm::kAtoms - 1) {
+            tc_fence_before();
+            if (FUSED) mbar_arrive(&bars[kBarEpiDone]);
+          }
+          flush_rows(h);
         }
-        tc_fence_before();
-        if (FUSED) mbar_arrive(&bars[kBarEpiDone]);
-        flush_rows();
+      } else if constexpr (D != 64) {
+        // unreachable: the host never cuts a unit of this head dimension
+        // between CTAs (its plan runs one CTA per unit)
+        return false;
       } else {
         // Cut unit: the schedule cuts a unit at most once, into two pieces
         // that may run in different CTAs.  Each query tile has its own
@@ -873,7 +949,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             stage16(16 * cc, v, inv_l);
           }
-          flush_rows();
+          flush_rows(0);
         };
         unsigned long long* counter = args.counters + 2 * static_cast<size_t>(sg.u) + wg;
         if (r == 0) {

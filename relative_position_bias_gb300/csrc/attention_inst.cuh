@@ -1,4 +1,6 @@
 // Definition of launch_attention<WP>; included by one .cu per padded width.
+// Each width instantiates the kernel for head_dim 64 and 128, fused or not,
+// bf16 or fp16 inputs.
 #pragma once
 #include <atomic>
 
@@ -7,12 +9,14 @@
 
 namespace dera {
 
-template <int WP>
-cudaError_t launch_attention(const AttnMaps& maps, const AttnArgs& args, int ctas, bool fused, cudaStream_t stream) {
+template <int WP, int D>
+cudaError_t launch_attention_d(const AttnMaps& maps, const AttnArgs& args, int ctas, bool fused,
+                               cudaStream_t stream) {
+  using SM = AttnSmem<D, KeyTile<WP, D>::BN>;
   const bool bf16 = args.in_fmt == kBF16;
-  auto kern = fused ? (bf16 ? relpos_attn_kernel<WP, true, true> : relpos_attn_kernel<WP, true, false>)
-                    : (bf16 ? relpos_attn_kernel<WP, false, true> : relpos_attn_kernel<WP, false, false>);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnSmem::kAlloc);
+  auto kern = fused ? (bf16 ? relpos_attn_kernel<WP, true, true, D> : relpos_attn_kernel<WP, true, false, D>)
+                    : (bf16 ? relpos_attn_kernel<WP, false, true, D> : relpos_attn_kernel<WP, false, false, D>);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
   if (e != cudaSuccess) return e;
   // The kernel's setmaxnreg split needs the block to launch with at least
   // kLaunchRegs registers per thread; a build that compiled to fewer is
@@ -27,8 +31,15 @@ cudaError_t launch_attention(const AttnMaps& maps, const AttnArgs& args, int cta
   }
   if (ok.load(std::memory_order_relaxed) < 0) return cudaErrorInvalidKernelImage;
   const unsigned grid = static_cast<unsigned>(ctas);
-  kern<<<grid, kAttnThreads, AttnSmem::kAlloc, stream>>>(maps.q, maps.k, maps.v, maps.th, maps.tw, args);
+  kern<<<grid, kAttnThreads, SM::kAlloc, stream>>>(maps.q, maps.k, maps.v, maps.th, maps.tw, args);
   return cudaGetLastError();
+}
+
+template <int WP>
+cudaError_t launch_attention(const AttnMaps& maps, const AttnArgs& args, int ctas, bool fused, int head_dim,
+                             cudaStream_t stream) {
+  return head_dim == 128 ? launch_attention_d<WP, 128>(maps, args, ctas, fused, stream)
+                         : launch_attention_d<WP, 64>(maps, args, ctas, fused, stream);
 }
 
 }  // namespace dera

@@ -2,5 +2,5 @@
 #include "attention_inst.cuh"
 
 namespace dera {
-template cudaError_t launch_attention<40>(const AttnMaps&, const AttnArgs&, int, bool, cudaStream_t);
+template cudaError_t launch_attention<40>(const AttnMaps&, const AttnArgs&, int, bool, int, cudaStream_t);
 }  // namespace dera

@@ -9,12 +9,12 @@
 
 namespace dera {
 
-constexpr int kHeadDim = 64;
 constexpr int kBlockM = 128;      // query rows per tile (one TMEM lane per row)
-constexpr int kRowBytes = 128;    // one 64-element 16-bit row
-constexpr int kTileBytes = 128 * kRowBytes;  // a 128-row operand tile (16 KB)
+constexpr int kRowBytes = 128;    // 64 16-bit elements: one swizzle atom of a row
+constexpr int kTileBytes = 128 * kRowBytes;  // one atom of a 128-row operand tile (16 KB)
 constexpr float kLog2e = 1.4426950408889634f;
-// One partial-result slot of a query tile: O as 16 column chunks of 4 floats,
+// One partial-result slot of a query tile (head_dim 64, the only one whose
+// units are cut between CTAs): O as 16 column chunks of 4 floats,
 // chunk-major ([16][128] float4, so a warp's 32 rows of one chunk are 512
 // contiguous bytes), then (m, l) per row ([128] float2).
 constexpr int kSlotFloats = 128 * 66;
@@ -22,14 +22,22 @@ constexpr int kSlotFloats = 128 * 66;
 // Key tiles cover KHT whole grid rows of WP (>= W) padded columns, so the
 // column of a key inside its tile fixes kw at compile time.  The padded
 // columns (kw >= W) and padded rows (kh >= H) are zero-filled by TMA and get
-// a -inf bias, which removes them from the softmax.
-template <int WP>
+// a -inf bias, which removes them from the softmax.  With head_dim 128 a key
+// tile holds about 64 keys (half as many grid rows), so that its K and V fit
+// the shared-memory ring and its S, P and O the TMEM budget.
+template <int WP, int D = 64>
 struct KeyTile {
-  static constexpr int KHT = WP <= 16 ? 8 : (WP <= 32 ? 4 : 2);
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  static constexpr int KHT = D == 64 ? (WP <= 16 ? 8 : (WP <= 32 ? 4 : 2)) : (WP <= 16 ? 4 : (WP <= 40 ? 2 : 1));
   static constexpr int BN = KHT * WP;
   static_assert(BN % 16 == 0 && BN <= 128, "tcgen05 N constraint");
   static_assert(WP % 2 == 0, "packed pairs must not straddle a grid row");
 };
+
+// Operand tiles of head dimension D are D / 64 swizzle atoms: an atom holds
+// 64 elements (128 bytes) of every row, and TMA loads each atom as one box.
+template <int D>
+constexpr int atoms_of() { return D / 64; }
 
 // Element types.
 enum : int { kF16 = 0, kBF16 = 1, kF32 = 2 };
@@ -37,7 +45,7 @@ enum : int { kF16 = 0, kBF16 = 1, kF32 = 2 };
 struct AttnArgs {
   const void* rel_h;   // [BH, N, H] (compact entry)
   const void* rel_w;   // [BH, N, W]
-  void* out;           // [BH, N, 64]
+  void* out;           // [BH, N, head_dim]
   int* status;         // device status word
   float* partials;     // [2 * gridDim.x][2][kSlotFloats] partial results (split units only)
   unsigned long long* counters;  // [n_units][2] arrival tags per unit and query tile (split units only)

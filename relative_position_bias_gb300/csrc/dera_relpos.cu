@@ -23,17 +23,24 @@ namespace dera {
 // Device status word: 0, or DERA_ERR_TIMEOUT once a bounded wait expired.
 __device__ int g_status_word = 0;
 
-cudaError_t launch_project(const CUtensorMap& q, const CUtensorMap& th, const CUtensorMap& tw,
-                           const ProjArgs& args, int in_fmt, int max_ctas, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(relpos_project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       ProjSmem::kAlloc);
+template <int D>
+cudaError_t launch_project_d(const CUtensorMap& q, const CUtensorMap& th, const CUtensorMap& tw,
+                             const ProjArgs& args, int in_fmt, int max_ctas, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(relpos_project_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       ProjSmem<D>::kAlloc);
   if (e != cudaSuccess) return e;
   const int n_qtiles = (args.N + kBlockM - 1) / kBlockM;
   // persistent: at most max_ctas CTAs (one per SM), each walking a strided list of tiles
   const unsigned tiles = static_cast<unsigned>(n_qtiles) * static_cast<unsigned>(args.BH);
   const unsigned grid = max_ctas > 0 ? std::min(tiles, static_cast<unsigned>(max_ctas)) : tiles;
-  relpos_project_kernel<<<grid, kProjThreads, ProjSmem::kAlloc, stream>>>(q, th, tw, args, in_fmt, n_qtiles);
+  relpos_project_kernel<D><<<grid, kProjThreads, ProjSmem<D>::kAlloc, stream>>>(q, th, tw, args, in_fmt, n_qtiles);
   return cudaGetLastError();
+}
+
+cudaError_t launch_project(const CUtensorMap& q, const CUtensorMap& th, const CUtensorMap& tw,
+                           const ProjArgs& args, int in_fmt, int head_dim, int max_ctas, cudaStream_t stream) {
+  return head_dim == 128 ? launch_project_d<128>(q, th, tw, args, in_fmt, max_ctas, stream)
+                         : launch_project_d<64>(q, th, tw, args, in_fmt, max_ctas, stream);
 }
 
 // One thread waits on an mbarrier that nothing arrives on; the bounded wait
@@ -93,7 +100,7 @@ bool is_float(dera_dtype t) { return t == DERA_F16 || t == DERA_BF16 || t == DER
 int fmt_of(dera_dtype t) { return t == DERA_F16 ? kF16 : (t == DERA_BF16 ? kBF16 : kF32); }
 
 dera_status check_shape(int BH, int H, int W, int head_dim) {
-  if (head_dim != kHeadDim) return DERA_ERR_HEAD_DIM;
+  if (head_dim != 64 && head_dim != 128) return DERA_ERR_HEAD_DIM;
   if (BH < 0 || H < 1 || W < 1 || H > 64 || W > 64) return DERA_ERR_SHAPE;
   // grid size: ceil(N/256) CTAs per head must fit 2^31 - 1 in total
   const long long pairs = (static_cast<long long>(H) * W + 255) / 256;
@@ -137,33 +144,42 @@ CUtensorMapDataType tma_type(dera_dtype t) {
   return t == DERA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 }
 
-// q / out-like tensor [BH, N, 64] read in 128-row tiles
-bool map_rows(CUtensorMap* m, const void* p, dera_dtype t, int BH, int N) {
-  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
-  const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(N) * 128};
+// Every box is 64 elements (128 bytes, one swizzle atom) wide; a row of
+// head_dim d is d / 64 boxes, loaded at element offsets 0 and 64.
+
+// q / out-like tensor [BH, N, d] read in 128-row tiles
+bool map_rows(CUtensorMap* m, const void* p, dera_dtype t, int BH, int N, int d) {
+  const cuuint64_t row = 2 * static_cast<cuuint64_t>(d);
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {row, static_cast<cuuint64_t>(N) * row};
   const cuuint32_t box[3] = {64, 128, 1};
   return make_map(m, p, tma_type(t), 3, dims, strides, box);
 }
 
-// k / v viewed as [BH, H, W, 64], read in tiles of KHT grid rows x WP columns
-bool map_keys(CUtensorMap* m, const void* p, dera_dtype t, int BH, int H, int W, int WP, int KHT) {
-  const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(W), static_cast<cuuint64_t>(H),
+// k / v viewed as [BH, H, W, d], read in tiles of KHT grid rows x WP columns
+bool map_keys(CUtensorMap* m, const void* p, dera_dtype t, int BH, int H, int W, int d, int WP, int KHT) {
+  const cuuint64_t row = 2 * static_cast<cuuint64_t>(d);
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(W), static_cast<cuuint64_t>(H),
                               static_cast<cuuint64_t>(BH)};
-  const cuuint64_t strides[3] = {128, static_cast<cuuint64_t>(W) * 128, static_cast<cuuint64_t>(H) * W * 128};
+  const cuuint64_t strides[3] = {row, static_cast<cuuint64_t>(W) * row, static_cast<cuuint64_t>(H) * W * row};
   const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(WP), static_cast<cuuint32_t>(KHT), 1};
   return make_map(m, p, tma_type(t), 4, dims, strides, box);
 }
 
-// table [2L-1, 64], one 128-row box (rows past 2L-1 read as zero)
-bool map_table(CUtensorMap* m, const void* p, dera_dtype t, int L) {
-  const cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(2 * L - 1)};
-  const cuuint64_t strides[1] = {128};
+// table [2L-1, d], one 128-row box per 64 columns (rows past 2L-1 read as zero)
+bool map_table(CUtensorMap* m, const void* p, dera_dtype t, int L, int d) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(2 * L - 1)};
+  const cuuint64_t strides[1] = {2 * static_cast<cuuint64_t>(d)};
   const cuuint32_t box[2] = {64, 128};
   return make_map(m, p, tma_type(t), 2, dims, strides, box);
 }
 
 int padded_width(int W) { return W <= 16 ? 16 : (W <= 32 ? 32 : (W <= 40 ? 40 : 64)); }
-int rows_per_tile(int WP) { return WP <= 16 ? 8 : (WP <= 32 ? 4 : 2); }
+// grid rows per key tile (KeyTile<WP, d>::KHT)
+int rows_per_tile(int WP, int d) {
+  if (d == 64) return WP <= 16 ? 8 : (WP <= 32 ? 4 : 2);
+  return WP <= 16 ? 4 : (WP <= 40 ? 2 : 1);
+}
 
 // Streaming-multiprocessor count of a device (cached; 0 if the query fails).
 int sm_count(int dev) {
@@ -210,10 +226,10 @@ struct Plan {
   size_t counters_bytes, partial_bytes;
 };
 
-Plan make_plan(int BH, int H, int W, int sms) {
+Plan make_plan(int BH, int H, int W, int d, int sms) {
   Plan p;
   const int N = H * W;
-  const int KHT = rows_per_tile(padded_width(W));
+  const int KHT = rows_per_tile(padded_width(W), d);
   p.n_qtiles = (N + kBlockM - 1) / kBlockM;
   p.n_pairs = (p.n_qtiles + 1) / 2;
   p.n_units = BH * p.n_pairs;
@@ -224,7 +240,9 @@ Plan make_plan(int BH, int H, int W, int sms) {
   // kMinSplitKeyTiles key tiles (small grids such as 14x14 windows) are not
   // split: the merge of a cut unit costs more than the imbalance it removes
   // (measured on 25 windows x 12 heads of 14x14: 28 us whole, 32 us split).
-  p.split = sms > 0 && p.n_kv >= kMinSplitKeyTiles && p.n_units > sms && p.n_units % sms != 0;
+  // The merge of cut units is built for head_dim 64 only; head_dim 128 runs
+  // one CTA per unit.
+  p.split = d == 64 && sms > 0 && p.n_kv >= kMinSplitKeyTiles && p.n_units > sms && p.n_units % sms != 0;
   p.ctas = p.split ? sms : p.n_units;
   p.counters_bytes = align256(static_cast<size_t>(p.n_units) * 2 * sizeof(unsigned long long));  // one per query tile
   p.partial_bytes = static_cast<size_t>(2) * sms * 2 * kSlotFloats * sizeof(float);
@@ -247,24 +265,24 @@ dera_status current_device(int* dev) {
   } while (0)
 
 dera_status run_attention(const void* q, const void* k, const void* v, const void* a, const void* b, void* out,
-                          int BH, int H, int W, float scale, dera_dtype in_dtype, dera_dtype bias_dtype,
+                          int BH, int H, int W, int d, float scale, dera_dtype in_dtype, dera_dtype bias_dtype,
                           dera_dtype out_dtype, bool fused, void* workspace, size_t workspace_bytes,
                           void* stream) {
   int dev = 0;
   DERA_TRY(current_device(&dev));
   const int N = H * W;
-  Plan plan = make_plan(BH, H, W, sm_count(dev));
+  Plan plan = make_plan(BH, H, W, d, sm_count(dev));
   if (plan.split && (workspace == nullptr || workspace_bytes < workspace_bytes_for(plan))) {
     plan.split = false;  // no (or too small a) workspace: one CTA per unit
     plan.ctas = plan.n_units;
   }
-  const int WP = padded_width(W), KHT = rows_per_tile(WP);
+  const int WP = padded_width(W), KHT = rows_per_tile(WP, d);
   AttnMaps maps;
-  if (!map_rows(&maps.q, q, in_dtype, BH, N) || !map_keys(&maps.k, k, in_dtype, BH, H, W, WP, KHT) ||
-      !map_keys(&maps.v, v, in_dtype, BH, H, W, WP, KHT))
+  if (!map_rows(&maps.q, q, in_dtype, BH, N, d) || !map_keys(&maps.k, k, in_dtype, BH, H, W, d, WP, KHT) ||
+      !map_keys(&maps.v, v, in_dtype, BH, H, W, d, WP, KHT))
     return DERA_ERR_CUDA;
   if (fused) {
-    if (!map_table(&maps.th, a, in_dtype, H) || !map_table(&maps.tw, b, in_dtype, W)) return DERA_ERR_CUDA;
+    if (!map_table(&maps.th, a, in_dtype, H, d) || !map_table(&maps.tw, b, in_dtype, W, d)) return DERA_ERR_CUDA;
   } else {
     maps.th = maps.q;  // unused by the compact-bias kernel
     maps.tw = maps.q;
@@ -298,10 +316,10 @@ dera_status run_attention(const void* q, const void* k, const void* v, const voi
   }
   cudaError_t e;
   switch (WP) {
-    case 16: e = launch_attention<16>(maps, args, plan.ctas, fused, s); break;
-    case 32: e = launch_attention<32>(maps, args, plan.ctas, fused, s); break;
-    case 40: e = launch_attention<40>(maps, args, plan.ctas, fused, s); break;
-    default: e = launch_attention<64>(maps, args, plan.ctas, fused, s); break;
+    case 16: e = launch_attention<16>(maps, args, plan.ctas, fused, d, s); break;
+    case 32: e = launch_attention<32>(maps, args, plan.ctas, fused, d, s); break;
+    case 40: e = launch_attention<40>(maps, args, plan.ctas, fused, d, s); break;
+    default: e = launch_attention<64>(maps, args, plan.ctas, fused, d, s); break;
   }
   return e == cudaSuccess ? DERA_OK : DERA_ERR_CUDA;
 }
@@ -338,7 +356,7 @@ const char* dera_status_string(dera_status status) {
     case DERA_ERR_NULL: return "DERA_ERR_NULL: a required pointer is NULL";
     case DERA_ERR_SHAPE: return "DERA_ERR_SHAPE: H, W or BH out of range";
     case DERA_ERR_DTYPE: return "DERA_ERR_DTYPE: unsupported dtype for this argument";
-    case DERA_ERR_HEAD_DIM: return "DERA_ERR_HEAD_DIM: head_dim must be 64";
+    case DERA_ERR_HEAD_DIM: return "DERA_ERR_HEAD_DIM: head_dim must be 64 or 128";
     case DERA_ERR_ALIGN: return "DERA_ERR_ALIGN: pointer not 16-byte aligned";
     case DERA_ERR_DEVICE: return "DERA_ERR_DEVICE: pointer is not device memory of the current device";
     case DERA_ERR_TIMEOUT: return "DERA_ERR_TIMEOUT: a bounded wait expired inside a kernel";
@@ -363,8 +381,8 @@ dera_status dera_relpos_project(const void* q, const void* rel_pos_h, const void
     DERA_TRY(check_ptr(p, dev));
   const int N = H * W;
   CUtensorMap mq, mh, mw;
-  if (!map_rows(&mq, q, in_dtype, BH, N) || !map_table(&mh, rel_pos_h, in_dtype, H) ||
-      !map_table(&mw, rel_pos_w, in_dtype, W))
+  if (!map_rows(&mq, q, in_dtype, BH, N, head_dim) || !map_table(&mh, rel_pos_h, in_dtype, H, head_dim) ||
+      !map_table(&mw, rel_pos_w, in_dtype, W, head_dim))
     return DERA_ERR_CUDA;
   ProjArgs args;
   args.rel_h = rel_h;
@@ -377,7 +395,7 @@ dera_status dera_relpos_project(const void* q, const void* rel_pos_h, const void
   args.N = N;
   args.bias_fmt = fmt_of(bias_dtype);
   const cudaError_t e =
-      launch_project(mq, mh, mw, args, fmt_of(in_dtype), sm_count(dev), static_cast<cudaStream_t>(stream));
+      launch_project(mq, mh, mw, args, fmt_of(in_dtype), head_dim, sm_count(dev), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DERA_OK : DERA_ERR_CUDA;
 }
 
@@ -388,7 +406,7 @@ dera_status dera_relpos_workspace_size(int BH, int H, int W, int head_dim, size_
   if (BH == 0) return DERA_OK;
   int dev = 0;
   DERA_TRY(current_device(&dev));
-  *bytes = workspace_bytes_for(make_plan(BH, H, W, sm_count(dev)));
+  *bytes = workspace_bytes_for(make_plan(BH, H, W, head_dim, sm_count(dev)));
   return DERA_OK;
 }
 
@@ -408,7 +426,7 @@ dera_status dera_relpos_attention(const void* q, const void* k, const void* v, c
     if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return DERA_ERR_ALIGN;
     DERA_TRY(check_ptr(workspace, dev));
   }
-  return run_attention(q, k, v, rel_h, rel_w, out, BH, H, W, scale, in_dtype, bias_dtype, out_dtype, false,
+  return run_attention(q, k, v, rel_h, rel_w, out, BH, H, W, head_dim, scale, in_dtype, bias_dtype, out_dtype, false,
                        workspace, workspace_bytes, stream);
 }
 
@@ -428,7 +446,7 @@ dera_status dera_relpos_fused(const void* q, const void* k, const void* v, const
     if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return DERA_ERR_ALIGN;
     DERA_TRY(check_ptr(workspace, dev));
   }
-  return run_attention(q, k, v, rel_pos_h, rel_pos_w, out, BH, H, W, scale, in_dtype, in_dtype, out_dtype, true,
+  return run_attention(q, k, v, rel_pos_h, rel_pos_w, out, BH, H, W, head_dim, scale, in_dtype, in_dtype, out_dtype, true,
                        workspace, workspace_bytes, stream);
 }
 
@@ -468,7 +486,7 @@ dera_status dera_relpos_fused_noalloc(const void* q, const void* k, const void* 
   // cannot be read is refused (that count sizes the schedule and its scratch).
   const int sms = sm_count(dev);
   if (sms <= 0) return DERA_ERR_CUDA;
-  const size_t need = workspace_bytes_for(make_plan(BH, H, W, sms));
+  const size_t need = workspace_bytes_for(make_plan(BH, H, W, head_dim, sms));
   if (need > DERA_NOALLOC_SCRATCH_BYTES) return DERA_ERR_SCRATCH;
   for (const void* p : {q, k, v, rel_pos_h, rel_pos_w, static_cast<const void*>(out)})
     DERA_TRY(check_ptr(p, dev));
@@ -477,7 +495,7 @@ dera_status dera_relpos_fused_noalloc(const void* q, const void* k, const void* 
     scratch = noalloc_scratch(dev);
     if (!scratch) return DERA_ERR_CUDA;
   }
-  return run_attention(q, k, v, rel_pos_h, rel_pos_w, out, BH, H, W, scale, in_dtype, in_dtype, out_dtype, true,
+  return run_attention(q, k, v, rel_pos_h, rel_pos_w, out, BH, H, W, head_dim, scale, in_dtype, in_dtype, out_dtype, true,
                        scratch, need, stream);
 }
 

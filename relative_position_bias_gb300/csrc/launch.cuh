@@ -13,10 +13,11 @@ struct AttnMaps {
 };
 
 template <int WP>
-cudaError_t launch_attention(const AttnMaps& maps, const AttnArgs& args, int ctas, bool fused, cudaStream_t stream);
+cudaError_t launch_attention(const AttnMaps& maps, const AttnArgs& args, int ctas, bool fused, int head_dim,
+                             cudaStream_t stream);
 
 cudaError_t launch_project(const CUtensorMap& q, const CUtensorMap& th, const CUtensorMap& tw,
-                           const ProjArgs& args, int in_fmt, int max_ctas, cudaStream_t stream);
+                           const ProjArgs& args, int in_fmt, int head_dim, int max_ctas, cudaStream_t stream);
 
 cudaError_t launch_wait_selftest(int* status, long long budget, cudaStream_t stream);
 

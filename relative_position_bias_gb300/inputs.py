@@ -6,9 +6,11 @@ arithmetic, so both the CUDA path and the CPU oracle can be fed from it.
 Workloads follow the DeepEncoder global-attention setting described on the
 vLLM PR #55629 page (section "功能与动机", motivation: 64x64 global attention,
 BF16) plus a small grid, a batched encoder, a ragged 40x40 grid, a wider
-16-head encoder, and the same encoder's windowed blocks (section 实现拆解
-item 3 keeps them on SDPA): the 64x64 grid padded to 70x70 and cut into 25
-windows of 14x14, each window an independent attention problem.  Each tensor is drawn as fp32 ``sigma * randn`` from one CPU
+16-head encoder, the same encoder's windowed blocks (section 实现拆解 item 3
+keeps them on SDPA): the 64x64 grid padded to 70x70 and cut into 25 windows
+of 14x14, each window an independent attention problem, and the 64x64
+encoder with head_dim 128 (section 风险与影响 names BLOCK_D = 64 as the
+kernel's limit).  Each tensor is drawn as fp32 ``sigma * randn`` from one CPU
 generator in the fixed order q, k, v, rel_pos_h, rel_pos_w and then
 rounded-to-nearest to the workload dtype; the same rounded values go to the
 GPU and to the oracle.
@@ -56,8 +58,8 @@ class Workload:
                        name=f"{self.name}-{H}x{W}")
 
 
-# The workloads.  scale = 64**-0.5 = 1/8 everywhere (the SDPA default for
-# head_dim 64); sigma is a standard deviation.
+# The workloads.  scale = head_dim**-0.5 (the SDPA default): 1/8 for head_dim
+# 64; sigma is a standard deviation.
 WORKLOADS: dict[str, Workload] = {
     "grid16": Workload("grid16", B=1, heads=2, H=16, W=16),
     "global64": Workload("global64", B=1, heads=12, H=64, W=64),
@@ -66,6 +68,8 @@ WORKLOADS: dict[str, Workload] = {
                          sigma_v=1.0, sigma_table=1.0),
     "wide64": Workload("wide64", B=4, heads=16, H=64, W=64, entry="fused"),
     "window14": Workload("window14", B=1, heads=12, H=14, W=14, windows=25, entry="fused"),
+    # the same 64x64 encoder with head_dim 128 (the pages' kernel fixes BLOCK_D = 64)
+    "global64d128": Workload("global64d128", B=1, heads=12, H=64, W=64, d=128, scale=128 ** -0.5, entry="fused"),
 }
 
 

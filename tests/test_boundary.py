@@ -62,7 +62,8 @@ def _proj(lib, *, ptrs=(FAKE,) * 5, BH=1, H=4, W=4, d=64, in_dt=1, bias_dt=2):
 
 @pytest.mark.parametrize("call", [_fused, _attn, _proj])
 def test_host_validation(lib, call):
-    assert call(lib, d=128) == 4                      # head_dim
+    assert call(lib, d=256) == 4                      # head_dim: 64 or 128
+    assert call(lib, d=32) == 4
     assert call(lib, d=63) == 4
     assert call(lib, H=0) == 2                        # shape
     assert call(lib, W=65) == 2

@@ -19,6 +19,8 @@ from __future__ import annotations
 import re
 from pathlib import Path
 
+from dataclasses import replace
+
 import numpy as np
 import pytest
 import torch
@@ -86,16 +88,18 @@ def query_tiles_per_unit() -> int:
 
 def default_plan(w: I.Workload) -> tuple[bool, int, int]:
     """(split, units, units per head) of the default (workspace) schedule, restated from the host
-    plan: units are groups of query tiles of one head; the work is split when the units do not
-    fill whole waves of one CTA per SM and a unit spans at least 4 key tiles (128 keys each:
-    whole grid rows of the padded width 16, 32, 40 or 64)."""
+    plan: units are groups of query tiles of one head; with head_dim 64 the work is split when
+    the units do not fill whole waves of one CTA per SM and a unit spans at least 4 key tiles
+    (whole grid rows of the padded width 16, 32, 40 or 64 per tile)."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     per = query_tiles_per_unit()
     units_per_head = (-(-w.N // 128) + per - 1) // per
     U = w.BH * units_per_head
     wp = next(x for x in (16, 32, 40, 64) if x >= w.W)
-    n_kv = -(-w.H // {16: 8, 32: 4, 40: 2, 64: 2}[wp])
-    return (n_kv >= 4 and U > sms and U % sms != 0), U, units_per_head
+    kht = {16: 8, 32: 4, 40: 2, 64: 2}[wp] if w.d == 64 else {16: 4, 32: 2, 40: 2, 64: 1}[wp]
+    n_kv = -(-w.H // kht)
+    # only head_dim 64 cuts units between CTAs
+    return (w.d == 64 and n_kv >= 4 and U > sms and U % sms != 0), U, units_per_head
 
 
 def tail_heads(w: I.Workload) -> set[int]:
@@ -240,7 +244,7 @@ def test_split_schedule_ragged(entry, BH):
     units = {None: sms + 1, 1: sms + sms // 2, 2: 2 * sms + 1, 3: 3 * sms - 1}[BH]
     heads = -(-units // per_head)
     w = I.WORKLOADS["ragged40"].with_grid(40, 40, B=1, heads=heads)
-    assert rpb.workspace_size(w.BH, w.H, w.W) > 0
+    assert rpb.workspace_size(w.BH, w.H, w.W, w.d) > 0
     x = I.make_inputs(w, seed=heads)
     d = _dev(x)
     f = _f64(x)
@@ -269,7 +273,7 @@ def test_workspace_size_formula(name):
     per = query_tiles_per_unit()
     split, units, _ = default_plan(w)
     want = ((8 * per * units + 255) // 256 * 256 + 2 * sms * per * 128 * 66 * 4) if split else 0
-    assert rpb.workspace_size(w.BH, w.H, w.W) == want
+    assert rpb.workspace_size(w.BH, w.H, w.W, w.d) == want
 
 
 def test_caller_workspace_and_reuse():
@@ -278,7 +282,7 @@ def test_caller_workspace_and_reuse():
     d = _dev(I.make_inputs(w))
     args = (d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W, w.scale)
     ref = rpb.fused(*args)
-    ws = torch.empty(rpb.workspace_size(w.BH, w.H, w.W), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(rpb.workspace_size(w.BH, w.H, w.W, w.d), dtype=torch.uint8, device="cuda")
     for _ in range(3):
         again = rpb.fused(*args, workspace=ws)
         torch.cuda.synchronize()
@@ -295,7 +299,7 @@ def test_default_workspace_per_stream():
     """Calls on two streams that overlap on the GPU each get their own cached scratch, so both
     match a serial call bit for bit."""
     w = I.WORKLOADS["global64"]
-    assert rpb.workspace_size(w.BH, w.H, w.W) > 0, "this workload must use the split schedule"
+    assert rpb.workspace_size(w.BH, w.H, w.W, w.d) > 0, "this workload must use the split schedule"
     d = _dev(I.make_inputs(w))
     d2 = _dev(I.make_inputs(w, seed=1))
     ref1 = rpb.fused(d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W, w.scale)
@@ -321,7 +325,7 @@ def test_workspace_contents_are_ignored(name, entry):
     full of arbitrary bytes (never cleared) gives the same result as the
     library's own workspace, call after call."""
     w = I.WORKLOADS[name]
-    assert rpb.workspace_size(w.BH, w.H, w.W) > 0, "this workload must use the split schedule"
+    assert rpb.workspace_size(w.BH, w.H, w.W, w.d) > 0, "this workload must use the split schedule"
     d = _dev(I.make_inputs(w))
     if entry == "fused":
         args = (d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W, w.scale)
@@ -331,7 +335,7 @@ def test_workspace_contents_are_ignored(name, entry):
         args = (d["q"], d["k"], d["v"], rh, rw, w.H, w.W, w.scale)
         call = rpb.attention
     ref = call(*args)
-    ws = torch.empty(rpb.workspace_size(w.BH, w.H, w.W), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(rpb.workspace_size(w.BH, w.H, w.W, w.d), dtype=torch.uint8, device="cuda")
     g = torch.Generator(device="cuda").manual_seed(11)
     for trial in range(4):
         if trial < 3:
@@ -410,6 +414,34 @@ def test_edge_grids(grid, dtype):
     want = oracle.fused(f["q"], f["k"], f["v"], f["rel_pos_h"], f["rel_pos_w"], H, W, w.scale)
     check_out(o32, want, what=f"fused {H}x{W} {dtype}")
     check_out(a32, want, what=f"two-step {H}x{W} {dtype}")
+
+
+EDGE_GRIDS_D128 = [(1, 1), (3, 5), (17, 13), (64, 1), (7, 40), (33, 33), (20, 48), (2, 16), (40, 40), (64, 33),
+                   (11, 37), (64, 64)]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("grid", EDGE_GRIDS_D128, ids=lambda g: f"{g[0]}x{g[1]}")
+def test_edge_grids_head_dim_128(grid, dtype):
+    """head_dim 128 on every padded width (16, 32, 40, 64: key tiles of 4, 2, 2 and 1 grid rows),
+    ragged tails and single rows or columns, fused and two-step, against the oracle."""
+    H, W = grid
+    base = I.WORKLOADS["ragged40"] if dtype == "f16" else I.WORKLOADS["global64d128"]
+    w = replace(base.with_grid(H, W, B=1, heads=3), d=128, scale=128 ** -0.5)
+    x = I.make_inputs(w, seed=H * 89 + W)
+    d = _dev(x)
+    f = _f64(x)
+    o32 = rpb.fused(d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], H, W, w.scale, out_dtype=torch.float32)
+    o16 = rpb.fused(d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], H, W, w.scale)
+    rh, rw = rpb.project(d["q"], d["rel_pos_h"], d["rel_pos_w"], H, W)
+    a32 = rpb.attention(d["q"], d["k"], d["v"], rh, rw, H, W, w.scale, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    want_h, want_w = oracle.project(f["q"], f["rel_pos_h"], f["rel_pos_w"], H, W)
+    assert np.abs(rh.double().cpu().numpy() - want_h).max() <= 2e-4 * (1 + np.abs(want_h).max())
+    assert np.abs(rw.double().cpu().numpy() - want_w).max() <= 2e-4 * (1 + np.abs(want_w).max())
+    want = oracle.fused(f["q"], f["k"], f["v"], f["rel_pos_h"], f["rel_pos_w"], H, W, w.scale)
+    check_out(o32, want, o16, what=f"fused d128 {H}x{W} {dtype}")
+    check_out(a32, want, what=f"two-step d128 {H}x{W} {dtype}")
 
 
 def test_empty_batch_is_a_noop():
