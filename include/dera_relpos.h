@@ -140,10 +140,10 @@ DERA_API dera_status dera_relpos_fused(const void* q, const void* k, const void*
  * cutting (no scratch used).
  *
  * Scheduling (no counterpart on the pages, which give no kernel schedule):
- * the work unit is a pair of 128-row query tiles of one head.  When
- * head_dim is 64, the number of units is not a whole number of waves of one
- * CTA per SM and a unit spans at least 4 key tiles (grids of at least 4 x 16
- * or so), the kernel runs one persistent CTA per SM over equal shares of the
+ * the work unit is a pair of 128-row query tiles of one head.  When the
+ * number of units is not a whole number of waves of one CTA per SM and a
+ * unit spans at least 4 key tiles (grids of at least 4 x 16 or so), the
+ * kernel runs one persistent CTA per SM over equal shares of the
  * (unit, key tile) iteration space and cuts some units between two CTAs; the
  * partial results (unnormalised O, row max, row sum, fp32) and two 8-byte
  * arrival counters per unit (one per query tile) live in the caller's
@@ -171,7 +171,7 @@ DERA_API dera_status dera_relpos_workspace_size(int BH, int H, int W, int head_d
  * This entry point computes exactly what dera_relpos_fused computes (same
  * arguments minus the workspace) and takes its scratch from a buffer
  * compiled into the library: a file-scope device array of
- * DERA_NOALLOC_SCRATCH_BYTES (24 MiB) that every GPU which loads the library
+ * DERA_NOALLOC_SCRATCH_BYTES (48 MiB) that every GPU which loads the library
  * holds until the process exits.  It calls no cudaMalloc/cudaFree and no
  * allocating library routine.
  *   - Set-up: the first call on each device looks up the device address of
@@ -180,9 +180,10 @@ DERA_API dera_status dera_relpos_workspace_size(int BH, int H, int W, int head_d
  *   - Limit: problems whose split schedule needs more scratch than the
  *     buffer holds are rejected with DERA_ERR_SCRATCH before anything is
  *     enqueued.  The need is what dera_relpos_workspace_size reports: on a
- *     152-SM GB300, 20 545 536 bytes of partial-result slots plus 16 bytes per
- *     work unit (a pair of 128-row query tiles of one head), so problems of
- *     up to about 288 000 units fit.  Problems that need no scratch always run.
+ *     152-SM GB300, 20 545 536 bytes of partial-result slots (40 468 480 with
+ *     head_dim 128) plus 16 bytes per work unit (a pair of 128-row query
+ *     tiles of one head), so problems of up to about 1.8 million units (600 000
+ *     with head_dim 128) fit.  Problems that need no scratch always run.
  *   - Sharing: every call on a device uses the same buffer and leaves its
  *     contents behind; like a caller's workspace, the buffer needs no
  *     clearing between calls (see dera_relpos_workspace_size).  Calls that overlap on
@@ -190,7 +191,7 @@ DERA_API dera_status dera_relpos_workspace_size(int BH, int H, int W, int head_d
  *     results: serialise them.
  * Other arguments, layouts and errors: as dera_relpos_fused.
  */
-#define DERA_NOALLOC_SCRATCH_BYTES (24u * 1024u * 1024u)
+#define DERA_NOALLOC_SCRATCH_BYTES (48u * 1024u * 1024u)
 DERA_API dera_status dera_relpos_fused_noalloc(const void* q, const void* k, const void* v, const void* rel_pos_h,
                                                const void* rel_pos_w, void* out, int BH, int H, int W,
                                                int head_dim, float scale, dera_dtype in_dtype, dera_dtype out_dtype,

@@ -19,7 +19,7 @@
 //
 // Warp roles (384 threads; warps 0-3 run with 104 registers, the softmax
 // warpgroups with 200, set by setmaxnreg):
-//   warp 0      TMA producer: Q pair, [tables,] K/V ring (3 stages)
+//   warp 0      TMA producer: Q pair, [tables,] K/V ring (2 to 4 stages)
 //   warp 1      tcgen05.mma issuer (the warp walks the loop, an elected lane issues)
 //   warp 2      TMEM allocator; with warp 3, converts bf16 V tiles to fp16
 //   warps 4-7   softmax / epilogue of query tile 0 (one thread per row)
@@ -36,7 +36,7 @@
 
 namespace dera {
 
-constexpr int kMaxStages = 3;     // K/V ring depth (head_dim 64; 2 for head_dim 128)
+constexpr int kMaxStages = 4;     // deepest K/V ring (head_dim 64)
 constexpr int kTilesPerUnit = 2;  // 128-row query tiles per work unit
 constexpr int kAttnThreads = 384;
 // Largest accepted row sum of a speculative tile: with the sum at most this,
@@ -72,11 +72,13 @@ struct AttnDims {
   // for head_dim 64; 64 or 80 x 256 B for head_dim 128)
   static constexpr int kKVBytes = D == 64 ? kTileBytes : BN * 2 * D;
   static constexpr int kStageBytes = 2 * kKVBytes;
-  // K/V ring depth: three stages, except for head_dim 128 with 80-key tiles,
-  // where three do not fit beside the query tiles and the bias areas
-  static constexpr int kStages = kStageBytes <= 32 * 1024 ? 3 : 2;
-  // floats per row of a bias staging area (65 where a third stage has to fit)
-  static constexpr int kBiasStride = D == 64 ? 66 : 65;
+  // K/V ring depth, as deep as shared memory allows beside the query tiles and
+  // the bias areas: 4 stages for head_dim 64, 3 for head_dim 128 with 64-key
+  // tiles, 2 with 80-key tiles
+  static constexpr int kStages = D == 64 ? 4 : (kStageBytes <= 32 * 1024 ? 3 : 2);
+  // floats per row of a bias staging area (an odd stride: a warp's staged
+  // rows start in different banks)
+  static constexpr int kBiasStride = 65;
   // ring stages the fused prologue's tables take: [T_h | T_w] in one stage,
   // or T_h and T_w (32 KB each) in one stage apiece
   static constexpr int kTableSlots = D == 64 ? 1 : 2;
@@ -900,10 +902,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
           flush_rows(h);
         }
-      } else if constexpr (D != 64) {
-        // unreachable: the host never cuts a unit of this head dimension
-        // between CTAs (its plan runs one CTA per unit)
-        return false;
       } else {
         // Cut unit: the schedule cuts a unit at most once, into two pieces
         // that may run in different CTAs.  Each query tile has its own
@@ -918,7 +916,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         //    never need clearing.
         // Both merges combine the pieces in the same order (the unit's first
         // piece, then its second) from the same fp32 values, so the result
-        // does not depend on which path ran.
+        // does not depend on which path ran.  O is merged and stored 64
+        // columns at a time.
         const int c = blockIdx.x;
         const int slot = (sg.tail == 0) ? 2 * c : 2 * c + 1;
         const long long u0 = static_cast<long long>(sg.u) * n_kv;
@@ -927,12 +926,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int sl1 = 2 * (c_first + 1);
         // a slot of this query tile; this thread's row is O chunk q at
         // float4 index q * 128 + r, and (m, l) at float2 index r after the
-        // 64 * 128 floats of O
-        auto slot_of = [&](int s_) { return args.partials + (static_cast<size_t>(s_) * 2 + wg) * kSlotFloats; };
+        // D * 128 floats of O
+        auto slot_of = [&](int s_) { return args.partials + (static_cast<size_t>(s_) * 2 + wg) * slot_floats<D>(); };
         auto ld_chunk = [&](const float* sl, int q) { return __ldcg(reinterpret_cast<const float4*>(sl) + q * kBlockM + r); };
-        auto ld_ml = [&](const float* sl) { return __ldcg(reinterpret_cast<const float2*>(sl + 64 * kBlockM) + r); };
-        // out = (fa O_a + fb O_b) / (fa l_a + fb l_b), rescaled to the larger running max
-        auto merge_store = [&](const float4 (&xa)[16], float2 ma, const float4 (&xb)[16], float2 mb) {
+        auto ld_ml = [&](const float* sl) { return __ldcg(reinterpret_cast<const float2*>(sl + D * kBlockM) + r); };
+        // columns [64h, 64h + 64) of out = (fa O_a + fb O_b) / (fa l_a + fb l_b),
+        // rescaled to the larger running max
+        auto merge_store = [&](int h, const float4 (&xa)[16], float2 ma, const float4 (&xb)[16], float2 mb) {
           const float mstar = fmaxf(ma.x, mb.x);
           const float fa = ex2_approx(ma.x - mstar), fb = ex2_approx(mb.x - mstar);
           const float inv_l = 1.0f / (fa * ma.y + fb * mb.y);
@@ -949,7 +949,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             stage16(16 * cc, v, inv_l);
           }
-          flush_rows(0);
+          flush_rows(h);
         };
         unsigned long long* counter = args.counters + 2 * static_cast<size_t>(sg.u) + wg;
         if (r == 0) {
@@ -961,31 +961,36 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (!ok) return false;
         if (merge_flag[wg]) {
           const float* po = slot_of(slot == sl0 ? sl1 : sl0);
-          float4 xo[16];
-          #pragma unroll
-          for (int q = 0; q < 16; ++q) xo[q] = ld_chunk(po, q);
-          const float2 mo = ld_ml(po);
-          uint32_t oa[64];
-          tmem_ld32(tO, *reinterpret_cast<uint32_t(*)[32]>(&oa[0]));
-          tmem_ld32(tO + 32, *reinterpret_cast<uint32_t(*)[32]>(&oa[32]));
-          tmem_wait_ld();
-          tc_fence_before();
-          if (FUSED) mbar_arrive(&bars[kBarEpiDone]);
-          const bool first = slot == sl0;  // warp-uniform
-          float4 xa[16], xb[16];
-          #pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            const float4 own = make_float4(__uint_as_float(oa[4 * q]), __uint_as_float(oa[4 * q + 1]),
-                                           __uint_as_float(oa[4 * q + 2]), __uint_as_float(oa[4 * q + 3]));
-            xa[q] = first ? own : xo[q];
-            xb[q] = first ? xo[q] : own;
+          #pragma unroll 1
+          for (int h = 0; h < Dm::kAtoms; ++h) {
+            float4 xo[16];
+            #pragma unroll
+            for (int q = 0; q < 16; ++q) xo[q] = ld_chunk(po, 16 * h + q);
+            const float2 mo = ld_ml(po);
+            uint32_t oa[64];
+            tmem_ld32(tO + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&oa[0]));
+            tmem_ld32(tO + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&oa[32]));
+            tmem_wait_ld();
+            if (h == Dm::kAtoms - 1) {
+              tc_fence_before();
+              if (FUSED) mbar_arrive(&bars[kBarEpiDone]);
+            }
+            const bool first = slot == sl0;  // warp-uniform
+            float4 xa[16], xb[16];
+            #pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              const float4 own = make_float4(__uint_as_float(oa[4 * q]), __uint_as_float(oa[4 * q + 1]),
+                                             __uint_as_float(oa[4 * q + 2]), __uint_as_float(oa[4 * q + 3]));
+              xa[q] = first ? own : xo[q];
+              xb[q] = first ? xo[q] : own;
+            }
+            const float2 mown = make_float2(m_used, l);
+            merge_store(h, xa, first ? mown : mo, xb, first ? mo : mown);
           }
-          const float2 mown = make_float2(m_used, l);
-          merge_store(xa, first ? mown : mo, xb, first ? mo : mown);
         } else {
           float* ws = slot_of(slot);
           #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
+          for (int cc = 0; cc < D / 16; ++cc) {
             uint32_t u[16];
             tmem_ld16(tO + 16 * cc, u);
             tmem_wait_ld();
@@ -995,7 +1000,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                      make_float4(__uint_as_float(u[4 * q]), __uint_as_float(u[4 * q + 1]),
                                  __uint_as_float(u[4 * q + 2]), __uint_as_float(u[4 * q + 3])));
           }
-          __stcg(reinterpret_cast<float2*>(ws + 64 * kBlockM) + r, make_float2(m_used, l));
+          __stcg(reinterpret_cast<float2*>(ws + D * kBlockM) + r, make_float2(m_used, l));
           tc_fence_before();
           if (FUSED) mbar_arrive(&bars[kBarEpiDone]);
           // mbarrier arrive/wait order these writes before the elected thread's
@@ -1014,13 +1019,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (merge_flag[wg]) {
             const float* pa = slot_of(sl0);
             const float* pb = slot_of(sl1);
-            float4 xa[16], xb[16];
-            #pragma unroll
-            for (int q = 0; q < 16; ++q) {
-              xa[q] = ld_chunk(pa, q);
-              xb[q] = ld_chunk(pb, q);
+            #pragma unroll 1
+            for (int h = 0; h < Dm::kAtoms; ++h) {
+              float4 xa[16], xb[16];
+              #pragma unroll
+              for (int q = 0; q < 16; ++q) {
+                xa[q] = ld_chunk(pa, 16 * h + q);
+                xb[q] = ld_chunk(pb, 16 * h + q);
+              }
+              merge_store(h, xa, ld_ml(pa), xb, ld_ml(pb));
             }
-            merge_store(xa, ld_ml(pa), xb, ld_ml(pb));
           }
         }
       }

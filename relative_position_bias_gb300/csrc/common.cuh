@@ -13,11 +13,12 @@ constexpr int kBlockM = 128;      // query rows per tile (one TMEM lane per row)
 constexpr int kRowBytes = 128;    // 64 16-bit elements: one swizzle atom of a row
 constexpr int kTileBytes = 128 * kRowBytes;  // one atom of a 128-row operand tile (16 KB)
 constexpr float kLog2e = 1.4426950408889634f;
-// One partial-result slot of a query tile (head_dim 64, the only one whose
-// units are cut between CTAs): O as 16 column chunks of 4 floats,
-// chunk-major ([16][128] float4, so a warp's 32 rows of one chunk are 512
-// contiguous bytes), then (m, l) per row ([128] float2).
-constexpr int kSlotFloats = 128 * 66;
+// One partial-result slot of a query tile with head_dim D: O as D / 4
+// column chunks of 4 floats, chunk-major ([D / 4][128] float4, so a warp's 32
+// rows of one chunk are 512 contiguous bytes), then (m, l) per row ([128]
+// float2).
+template <int D>
+constexpr int slot_floats() { return 128 * (D + 2); }
 
 // Key tiles cover KHT whole grid rows of WP (>= W) padded columns, so the
 // column of a key inside its tile fixes kw at compile time.  The padded
@@ -47,7 +48,7 @@ struct AttnArgs {
   const void* rel_w;   // [BH, N, W]
   void* out;           // [BH, N, head_dim]
   int* status;         // device status word
-  float* partials;     // [2 * gridDim.x][2][kSlotFloats] partial results (split units only)
+  float* partials;     // [2 * gridDim.x][2][slot_floats<D>()] partial results (split units only)
   unsigned long long* counters;  // [n_units][2] arrival tags per unit and query tile (split units only)
   unsigned long long tag;        // this launch's arrival tag: no earlier launch of the process used it
   int BH, H, W, N;

@@ -240,12 +240,11 @@ Plan make_plan(int BH, int H, int W, int d, int sms) {
   // kMinSplitKeyTiles key tiles (small grids such as 14x14 windows) are not
   // split: the merge of a cut unit costs more than the imbalance it removes
   // (measured on 25 windows x 12 heads of 14x14: 28 us whole, 32 us split).
-  // The merge of cut units is built for head_dim 64 only; head_dim 128 runs
-  // one CTA per unit.
-  p.split = d == 64 && sms > 0 && p.n_kv >= kMinSplitKeyTiles && p.n_units > sms && p.n_units % sms != 0;
+  p.split = sms > 0 && p.n_kv >= kMinSplitKeyTiles && p.n_units > sms && p.n_units % sms != 0;
   p.ctas = p.split ? sms : p.n_units;
   p.counters_bytes = align256(static_cast<size_t>(p.n_units) * 2 * sizeof(unsigned long long));  // one per query tile
-  p.partial_bytes = static_cast<size_t>(2) * sms * 2 * kSlotFloats * sizeof(float);
+  p.partial_bytes = static_cast<size_t>(2) * sms * 2 * (d == 128 ? slot_floats<128>() : slot_floats<64>()) *
+                    sizeof(float);
   return p;
 }
 

@@ -88,9 +88,9 @@ def query_tiles_per_unit() -> int:
 
 def default_plan(w: I.Workload) -> tuple[bool, int, int]:
     """(split, units, units per head) of the default (workspace) schedule, restated from the host
-    plan: units are groups of query tiles of one head; with head_dim 64 the work is split when
-    the units do not fill whole waves of one CTA per SM and a unit spans at least 4 key tiles
-    (whole grid rows of the padded width 16, 32, 40 or 64 per tile)."""
+    plan: units are groups of query tiles of one head; the work is split when the units do not
+    fill whole waves of one CTA per SM and a unit spans at least 4 key tiles (whole grid rows of
+    the padded width 16, 32, 40 or 64 per tile, fewer rows with head_dim 128)."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     per = query_tiles_per_unit()
     units_per_head = (-(-w.N // 128) + per - 1) // per
@@ -98,8 +98,7 @@ def default_plan(w: I.Workload) -> tuple[bool, int, int]:
     wp = next(x for x in (16, 32, 40, 64) if x >= w.W)
     kht = {16: 8, 32: 4, 40: 2, 64: 2}[wp] if w.d == 64 else {16: 4, 32: 2, 40: 2, 64: 1}[wp]
     n_kv = -(-w.H // kht)
-    # only head_dim 64 cuts units between CTAs
-    return (w.d == 64 and n_kv >= 4 and U > sms and U % sms != 0), U, units_per_head
+    return (n_kv >= 4 and U > sms and U % sms != 0), U, units_per_head
 
 
 def tail_heads(w: I.Workload) -> set[int]:
@@ -272,7 +271,7 @@ def test_workspace_size_formula(name):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     per = query_tiles_per_unit()
     split, units, _ = default_plan(w)
-    want = ((8 * per * units + 255) // 256 * 256 + 2 * sms * per * 128 * 66 * 4) if split else 0
+    want = ((8 * per * units + 255) // 256 * 256 + 2 * sms * per * 128 * (w.d + 2) * 4) if split else 0
     assert rpb.workspace_size(w.BH, w.H, w.W, w.d) == want
 
 

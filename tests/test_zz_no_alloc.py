@@ -71,7 +71,7 @@ def test_noalloc_rejects_problems_beyond_its_buffer():
     rbuild.build()
     lib = rpb.load_library()
     fn = _noalloc(lib)
-    # A head count whose unit counters alone exceed the 24 MiB buffer: refused before anything
+    # A head count whose unit counters alone exceed the 48 MiB buffer: refused before anything
     # is enqueued.  The pointers are 16-byte aligned pinned HOST memory, so even if the size
     # check ever stopped firing, the device-memory check would still refuse the call
     # (DERA_ERR_DEVICE) and nothing could be launched on them.
@@ -80,7 +80,7 @@ def test_noalloc_rejects_problems_beyond_its_buffer():
     if need == 0:    # whole waves on this device: nudge the count so the split schedule applies
         BH += 1
         need = rpb.workspace_size(BH, 64, 64)
-    assert need > 24 * 1024 * 1024
+    assert need > 48 * 1024 * 1024
     t = torch.zeros(64, dtype=torch.bfloat16).pin_memory()
     p = t.data_ptr()
     assert p % 16 == 0
