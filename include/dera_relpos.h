@@ -92,7 +92,7 @@ typedef enum dera_dtype { DERA_F16 = 0, DERA_BF16 = 1, DERA_F32 = 2 } dera_dtype
  * of section 实现拆解 item 2):
  *     rel_h[b, n, kh] = sum_c q[b, n, c] * rel_pos_h[qh(n) - kh + H - 1, c]
  *     rel_w[b, n, kw] = sum_c q[b, n, c] * rel_pos_w[qw(n) - kw + W - 1, c]
- * in:  q [BH,N,64], rel_pos_h [2H-1,64], rel_pos_w [2W-1,64], all in_dtype
+ * in:  q [BH,N,head_dim], rel_pos_h [2H-1,head_dim], rel_pos_w [2W-1,head_dim], all in_dtype
  *      (DERA_F16 | DERA_BF16).
  * out: rel_h [BH,N,H], rel_w [BH,N,W] in bias_dtype (DERA_F32, or
  *      DERA_BF16/DERA_F16, rounded to nearest from the fp32 accumulator).
@@ -105,9 +105,9 @@ DERA_API dera_status dera_relpos_project(const void* q, const void* rel_pos_h, c
  * A2..A7 — attention with a compact bias (deepencoder_rel_pos_attention;
  * page sections 关键源码片段 and 实现拆解 item 1):
  *     out[b, n] = sum_m softmax_m(scale * q[b,n].k[b,m] + rel_h[b,n,kh(m)] + rel_w[b,n,kw(m)]) v[b,m]
- * in:  q, k, v [BH,N,64] in_dtype (DERA_F16 | DERA_BF16);
+ * in:  q, k, v [BH,N,head_dim] in_dtype (DERA_F16 | DERA_BF16);
  *      rel_h [BH,N,H], rel_w [BH,N,W] in bias_dtype (DERA_F32 | DERA_BF16 | DERA_F16).
- * out: out [BH,N,64] in out_dtype (DERA_F32, or in_dtype).
+ * out: out [BH,N,head_dim] in out_dtype (DERA_F32, or in_dtype).
  * workspace / workspace_bytes: optional scratch, see dera_relpos_workspace_size.
  * Softmax runs in base 2 with fp32 accumulation; P is rounded to fp16 for the
  * P.V product (for bf16 inputs, V tiles are converted to fp16 on chip, so
@@ -124,8 +124,8 @@ DERA_API dera_status dera_relpos_attention(const void* q, const void* k, const v
  * A1..A7 fused — projection computed inside the attention kernel (tensor-core
  * q.rel_pos^T products, skewed on chip), so neither the dense HW x HW bias
  * nor the compact rel_h / rel_w ever reaches global memory.
- * in:  q, k, v [BH,N,64], rel_pos_h [2H-1,64], rel_pos_w [2W-1,64], in_dtype.
- * out: out [BH,N,64] in out_dtype (DERA_F32, or in_dtype).
+ * in:  q, k, v [BH,N,head_dim], rel_pos_h [2H-1,head_dim], rel_pos_w [2W-1,head_dim], in_dtype.
+ * out: out [BH,N,head_dim] in out_dtype (DERA_F32, or in_dtype).
  * workspace / workspace_bytes: optional scratch, see dera_relpos_workspace_size.
  */
 DERA_API dera_status dera_relpos_fused(const void* q, const void* k, const void* v, const void* rel_pos_h,
