@@ -47,6 +47,12 @@ constexpr float kSpecSumLimit = 65000.0f;
 // above 2^-12, inside the fp16 normal range; kStartMargin below the estimate.
 constexpr float kStartCap = 12.0f;
 constexpr float kStartMargin = 4.0f;
+// Cap used once a row of the CTA has failed the row check: with the starting
+// maximum at most 3 above the first tile's exact maximum, l >= 2^-3, which
+// passes the check for every segment (n <= 4096 keys), so no later segment
+// of the CTA needs a replay.  Inputs whose row maximum moves far between key
+// tiles (wide logit ranges) fail early and then run with this cap.
+constexpr float kSafeCap = 3.0f;
 // Row-sum check at the end of a segment: the row sum l, in units of the
 // running maximum, must be at least the segment's valid key count times
 // 2^kMinRowSumLog2 (see the epilogue).
@@ -243,6 +249,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   volatile int* merge_flag = reinterpret_cast<volatile int*>(smem + SM::kMisc + 8);  // [2]
   volatile int* bad_flag = reinterpret_cast<volatile int*>(smem + SM::kMisc + 16);   // [2 tiles][2 parities]
   ReplayRecord* replay = reinterpret_cast<ReplayRecord*>(smem + SM::kMisc + 32);     // [2 tiles]
+  volatile int* cap_drop = reinterpret_cast<volatile int*>(smem + SM::kMisc + 80);   // a row check failed
   int* status = args.status;
 
   const int warp = threadIdx.x >> 5;
@@ -260,6 +267,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     merge_flag[0] = 0;
     merge_flag[1] = 0;
     for (int i = 0; i < 4; ++i) bad_flag[i] = 0;
+    *cap_drop = 0;
     replay[0].pending = 0;
     replay[1].pending = 0;
     mbar_init(&bars[kBarQFull], 1);
@@ -563,7 +571,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const float2 sl2v = make_float2(sl2, sl2);
 
     int gi = 0, seg = 0;
-    float cap = kStartCap;  // overshoot allowed to the starting maximum; 0 after a failed check
+    // overshoot allowed to the starting maximum: kStartCap until a row check
+    // of the CTA fails, kSafeCap after, 0 in replays
+    float cap = kStartCap;
+    bool own_failed = false;  // this warpgroup has failed a row check (uniform over it)
     int pseg = 0;  // completed phases of this warpgroup's merge-go barrier
     int ppub = 0;  // completed phases of its partial-written barrier
     uint32_t stg_phase = 0;  // completed phases of this warpgroup's staging barrier
@@ -576,6 +587,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     };
     bool ok = true;
     auto run_seg = [&](const Segment& sg, int store_mask) -> bool {
+      // the other warpgroup's flag may be seen late; either value is safe
+      cap = store_mask >= 0 ? 0.f : ((own_failed || *cap_drop) ? kSafeCap : kStartCap);
       const int bh = sg.u / args.n_pairs;
       const int qt = 2 * (sg.u - bh * args.n_pairs) + wg;
       const int n = qt * kBlockM + r;
@@ -831,8 +844,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (r == 0) {
           replay[wg].sg = sg;
           replay[wg].pending = 1;
+          *cap_drop = 1;
         }
-        cap = 0.f;
+        own_failed = true;
       }
       if (!store) {
         tc_fence_before();
