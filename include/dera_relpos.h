@@ -147,8 +147,9 @@ DERA_API dera_status dera_relpos_fused(const void* q, const void* k, const void*
  * (unit, key tile) iteration space and cuts some units between two CTAs; the
  * partial results (unnormalised O, row max, row sum, fp32) and two 8-byte
  * arrival counters per unit (one per query tile) live in the caller's
- * `workspace`.  A NULL workspace, or one smaller than this size, selects one
- * CTA per unit instead (same result, no scratch, less even load).  The
+ * `workspace`.  A NULL workspace, or one smaller than this size, selects
+ * whole units taken round-robin by one CTA per SM instead (same result, no
+ * scratch, less even load).  The
  * workspace must be device memory, 256-byte aligned, owned by the caller, and
  * not used by another call in flight.  Its contents need no initialisation
  * and are never cleared: each launch marks its arrivals with a 64-bit tag that

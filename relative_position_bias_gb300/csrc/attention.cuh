@@ -153,14 +153,25 @@ static_assert(kBarCount <= AttnSmem<64, 128>::kNumBars, "barrier slots");
 // then holds fewer key tiles the more unit starts it contains.  Each range
 // still spans at least n_kv + kSegCost virtual slots, so no unit is cut into
 // more than two segments.
+//
+// Without cuts (no workspace, or units too short to be worth cutting) the G
+// CTAs take whole units round-robin: CTA c runs units c, c + G, c + 2G, ...
+// (the last round may hold fewer units than CTAs), so a CTA's later units are
+// loaded while it computes the earlier ones.
 struct Schedule {
   static constexpr int kSegCost = 8;
-  int G, n_kv, dp_rounds;
-  long long sk_base, V;  // first tail iteration; tail length in virtual slots
-  __device__ __forceinline__ Schedule(int U, int G_, int n_kv_) : G(G_), n_kv(n_kv_) {
-    dp_rounds = max(U / G - 1, 0);
-    sk_base = static_cast<long long>(dp_rounds) * G * n_kv;
-    V = static_cast<long long>(U - dp_rounds * G) * (n_kv + kSegCost);
+  int G, n_kv, dp_rounds, U;
+  long long sk_base, V;  // first tail iteration; tail length in virtual slots (0: no tail)
+  __device__ __forceinline__ Schedule(int U_, int G_, int n_kv_, bool cut) : G(G_), n_kv(n_kv_), U(U_) {
+    if (cut) {
+      dp_rounds = max(U / G - 1, 0);
+      sk_base = static_cast<long long>(dp_rounds) * G * n_kv;
+      V = static_cast<long long>(U - dp_rounds * G) * (n_kv + kSegCost);
+    } else {
+      dp_rounds = (U + G - 1) / G;
+      sk_base = static_cast<long long>(U) * n_kv;
+      V = 0;
+    }
   }
   // tail iteration (relative to sk_base) at virtual slot v, 0 <= v <= V
   __device__ __forceinline__ long long real_of(long long v) const {
@@ -171,7 +182,7 @@ struct Schedule {
   __device__ __forceinline__ long long begin(int c) const {
     return sk_base + real_of(static_cast<long long>(c) * V / G);
   }
-  // CTA whose tail range holds iteration t (t >= sk_base)
+  // CTA whose tail range holds iteration t (t >= sk_base; only with cuts)
   __device__ __forceinline__ int cta_of(long long t) const {
     const long long tr = t - sk_base, u = tr / n_kv;
     const long long v = u * (n_kv + kSegCost) + kSegCost + (tr - u * n_kv);
@@ -202,7 +213,8 @@ struct Cursor {
       sg.j1 = s.n_kv;
       sg.tail = -1;
       ++round;
-      return true;
+      if (sg.u < s.U) return true;
+      round = s.dp_rounds;  // a last round with fewer units than CTAs
     }
     if (it >= end) return false;
     sg.u = static_cast<int>(it / s.n_kv);
@@ -259,7 +271,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_kv = args.n_kv;
-  const Schedule sched(args.n_units, static_cast<int>(gridDim.x), n_kv);
+  const Schedule sched(args.n_units, static_cast<int>(gridDim.x), n_kv, args.counters != nullptr);
   constexpr bool convert_v = BF16;  // P is fp16, so bf16 V tiles are converted to fp16 on chip
 
   auto sQ = [&](int i) { return smem + SM::kQ + i * Dm::kQTile; };

@@ -226,6 +226,11 @@ struct Plan {
   size_t counters_bytes, partial_bytes;
 };
 
+// CTAs of a schedule without cuts: one per SM, taking whole units
+// round-robin, or one per unit when there are fewer units (or the SM count
+// is unknown).
+int uncut_ctas(int n_units, int sms) { return sms > 0 && n_units > sms ? sms : n_units; }
+
 Plan make_plan(int BH, int H, int W, int d, int sms) {
   Plan p;
   const int N = H * W;
@@ -241,7 +246,7 @@ Plan make_plan(int BH, int H, int W, int d, int sms) {
   // split: the merge of a cut unit costs more than the imbalance it removes
   // (measured on 25 windows x 12 heads of 14x14: 28 us whole, 32 us split).
   p.split = sms > 0 && p.n_kv >= kMinSplitKeyTiles && p.n_units > sms && p.n_units % sms != 0;
-  p.ctas = p.split ? sms : p.n_units;
+  p.ctas = p.split ? sms : uncut_ctas(p.n_units, sms);
   p.counters_bytes = align256(static_cast<size_t>(p.n_units) * 2 * sizeof(unsigned long long));  // one per query tile
   p.partial_bytes = static_cast<size_t>(2) * sms * 2 * (d == 128 ? slot_floats<128>() : slot_floats<64>()) *
                     sizeof(float);
@@ -272,8 +277,8 @@ dera_status run_attention(const void* q, const void* k, const void* v, const voi
   const int N = H * W;
   Plan plan = make_plan(BH, H, W, d, sm_count(dev));
   if (plan.split && (workspace == nullptr || workspace_bytes < workspace_bytes_for(plan))) {
-    plan.split = false;  // no (or too small a) workspace: one CTA per unit
-    plan.ctas = plan.n_units;
+    plan.split = false;  // no (or too small a) workspace: whole units, round-robin
+    plan.ctas = uncut_ctas(plan.n_units, sm_count(dev));
   }
   const int WP = padded_width(W), KHT = rows_per_tile(WP, d);
   AttnMaps maps;

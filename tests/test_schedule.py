@@ -84,3 +84,17 @@ def test_tail_partition(n_kv, G):
                 (c0, a0, b0, t0), (c1, a1, b1, t1) = ps
                 assert c1 == c0 + 1 and t1 == 0 and a0 == 0 and b1 == n_kv and b0 == a1
                 assert (t0 == 0) == (begin(c0) == u0)
+
+
+@pytest.mark.parametrize("G", [1, 2, 3, 7, 148, 152])
+def test_round_robin_without_cuts(G):
+    """Without cuts (no workspace, or units shorter than 4 key tiles) CTA c of G runs the whole
+    units c, c + G, c + 2G, ... below U: every unit exactly once, in ceil(U / G) rounds."""
+    for U in list(range(1, 3 * G + 3)) + [10 * G + 7]:
+        rounds = -(-U // G)
+        seen = []
+        for c in range(G):
+            mine = [r * G + c for r in range(rounds) if r * G + c < U]
+            assert len(mine) in (rounds - 1, rounds) or U < G
+            seen.extend(mine)
+        assert sorted(seen) == list(range(U))
