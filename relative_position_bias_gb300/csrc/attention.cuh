@@ -666,15 +666,41 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
           }
         };
-        copy_rows(args.rel_w, W, kBiasStride);
+        // An fp32 bias is copied as it is with cp.async: every element of
+        // the tile's rows goes out at once (element e of the block to thread
+        // e mod 128, so a warp reads 128 contiguous bytes), without a round
+        // trip through registers per batch of rows; the log2e scaling is
+        // applied where the rows are read.  Rows past N are written as 0.
+        const bool raw = args.bias_fmt == kF32;
+        auto copy_rows_async = [&](const float* src, int len, int stride) {
+          const int step_r = kBlockM / len, step_c = kBlockM - step_r * len;
+          int rr = r / len, c = r - rr * len;
+          for (int e = r; e < kBlockM * len; e += kBlockM) {
+            cp_async4(area + rr * stride + c, src + (row0 + (rr < nrows ? rr : 0)) * static_cast<size_t>(len) + c,
+                      rr < nrows ? 4u : 0u);
+            rr += step_r;
+            c += step_c;
+            if (c >= len) {
+              c -= len;
+              ++rr;
+            }
+          }
+          cp_async_wait_all();
+        };
+        if (raw) copy_rows_async(static_cast<const float*>(args.rel_w), W, kBiasStride);
+        else copy_rows(args.rel_w, W, kBiasStride);
         ok = wg_sync() && ok;
         const float* stg = area + r * kBiasStride;
+        const float wscale = raw ? kLog2e : 1.0f;
         #pragma unroll
-        for (int kw = 0; kw < WP; ++kw) bw[kw] = kw < W ? stg[kw] : NEG_INF;
+        for (int kw = 0; kw < WP; ++kw) bw[kw] = kw < W ? wscale * stg[kw] : NEG_INF;
         // every thread has its rel_w row before the area is reused for rel_h
         ok = wg_sync() && ok;
-        copy_rows(args.rel_h, H, HS);
+        if (raw) copy_rows_async(static_cast<const float*>(args.rel_h), H, HS);
+        else copy_rows(args.rel_h, H, HS);
         ok = wg_sync() && ok;
+        if (raw)
+          for (int kh = 0; kh < H; ++kh) bh_row[kh] *= kLog2e;   // this thread's own row
         for (int kh = H; kh < Hpad; ++kh) bh_row[kh] = NEG_INF;
         if (!ok) return false;
       }

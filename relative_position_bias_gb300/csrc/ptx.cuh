@@ -76,6 +76,16 @@ __device__ __forceinline__ bool mbar_wait_budget(uint64_t* bar, uint32_t parity,
   }
 }
 
+// ---------------------------------------------------------------- async copies
+// 4-byte global -> shared copy that does not pass through registers; with
+// src_bytes = 0 it writes zero and reads nothing.
+__device__ __forceinline__ void cp_async4(void* dst_smem, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst_smem)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+// Waits until every cp.async of this thread has landed in shared memory.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // ---------------------------------------------------------------- named barriers
 // Barrier `id` (1..15) over `count` threads (a multiple of 32); returns whether
 // `pred` holds on every thread that takes part.  The non-.aligned forms, so a
