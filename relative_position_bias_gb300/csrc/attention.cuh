@@ -580,7 +580,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t tO = tbase + lane_off + Dm::tmO(wg);
     float* area = reinterpret_cast<float*>(smem + SM::kBias) + wg * kBlockM * kBiasStride;
     const int Hpad = n_kv * KHT;
-    const int HS = Hpad + 1;
+    const int HS = kBiasStride;  // >= Hpad + 1; a thread's rel_h row is its staging row
     float* bh_row = area + r * HS;
     const float NEG_INF = -__int_as_float(0x7f800000);
     const float sl2 = args.scale_log2;
@@ -620,9 +620,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (ok) skew_row_to_smem(tbase + lane_off + 256 * wg + 128, qw, W, stg, kLog2e);
         #pragma unroll
         for (int kw = 0; kw < WP; ++kw) bw[kw] = (ok && kw < W) ? stg[kw] : NEG_INF;
-        // the staging rows (stride kBiasStride) overlap the bias rows (stride HS):
-        // every thread of the warpgroup has read its staged row before any bias row is written
-        ok = wg_sync() && ok;
+        // the staging row and the bias row of a thread are the same row (stride
+        // kBiasStride both), read and written by that thread alone
         if (ok) {
           skew_row_to_smem(tbase + lane_off + 256 * wg, qh, H, bh_row, kLog2e);
           for (int kh = H; kh < Hpad; ++kh) bh_row[kh] = NEG_INF;
