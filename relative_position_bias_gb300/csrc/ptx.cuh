@@ -86,26 +86,6 @@ __device__ __forceinline__ void cp_async4(void* dst_smem, const void* src, uint3
 // Waits until every cp.async of this thread has landed in shared memory.
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// ---------------------------------------------------------------- named barriers
-// Barrier `id` (1..15) over `count` threads (a multiple of 32); returns whether
-// `pred` holds on every thread that takes part.  The non-.aligned forms, so a
-// warp need not arrive converged.
-__device__ __forceinline__ bool bar_and(int id, int count, bool pred) {
-  int r;
-  asm volatile(
-      "{\n\t.reg .pred pi, po;\n\t"
-      "setp.ne.b32 pi, %1, 0;\n\t"
-      "barrier.red.and.pred po, %2, %3, pi;\n\t"
-      "selp.b32 %0, 1, 0, po;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<int>(pred)), "r"(id), "r"(count)
-      : "memory");
-  return r != 0;
-}
-__device__ __forceinline__ void bar_sync(int id, int count) {
-  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
