@@ -6,8 +6,8 @@ trigger the synchronisation an allocation can cause), so they cannot supply
 the scratch workspace that dera_relpos_fused uses when it splits work units
 between CTAs.  dera_relpos_fused_noalloc takes that scratch from a buffer
 compiled into the library instead.  This test calls it through the C ABI
-(ctypes, no binding helper) twice in a row on a workload whose schedule does
-split units, and compares each result with dera_relpos_fused's, within the
+(ctypes, no binding helper) twice in a row on workloads whose schedule does
+split units (head_dim 64 and 128), and compares each result with dera_relpos_fused's, within the
 tolerance the parity tests use (max-abs 4e-3, relative L2 1e-2).  It lives in
 its own file, collected last, and passes alone or after the other tests.
 """
@@ -39,12 +39,13 @@ def _noalloc(lib):
     return fn
 
 
-def test_noalloc_matches_fused_on_two_calls():
+@pytest.mark.parametrize("name", ["global64", "global64d128"])
+def test_noalloc_matches_fused_on_two_calls(name):
     rbuild.build()
     lib = rpb.load_library()
     fn = _noalloc(lib)
-    w = I.WORKLOADS["global64"]
-    assert rpb.workspace_size(w.BH, w.H, w.W) > 0, "this workload must use the split schedule"
+    w = I.WORKLOADS[name]
+    assert rpb.workspace_size(w.BH, w.H, w.W, w.d) > 0, "this workload must use the split schedule"
     x = I.make_inputs(w)
     d = {k: t.cuda() for k, t in x.items()}
     ref = rpb.fused(d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W, w.scale,
