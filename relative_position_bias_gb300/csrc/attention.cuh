@@ -65,6 +65,15 @@ constexpr float kSafeCap = 3.0f;
 // catches most redos of inputs whose rel_h spreads widely over the grid rows
 // (40x40 with fp16 inputs: 365 -> 307 us) and never fires on the 64x64 inputs.
 constexpr float kPredictMargin = 14.0f;
+// A warp in which at least kWideRows rows start with a rel_h-based estimate
+// more than kWideGap (base 2) above their first tile's exact maximum holds
+// rows whose rel_h spreads over most of the 40 binades of fp16 P; at
+// kStartCap such rows mostly fail the row check (and the segment is run
+// again), so the warp starts the segment at kSafeCap instead.  On the 40x40
+// fp16 inputs every warp qualifies (307 -> 287 us, the first segment of each
+// CTA no longer replayed); on the 64x64 inputs, head_dim 64 or 128, none does.
+constexpr float kWideGap = 32.0f;
+constexpr int kWideRows = 4;
 // Row-sum check at the end of a segment: the row sum l, in units of the
 // running maximum, must be at least the segment's valid key count times
 // 2^kMinRowSumLog2 (see the epilogue).
@@ -596,7 +605,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
     int gi = 0, seg = 0;
     // overshoot allowed to the starting maximum: kStartCap until a row check
-    // of the CTA fails, kSafeCap after, 0 in replays
+    // of the CTA fails, kSafeCap after (and for a segment of a warp of wide
+    // rows, kWideRows), 0 in replays
     float cap = kStartCap;
     bool own_failed = false;  // this warpgroup has failed a row check (uniform over it)
     int pseg = 0;  // completed phases of this warpgroup's merge-go barrier
@@ -852,7 +862,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             // row's largest rel_h (less a margin), capped above the exact
             // maximum of this tile: later tiles then seldom pass the row-sum
             // bound and need an exact redo
-            m_used = fmaxf(fmaxf(mt, fminf(mt + cap, base + mbh - kStartMargin)), -FLT_MAX);
+            const float est = base + mbh - kStartMargin;
+            if (__popc(__ballot_sync(0xffffffffu, est - mt > kWideGap)) >= kWideRows) cap = fminf(cap, kSafeCap);
+            m_used = fmaxf(fmaxf(mt, fminf(mt + cap, est)), -FLT_MAX);
           } else {
             wait_pv();
             // the same estimate, capped above this tile's exact maximum
