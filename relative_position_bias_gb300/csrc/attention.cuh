@@ -605,8 +605,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
     int gi = 0, seg = 0;
     // overshoot allowed to the starting maximum: kStartCap until a row check
-    // of the CTA fails, kSafeCap after (and for a segment of a warp of wide
-    // rows, kWideRows), 0 in replays
+    // of the CTA fails, kSafeCap after it (and in a segment where the warp's
+    // rows are wide, see kWideRows), 0 in replays
     float cap = kStartCap;
     bool own_failed = false;  // this warpgroup has failed a row check (uniform over it)
     int pseg = 0;  // completed phases of this warpgroup's merge-go barrier
