@@ -14,7 +14,12 @@ of keys sit about 13 (base 2) below the maximum.  A starting maximum estimated f
 largest rel_h" overshoots the true maximum by 12 there.
 
 `test_rows_sum_to_one` uses V = 1, for which every output is exactly 1 at any size, and checks it
-on every row of every workload, for both entries."""
+on every row of every workload, for both entries.
+
+`test_rel_h_patterns` moves the row maximum by large steps between key tiles through the rel_h
+term alone (rising, falling, and jumping on every other tile), which drives the kernel's
+decisions per tile: take a tile exact at once, exponentiate it speculatively, or start a warp at
+the safe cap."""
 from __future__ import annotations
 
 import math
@@ -133,3 +138,68 @@ def test_rows_sum_to_one(name, entry):
     record_margin(f"rows sum to 1: {entry} {name} (all rows)", err, rl2, "2e-3 / 1e-2")
     assert bool(torch.isfinite(out).all())
     assert err <= 2e-3, f"{entry} {name}: max |out - 1| = {err:.3e}"
+
+
+def ramp_case(H: int, W: int, heads: int, dtype: torch.dtype, pattern: str, seed: int = 11):
+    """A rel_h term that moves the row maximum by a fixed pattern across the key grid rows, the
+    same problem for every head.  q = a*e0 + small noise, T_h[i, 0] = f(i) / a, so
+    rel_h[n, kh] = f(qh - kh + H - 1) (natural units), and the scores and rel_w stay small:
+      "rise": f falls by 8 (base 2) per table row, so rel_h rises by 8 per key grid row and every
+              key tile lifts the row maximum by about 16: each tile is taken exact at once, and
+              the rel_h spread makes every warp start from the safe cap;
+      "fall": the mirror image: the first key tile holds the maximum and later tiles sit far below;
+      "zigzag": f is 24 (base 2) on pairs of table rows and 0 on the pairs between, so the
+              maximum jumps on every other key tile."""
+    a = 2.0
+    scale = 0.125
+    N = H * W
+    g = torch.Generator().manual_seed(seed)
+    q = 0.05 * torch.randn(N, 64, generator=g)
+    q[:, 0] = a
+    k = 0.5 * torch.randn(N, 64, generator=g)
+    k[:, 0] = 0.0
+    v = torch.randn(N, 64, generator=g)
+    i = torch.arange(2 * H - 1, dtype=torch.float32)
+    if pattern == "rise":
+        f = -8.0 * i
+    elif pattern == "fall":
+        f = 8.0 * i
+    else:
+        f = torch.where((torch.div(i, 2, rounding_mode="floor") % 2) == 0, torch.tensor(24.0), torch.tensor(0.0))
+    th = 0.1 * torch.randn(2 * H - 1, 64, generator=g)
+    th[:, 0] = f / LOG2E / a
+    tw = 0.1 * torch.randn(2 * W - 1, 64, generator=g)
+    x = {"q": q, "k": k, "v": v, "rel_pos_h": th, "rel_pos_w": tw}
+    x = {n: t.to(dtype) for n, t in x.items()}
+    for n in ("q", "k", "v"):
+        x[n] = x[n].expand(heads, N, 64).contiguous()
+    return x, scale
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "f16"])
+@pytest.mark.parametrize("grid", [(64, 64, 12), (40, 40, 24)], ids=["64x64", "40x40"])
+@pytest.mark.parametrize("pattern", ["rise", "fall", "zigzag"])
+@pytest.mark.parametrize("entry", ["fused", "attention"])
+def test_rel_h_patterns(entry, pattern, grid, dtype):
+    """Row maxima that move by large steps between key tiles: the tiles the kernel takes exact
+    at once, the ones it exponentiates speculatively and the safe starting cap all meet here."""
+    H, W, heads = grid
+    x, scale = ramp_case(H, W, heads, dtype, pattern)
+    d = {n: t.cuda() for n, t in x.items()}
+    f = {n: I.to_f64(t) for n, t in x.items()}
+    if entry == "fused":
+        out = rpb.fused(d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], H, W, scale,
+                        out_dtype=torch.float32)
+    else:
+        rh, rw = rpb.project(d["q"], d["rel_pos_h"], d["rel_pos_w"], H, W)
+        out = rpb.attention(d["q"], d["k"], d["v"], rh, rw, H, W, scale, out_dtype=torch.float32)
+    want = oracle.fused(f["q"][:1], f["k"][:1], f["v"][:1], f["rel_pos_h"], f["rel_pos_w"], H, W, scale)
+    torch.cuda.synchronize()
+    got = out.double().cpu().numpy()
+    assert np.isfinite(got).all()
+    err = np.abs(got - want)
+    rl2 = np.linalg.norm(got - want) / (np.linalg.norm(want) * math.sqrt(heads))
+    what = f"rel_h {pattern} {entry} {H}x{W} {str(dtype)[6:]}"
+    record_margin(what, err.max(), rl2)
+    assert err.max() <= ABS_TOL, f"{what}: max-abs {err.max():.3e}"
+    assert rl2 <= RL2_TOL
