@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define DERA_RELPOS_ABI_VERSION 2
+#define DERA_RELPOS_ABI_VERSION 3
 
 #if defined(__GNUC__)
 #define DERA_API __attribute__((visibility("default")))
@@ -159,6 +159,60 @@ DERA_API dera_status dera_relpos_fused(const void* q, const void* k, const void*
 DERA_API dera_status dera_relpos_workspace_size(int BH, int H, int W, int head_dim, size_t* bytes);
 
 /*
+ * Training forward: dera_relpos_fused that also writes, for every row, the
+ * base-2 log-sum-exp of its logits, lse[b, n] = log2(sum_m exp(Z[b, n, m])) with
+ * Z = scale q k^T + rel_h + rel_w (vLLM PR #55629 page, section 实现拆解 item 1:
+ * the online softmax's row maximum and row sum, combined).  lse: [BH, N] fp32,
+ * device memory, 16-byte aligned.  Every other argument, error and the output
+ * are as for dera_relpos_fused.  The backward needs lse.
+ */
+DERA_API dera_status dera_relpos_fused_lse(const void* q, const void* k, const void* v, const void* rel_pos_h,
+                                  const void* rel_pos_w, void* out, float* lse, int BH, int H, int W,
+                                  int head_dim, float scale, dera_dtype in_dtype, dera_dtype out_dtype,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Scratch needed by dera_relpos_fused_backward (bytes, written to *bytes):
+ * 4 * (BH N (2 (H + W) + 65) + BH ceil(N / 128) 64 (2H - 1 + 2W - 1)) plus
+ * alignment: the compact bias, row terms, dq before its bias part, the bias
+ * gradients and per-tile table-gradient partials, all fp32.  head_dim must be 64.
+ */
+DERA_API dera_status dera_relpos_backward_workspace_size(int BH, int H, int W, int head_dim, size_t* bytes);
+
+/*
+ * Backward of dera_relpos_fused (training use; the pages print no backward:
+ * this is the chain-rule gradient of the forward's definition).  With
+ * Z = scale q k^T + rel_h + rel_w, P = softmax(Z), an upstream gradient dout
+ * and D[n] = dout[n] . out[n], dZ = P * (dout v^T - D):
+ *   dv = P^T dout, dk = scale dZ^T q,
+ *   dq = scale dZ k + sum_kh drel_h[n, kh] rel_pos_h[qh - kh + H - 1] + sum_kw (same for w),
+ *   drel_pos_h[i] = sum over (b, n, kh) with qh - kh + H - 1 = i of drel_h[b, n, kh] q[b, n] (same for w),
+ * where drel_h[n, kh] = sum_kw dZ[n, kh W + kw] and drel_w[n, kw] = sum_kh dZ[n, kh W + kw].
+ * in:  q, k, v [BH,N,64] and rel_pos_h [2H-1,64], rel_pos_w [2W-1,64] in in_dtype
+ *      (as given to the forward); out [BH,N,64] (the forward's output) in out_dtype
+ *      (DERA_F32 or in_dtype); lse [BH,N] fp32 from dera_relpos_fused_lse; dout
+ *      [BH,N,64] in in_dtype.
+ * out: dq, dk, dv [BH,N,64] in grad_dtype (DERA_F32 or in_dtype); drel_pos_h
+ *      [2H-1,64] and drel_pos_w [2W-1,64] fp32 (summed over every batch and head).
+ * workspace: device memory of at least dera_relpos_backward_workspace_size bytes,
+ *      256-byte aligned, owned by the caller, not used by another call in flight;
+ *      its contents need no initialisation.
+ * Precision: P is recomputed from lse in fp32; dZ and P enter the tensor-core
+ *      products rounded to in_dtype (relative 2^-9 for bf16, 2^-11 for fp16), with
+ *      fp32 accumulation; the bias and table gradients are accumulated in fp32.
+ *      Nothing is accumulated with atomics: the result is the same on every run.
+ * Errors: DERA_ERR_HEAD_DIM unless head_dim is 64; DERA_ERR_SCRATCH if the
+ *      workspace is NULL or smaller than the size above; otherwise as for
+ *      dera_relpos_fused.
+ */
+DERA_API dera_status dera_relpos_fused_backward(const void* q, const void* k, const void* v, const void* rel_pos_h,
+                                       const void* rel_pos_w, const void* out, const float* lse,
+                                       const void* dout, void* dq, void* dk, void* dv, float* drel_pos_h,
+                                       float* drel_pos_w, int BH, int H, int W, int head_dim, float scale,
+                                       dera_dtype in_dtype, dera_dtype out_dtype, dera_dtype grad_dtype,
+                                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Allocation-free variant of dera_relpos_fused (the pages have no
  * counterpart: it exists for callers of this library that are not allowed
  * to allocate device memory).  Some callers cannot call cudaMalloc at all:
@@ -219,7 +273,8 @@ DERA_API dera_status dera_relpos_device_status(int* status, int reset);
  */
 DERA_API dera_status dera_relpos_selftest_wait_timeout(long long budget_cycles, void* stream);
 
-/* ABI version of the loaded library (DERA_RELPOS_ABI_VERSION; 2 added the workspace arguments). */
+/* ABI version of the loaded library (DERA_RELPOS_ABI_VERSION; 2 added the workspace arguments, 3 the
+ * training forward and the backward). */
 DERA_API int dera_relpos_abi_version(void);
 
 #ifdef __cplusplus

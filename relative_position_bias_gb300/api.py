@@ -64,6 +64,13 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.dera_relpos_selftest_wait_timeout.restype = i
         lib.dera_relpos_abi_version.argtypes = []
         lib.dera_relpos_abi_version.restype = i
+        lib.dera_relpos_fused_lse.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, sz, vp]
+        lib.dera_relpos_fused_lse.restype = i
+        lib.dera_relpos_backward_workspace_size.argtypes = [i, i, i, i, ctypes.POINTER(sz)]
+        lib.dera_relpos_backward_workspace_size.restype = i
+        lib.dera_relpos_fused_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f,
+                                                   i, i, i, vp, sz, vp]
+        lib.dera_relpos_fused_backward.restype = i
         _lib = lib
         return lib
 
@@ -212,6 +219,74 @@ def fused(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, rel_pos_h: torch.Te
     _check(lib.dera_relpos_fused(_ptr(q), _ptr(k), _ptr(v), _ptr(rel_pos_h), _ptr(rel_pos_w), _ptr(out), BH, H, W,
                                  d, float(scale), _code(q.dtype), _code(out.dtype), ws, ws_bytes, st))
     return out
+
+
+def fused_lse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, rel_pos_h: torch.Tensor, rel_pos_w: torch.Tensor,
+              H: int, W: int, scale: float | None = None, out_dtype: torch.dtype | None = None, stream=None,
+              workspace=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """Training forward via ``dera_relpos_fused_lse``: ``(out, lse)``, lse [BH, N] fp32 (base 2)."""
+    BH, N, d = q.shape
+    scale = d ** -0.5 if scale is None else scale
+    out = torch.empty((BH, N, d), dtype=out_dtype or q.dtype, device=q.device)
+    lse = torch.empty((BH, N), dtype=torch.float32, device=q.device)
+    for t, name in ((q, "q"), (k, "k"), (v, "v")):
+        _expect(t, (BH, H * W, d), name)
+    _expect(rel_pos_h, (2 * H - 1, d), "rel_pos_h")
+    _expect(rel_pos_w, (2 * W - 1, d), "rel_pos_w")
+    for t in (k, v, rel_pos_h, rel_pos_w):
+        if t.dtype != q.dtype:
+            raise TypeError("q, k, v and the tables must share a dtype")
+    lib = load_library()
+    st = _stream(q.device, stream)
+    ws, ws_bytes = _workspace(q.device, BH, H, W, d, workspace, st)
+    _check(lib.dera_relpos_fused_lse(_ptr(q), _ptr(k), _ptr(v), _ptr(rel_pos_h), _ptr(rel_pos_w), _ptr(out), _ptr(lse),
+                                     BH, H, W, d, float(scale), _code(q.dtype), _code(out.dtype), ws, ws_bytes, st))
+    return out, lse
+
+
+def backward_workspace_size(BH: int, H: int, W: int, head_dim: int = 64) -> int:
+    """Scratch bytes of :func:`fused_backward` for this size."""
+    n = ctypes.c_size_t(0)
+    _check(load_library().dera_relpos_backward_workspace_size(BH, H, W, head_dim, ctypes.byref(n)))
+    return n.value
+
+
+def fused_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, rel_pos_h: torch.Tensor,
+                   rel_pos_w: torch.Tensor, out: torch.Tensor, lse: torch.Tensor, dout: torch.Tensor, H: int, W: int,
+                   scale: float | None = None, grad_dtype: torch.dtype | None = None, stream=None,
+                   workspace: torch.Tensor | None = None):
+    """Gradients of :func:`fused` via ``dera_relpos_fused_backward``:
+    ``(dq, dk, dv, drel_pos_h, drel_pos_w)``; dq, dk, dv in ``grad_dtype`` (default fp32), the
+    table gradients fp32.  ``out`` and ``lse`` come from :func:`fused_lse`."""
+    BH, N, d = q.shape
+    scale = d ** -0.5 if scale is None else scale
+    gd = grad_dtype or torch.float32
+    for t, name in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        _expect(t, (BH, H * W, d), name)
+    _expect(lse, (BH, H * W), "lse")
+    _expect(rel_pos_h, (2 * H - 1, d), "rel_pos_h")
+    _expect(rel_pos_w, (2 * W - 1, d), "rel_pos_w")
+    for t in (k, v, rel_pos_h, rel_pos_w, dout):
+        if t.dtype != q.dtype:
+            raise TypeError("q, k, v, dout and the tables must share a dtype")
+    if lse.dtype != torch.float32:
+        raise TypeError("lse must be float32")
+    dq = torch.empty((BH, N, d), dtype=gd, device=q.device)
+    dk = torch.empty_like(dq)
+    dv = torch.empty_like(dq)
+    dth = torch.empty((2 * H - 1, d), dtype=torch.float32, device=q.device)
+    dtw = torch.empty((2 * W - 1, d), dtype=torch.float32, device=q.device)
+    lib = load_library()
+    st = _stream(q.device, stream)
+    if workspace is None:
+        with torch.cuda.device(q.device):
+            need = backward_workspace_size(BH, H, W, d)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _check(lib.dera_relpos_fused_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(rel_pos_h), _ptr(rel_pos_w), _ptr(out),
+                                          _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dth), _ptr(dtw),
+                                          BH, H, W, d, float(scale), _code(q.dtype), _code(out.dtype), _code(gd),
+                                          workspace.data_ptr(), workspace.numel() * workspace.element_size(), st))
+    return dq, dk, dv, dth, dtw
 
 
 def device_status(reset: bool = True) -> int:

@@ -16,7 +16,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdera_relpos.so")
-SOURCES = ["dera_relpos.cu", "attention_w16.cu", "attention_w32.cu", "attention_w40.cu", "attention_w64.cu"]
+SOURCES = ["dera_relpos.cu", "attention_w16.cu", "attention_w32.cu", "attention_w40.cu", "attention_w64.cu",
+           "backward.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
                 "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

@@ -243,9 +243,6 @@ struct Cursor {
   }
 };
 
-// Warp-uniform wait result: tcgen05.ld/st are warp-collective, so a warp
-// either proceeds as a whole or stops as a whole.
-__device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xffffffffu, ok); }
 
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   const float lo = __uint_as_float(w << 16);
@@ -971,6 +968,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       };
       if (sg.full(n_kv)) {
         const float inv_l = 1.0f / l;
+        if (args.lse != nullptr && row_valid) args.lse[static_cast<size_t>(bh) * N + n] = m_used + log2f(l);
         #pragma unroll
         for (int h = 0; h < Dm::kAtoms; ++h) {
           #pragma unroll
@@ -1023,6 +1021,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const float mstar = fmaxf(ma.x, mb.x);
           const float fa = ex2_approx(ma.x - mstar), fb = ex2_approx(mb.x - mstar);
           const float inv_l = 1.0f / (fa * ma.y + fb * mb.y);
+          if (h == 0 && args.lse != nullptr && row_valid)
+            args.lse[static_cast<size_t>(bh) * N + n] = mstar + log2f(fa * ma.y + fb * mb.y);
           #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
             float v[16];

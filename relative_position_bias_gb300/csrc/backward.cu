@@ -1,0 +1,58 @@
+// Launchers of the backward kernels (csrc/backward.cuh): the two attention
+// kernels for every padded width and input dtype, then the bias and table
+// kernels.
+#include "backward.cuh"
+#include "launch.cuh"
+
+namespace dera {
+
+namespace {
+
+template <int WP, bool BF16>
+cudaError_t launch_bwd_attn(const BwdMaps& maps, const BwdArgs& args, cudaStream_t stream) {
+  using SM = BwdSmem<KeyTile<WP, 64>::BN>;
+  auto rows = relpos_bwd_rows_kernel<WP, BF16>;
+  auto cols = relpos_bwd_cols_kernel<WP, BF16>;
+  cudaError_t e = cudaFuncSetAttribute(rows, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(cols, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
+  if (e != cudaSuccess) return e;
+  const unsigned grid_rows = static_cast<unsigned>(args.BH) * static_cast<unsigned>(args.n_qtiles);
+  rows<<<grid_rows, kBwdThreads, SM::kAlloc, stream>>>(maps.q, maps.dout, maps.k, maps.v, args);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const unsigned grid_cols = static_cast<unsigned>(args.BH) * static_cast<unsigned>(args.n_kv);
+  cols<<<grid_cols, kBwdThreads, SM::kAlloc, stream>>>(maps.q, maps.dout, maps.k, maps.v, args);
+  return cudaGetLastError();
+}
+
+template <int WP>
+cudaError_t launch_bwd_attn_w(const BwdMaps& maps, const BwdArgs& args, cudaStream_t stream) {
+  return args.in_fmt == kBF16 ? launch_bwd_attn<WP, true>(maps, args, stream)
+                              : launch_bwd_attn<WP, false>(maps, args, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_backward(const BwdMaps& maps, const BwdArgs& args, int WP, cudaStream_t stream) {
+  cudaError_t e;
+  switch (WP) {
+    case 16: e = launch_bwd_attn_w<16>(maps, args, stream); break;
+    case 32: e = launch_bwd_attn_w<32>(maps, args, stream); break;
+    case 40: e = launch_bwd_attn_w<40>(maps, args, stream); break;
+    default: e = launch_bwd_attn_w<64>(maps, args, stream); break;
+  }
+  if (e != cudaSuccess) return e;
+  const int bias_bytes = bias_smem_floats(args.H, args.W) * static_cast<int>(sizeof(float));
+  e = cudaFuncSetAttribute(relpos_bwd_bias_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bias_bytes);
+  if (e != cudaSuccess) return e;
+  const unsigned blocks = static_cast<unsigned>(args.BH) * static_cast<unsigned>(args.n_qtiles);
+  relpos_bwd_bias_kernel<<<blocks, kBiasThreads, bias_bytes, stream>>>(args);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int total = (2 * args.H - 1 + 2 * args.W - 1) * 64;
+  relpos_bwd_tables_kernel<<<(total + 255) / 256, 256, 0, stream>>>(args, static_cast<int>(blocks));
+  return cudaGetLastError();
+}
+
+}  // namespace dera

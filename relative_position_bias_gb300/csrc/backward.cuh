@@ -1,0 +1,672 @@
+// Backward pass of global attention with decomposed relative-position bias
+// (head_dim 64), on tcgen05.
+//
+// The forward (vLLM PR #55629 page, sections 实现拆解 item 1 and 关键源码片段)
+// is out = softmax(Z) v with Z = scale q k^T + rel_h[n, kh(m)] + rel_w[n, kw(m)]
+// and rel_h, rel_w the projections of q on the tables.  The pages print no
+// backward; this is its chain-rule gradient.  With P = softmax(Z), an upstream
+// gradient dO, D[n] = dO[n] . out[n] and dZ = P * (dO v^T - D):
+//   dv = P^T dO,  dk = scale dZ^T q,  dq = scale dZ k + (bias part),
+//   drel_h[n, kh] = sum_kw dZ[n, (kh, kw)],  drel_w[n, kw] = sum_kh dZ[n, (kh, kw)],
+// and through the projection
+//   dq[n] += sum_kh drel_h[n, kh] T_h[qh - kh + H - 1] + sum_kw drel_w[n, kw] T_w[qw - kw + W - 1],
+//   dT_h[i] = sum over (b, n, kh) with qh - kh + H - 1 = i of drel_h[b, n, kh] q[b, n]  (same for T_w).
+// P is recomputed from the forward's base-2 log-sum-exp of each row:
+//   P[n, m] = 2^(Z[n, m] log2(e) - lse2[n]).
+//
+// Four kernels, in stream order (the projection kernel of the forward first
+// writes the compact rel_h, rel_w in fp32):
+//   relpos_bwd_rows   one CTA per (head, 128-row query tile), key tiles streamed:
+//                     S = q k^T and dP = dO v^T on the tensor core, P and dZ on
+//                     the softmax warps (one thread per query row), dq_s += dZ k
+//                     on the tensor core; writes D, scale * dq_s, drel_h, drel_w.
+//   relpos_bwd_cols   one CTA per (head, key tile), query tiles streamed:
+//                     S^T = k q^T and dP^T = v dO^T, P^T and dZ^T per key row,
+//                     dv += P^T dO and dk += dZ^T q accumulated in TMEM.
+//   relpos_bwd_bias   one CTA per (head, query tile): dq = dq_s + the bias part,
+//                     and this tile's share of dT_h, dT_w (a partial per CTA).
+//   relpos_bwd_tables sums the per-CTA partials in a fixed order.
+// Nothing is accumulated with atomics, so the result does not depend on the
+// order in which CTAs run.
+#pragma once
+#include <cfloat>
+
+#include "common.cuh"
+
+namespace dera {
+
+constexpr int kBwdThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 one thread per TMEM lane
+constexpr int kBwdStages = 3;      // K/V (rows kernel) or Q/dO (cols kernel) ring depth
+
+
+// Shared-memory layout shared by the two attention kernels (1024-byte aligned
+// operand tiles first).
+template <int BN>
+struct BwdSmem {
+  static constexpr int kTile = kTileBytes;                  // 128 rows x 128 B
+  static constexpr int kA = 0;                              // rows: Q tile; cols: K tile
+  static constexpr int kB = kA + kTile;                     // rows: dO tile; cols: V tile
+  static constexpr int kRing = kB + kTile;                  // stages of two 16 KB tiles
+  static constexpr int kStage = 2 * kTile;
+  static constexpr int kStaging = kRing + kBwdStages * kStage;
+  // rows kernel: per-thread bias rows, 128 x 65 floats; cols kernel: two
+  // buffers of per-query-tile bias, lse and D (see the cols kernel)
+  static constexpr int kStagingBytes = 2 * 128 * 76 * 4;
+  static constexpr int kBars = kStaging + kStagingBytes;
+  static constexpr int kNumBars = 24;
+  static constexpr int kMisc = kBars + kNumBars * 8;
+  static constexpr int kBytes = kMisc + 64;
+  static constexpr int kAlloc = kBytes + 1024;
+  static_assert(kAlloc <= 232448, "shared memory");
+};
+
+__device__ __forceinline__ float ld_in(const void* p, size_t i, int fmt) {
+  const unsigned short raw = reinterpret_cast<const unsigned short*>(p)[i];
+  if (fmt == kBF16) return __uint_as_float(static_cast<uint32_t>(raw) << 16);
+  return __half2float(__ushort_as_half(raw));
+}
+
+__device__ __forceinline__ uint32_t pack_in(float lo, float hi, int fmt) {
+  return fmt == kBF16 ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
+}
+
+// Stores 4 consecutive gradient values of a row in the gradient dtype.
+__device__ __forceinline__ void st_grad4(void* base, size_t i, float a, float b, float c, float d, int fmt) {
+  if (fmt == kF32) {
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + i) = make_float4(a, b, c, d);
+  } else {
+    const uint2 w = make_uint2(pack_in(a, b, fmt), pack_in(c, d, fmt));
+    *reinterpret_cast<uint2*>(reinterpret_cast<unsigned short*>(base) + i) = w;
+  }
+}
+
+// Barrier slots of the two attention kernels.
+enum : int {
+  kBwQFull = 0,                            // rows: Q and dO tiles; cols: K and V tiles
+  kBwRingFull = 1,                         // [kBwdStages]
+  kBwRingEmpty = kBwRingFull + kBwdStages,
+  kBwSFull = kBwRingEmpty + kBwdStages,    // S and dP (or S^T and dP^T) of the current tile in TMEM
+  kBwPFull = kBwSFull + 1,                 // softmax threads wrote dZ (and P^T), read S and dP (count 128)
+  kBwMmaDone = kBwPFull + 1,               // the products that read dZ (and P^T) of a tile are complete
+  kBwStg = kBwMmaDone + 1,                 // staging barrier of the softmax threads (count 128)
+  kBwCount = kBwStg + 1
+};
+static_assert(kBwCount <= BwdSmem<128>::kNumBars, "barrier slots");
+
+// Common set-up of the two attention kernels: barriers, TMEM (all 512
+// columns), and the aligned shared-memory base.
+struct BwdCta {
+  uint8_t* smem;
+  uint64_t* bars;
+  volatile int* abort_flag;
+  uint32_t tbase;
+};
+
+template <int BN>
+__device__ __forceinline__ BwdCta bwd_setup(uint8_t* smem_raw, int warp) {
+  using SM = BwdSmem<BN>;
+  BwdCta c;
+  const uint32_t raw_u = smem_u32(smem_raw);
+  c.smem = smem_raw + (((raw_u + 1023u) & ~1023u) - raw_u);
+  c.bars = reinterpret_cast<uint64_t*>(c.smem + SM::kBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(c.smem + SM::kMisc);
+  c.abort_flag = reinterpret_cast<volatile int*>(c.smem + SM::kMisc + 4);
+  if (threadIdx.x == 0) {
+    *c.abort_flag = 0;
+    mbar_init(&c.bars[kBwQFull], 1);
+    for (int s = 0; s < kBwdStages; ++s) {
+      mbar_init(&c.bars[kBwRingFull + s], 1);
+      mbar_init(&c.bars[kBwRingEmpty + s], 1);
+    }
+    mbar_init(&c.bars[kBwSFull], 1);
+    mbar_init(&c.bars[kBwPFull], kBlockM);
+    mbar_init(&c.bars[kBwMmaDone], 1);
+    mbar_init(&c.bars[kBwStg], kBlockM);
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  c.tbase = *tmem_slot;
+  return c;
+}
+
+__device__ __forceinline__ void bwd_teardown(uint32_t tbase, int warp) {
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Rows kernel: one CTA per (head, query tile); thread r of warps 2-5 owns
+// query row r (TMEM lane r).  TMEM columns: S [0, 128), dP [128, 256), dZ in
+// the input dtype as packed pairs [256, 320), the dZ k accumulator [320, 384).
+template <int WP, bool BF16>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                       const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       const BwdArgs args) {
+  using KT = KeyTile<WP, 64>;
+  constexpr int KHT = KT::KHT, BN = KT::BN, KS = kBwdStages;
+  using SM = BwdSmem<BN>;
+  constexpr int fmt = BF16 ? kBF16 : kF16;
+  extern __shared__ uint8_t smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const BwdCta cta = bwd_setup<BN>(smem_raw, warp);
+  uint8_t* smem = cta.smem;
+  uint64_t* bars = cta.bars;
+  volatile int* abort_flag = cta.abort_flag;
+  const uint32_t tbase = cta.tbase;
+  int* status = args.status;
+  const int bh = blockIdx.x / args.n_qtiles, qt = blockIdx.x - bh * args.n_qtiles;
+  const int n_kv = args.n_kv, H = args.H, W = args.W, N = args.N;
+  auto sK = [&](int s) { return smem + SM::kRing + s * SM::kStage; };
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(&bars[kBwQFull], 2 * kTileBytes);
+      tma_load_3d(smem + SM::kA, &tm_q, &bars[kBwQFull], 0, qt * kBlockM, bh);
+      tma_load_3d(smem + SM::kB, &tm_do, &bars[kBwQFull], 0, qt * kBlockM, bh);
+      for (int j = 0; j < n_kv; ++j) {
+        const int s = j % KS;
+        if (!mbar_wait(&bars[kBwRingEmpty + s], ((j / KS) & 1) ^ 1, abort_flag, status)) break;
+        mbar_arrive_expect_tx(&bars[kBwRingFull + s], 2 * BN * 128);
+        tma_load_4d(sK(s), &tm_k, &bars[kBwRingFull + s], 0, 0, j * KHT, bh);
+        tma_load_4d(sK(s) + kTileBytes, &tm_v, &bars[kBwRingFull + s], 0, 0, j * KHT, bh);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    constexpr uint32_t id_s = idesc_f16(kBlockM, BN, fmt, fmt, 0, 0);   // S, dP: both K-major
+    constexpr uint32_t id_dq = idesc_f16(kBlockM, 64, fmt, fmt, 0, 1);  // dZ k: the k tile N-major
+    const uint64_t d_q = sdesc_sw128(smem_u32(smem + SM::kA), 16, 1024);
+    const uint64_t d_do = sdesc_sw128(smem_u32(smem + SM::kB), 16, 1024);
+    const uint64_t d_ring = sdesc_sw128(smem_u32(smem + SM::kRing), 16, 1024);
+    constexpr uint32_t kStageStep = SM::kStage >> 4, kVOfs = kTileBytes >> 4;
+    auto issue_dq = [&](int jj) {
+      const int sp = jj % KS;
+      #pragma unroll
+      for (int k = 0; k < BN / 16; ++k)
+        umma_ts_w(tbase + 320, tbase + 256 + 8 * k, d_ring + sp * kStageStep + 128 * k, id_dq,
+                  (jj > 0 || k > 0) ? 1u : 0u);
+      umma_commit_w(&bars[kBwMmaDone]);
+      umma_commit_w(&bars[kBwRingEmpty + sp]);
+    };
+    bool ok = warp_all(mbar_wait(&bars[kBwQFull], 0, abort_flag, status));
+    for (int j = 0; ok && j < n_kv; ++j) {
+      const int s = j % KS;
+      ok = warp_all(mbar_wait(&bars[kBwRingFull + s], (j / KS) & 1, abort_flag, status));
+      if (!ok) break;
+      if (j > 0) {
+        // the softmax threads have read S(j-1), dP(j-1) and written dZ(j-1)
+        ok = warp_all(mbar_wait(&bars[kBwPFull], (j - 1) & 1, abort_flag, status));
+        if (!ok) break;
+        tc_fence_after();
+        issue_dq(j - 1);
+      }
+      tc_fence_after();
+      #pragma unroll
+      for (int k = 0; k < 4; ++k)
+        umma_ss_w(tbase + 0, d_q + 2 * k, d_ring + s * kStageStep + 2 * k, id_s, k > 0);
+      #pragma unroll
+      for (int k = 0; k < 4; ++k)
+        umma_ss_w(tbase + 128, d_do + 2 * k, d_ring + s * kStageStep + kVOfs + 2 * k, id_s, k > 0);
+      umma_commit_w(&bars[kBwSFull]);
+    }
+    if (ok && warp_all(mbar_wait(&bars[kBwPFull], (n_kv - 1) & 1, abort_flag, status))) {
+      tc_fence_after();
+      issue_dq(n_kv - 1);
+    }
+    // every product issued above completes before TMEM is released
+    umma_commit_w(&bars[kBwQFull]);
+    mbar_wait_budget(&bars[kBwQFull], 1, kWaitBudgetCycles);
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- softmax threads
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const int n = qt * kBlockM + r;
+    const bool row_valid = n < N;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tbase + lane_off, tdP = tS + 128, tdZ = tS + 256, tdQ = tS + 320;
+    const size_t row = static_cast<size_t>(bh) * N + (row_valid ? n : 0);
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    const float sl2 = args.scale_log2;
+    // this thread's bias row (base 2): rel_w in registers, rel_h in shared memory
+    float bw[WP];
+    #pragma unroll
+    for (int kw = 0; kw < WP; ++kw)
+      bw[kw] = (kw < W) ? (row_valid ? kLog2e * args.rel_w[row * W + kw] : 0.f) : NEG_INF;
+    float* bh_row = reinterpret_cast<float*>(smem + SM::kStaging) + r * 65;
+    const int Hpad = n_kv * KHT;
+    for (int kh = 0; kh < Hpad; ++kh)
+      bh_row[kh] = (kh < H) ? (row_valid ? kLog2e * args.rel_h[row * H + kh] : 0.f) : NEG_INF;
+    const float lse2 = row_valid ? args.lse[row] : 0.f;
+    // D = dO . out for this row (out in fp32 or in the input dtype)
+    float Dn = 0.f;
+    if (row_valid) {
+      for (int c = 0; c < 64; ++c) {
+        const float o = args.out_fmt == kF32 ? reinterpret_cast<const float*>(args.out)[row * 64 + c]
+                                              : ld_in(args.out, row * 64 + c, fmt);
+        Dn = fmaf(ld_in(args.dout, row * 64 + c, fmt), o, Dn);
+      }
+      args.D[row] = Dn;
+    }
+    float dRW[WP];
+    #pragma unroll
+    for (int kw = 0; kw < WP; ++kw) dRW[kw] = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      float bhv[KHT];
+      #pragma unroll
+      for (int g = 0; g < KHT; ++g) bhv[g] = bh_row[j * KHT + g];
+      ok = warp_all(mbar_wait(&bars[kBwSFull], j & 1, abort_flag, status));
+      if (!ok) break;
+      tc_fence_after();
+      if (j > 0) {
+        // dZ(j-1) has been read by its product before dZ(j) is written
+        ok = warp_all(mbar_wait(&bars[kBwMmaDone], (j - 1) & 1, abort_flag, status));
+        if (!ok) break;
+        tc_fence_after();
+      }
+      float dRH[KHT];
+      #pragma unroll
+      for (int g = 0; g < KHT; ++g) dRH[g] = 0.f;
+      #pragma unroll
+      for (int cb = 0; cb < BN; cb += 16) {
+        uint32_t us[16], up[16];
+        tmem_ld16(tS + cb, us);
+        tmem_ld16(tdP + cb, up);
+        tmem_wait_ld();
+        uint32_t pk[8];
+        #pragma unroll
+        for (int k = 0; k < 16; k += 2) {
+          const int col = cb + k;
+          const int g = col / WP, kw = col % WP;
+          const float x0 = fmaf(__uint_as_float(us[k]), sl2, bw[kw] + bhv[g]) - lse2;
+          const float x1 = fmaf(__uint_as_float(us[k + 1]), sl2, bw[kw + 1] + bhv[g]) - lse2;
+          float d0 = ex2_approx(x0) * (__uint_as_float(up[k]) - Dn);
+          float d1 = ex2_approx(x1) * (__uint_as_float(up[k + 1]) - Dn);
+          if (!row_valid) d0 = d1 = 0.f;
+          dRW[kw] += d0;
+          dRW[kw + 1] += d1;
+          dRH[g] += d0 + d1;
+          pk[k / 2] = pack_in(d0, d1, fmt);
+        }
+        tmem_st8(tdZ + cb / 2, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars[kBwPFull]);
+      if (row_valid) {
+        #pragma unroll
+        for (int g = 0; g < KHT; ++g)
+          if (j * KHT + g < H) args.drel_h[row * H + j * KHT + g] = dRH[g];
+      }
+    }
+    if (ok) ok = warp_all(mbar_wait(&bars[kBwMmaDone], (n_kv - 1) & 1, abort_flag, status));
+    if (ok) {
+      tc_fence_after();
+      uint32_t a[32], b[32];
+      tmem_ld32(tdQ, a);
+      tmem_ld32(tdQ + 32, b);
+      tmem_wait_ld();
+      if (row_valid) {
+        float4* dst = reinterpret_cast<float4*>(args.dq_s + row * 64);
+        const float sc = args.scale;
+        #pragma unroll
+        for (int c = 0; c < 8; ++c)
+          dst[c] = make_float4(sc * __uint_as_float(a[4 * c]), sc * __uint_as_float(a[4 * c + 1]),
+                               sc * __uint_as_float(a[4 * c + 2]), sc * __uint_as_float(a[4 * c + 3]));
+        #pragma unroll
+        for (int c = 0; c < 8; ++c)
+          dst[8 + c] = make_float4(sc * __uint_as_float(b[4 * c]), sc * __uint_as_float(b[4 * c + 1]),
+                                   sc * __uint_as_float(b[4 * c + 2]), sc * __uint_as_float(b[4 * c + 3]));
+        #pragma unroll
+        for (int kw = 0; kw < WP; ++kw)
+          if (kw < W) args.drel_w[row * W + kw] = dRW[kw];
+      }
+    }
+  }
+  bwd_teardown(tbase, warp);
+}
+
+
+// ---------------------------------------------------------------------------
+// Cols kernel: one CTA per (head, key tile of KHT grid rows); thread m of warps
+// 2-5 owns key slot m of the tile (TMEM lane m; slots past the tile's BN keys,
+// padded columns and padded grid rows compute nothing that is stored).  TMEM
+// columns: S^T [0, 128), dP^T [128, 256), P^T and dZ^T in the input dtype as
+// packed pairs [256, 320) and [320, 384), dv [384, 448), dk [448, 512).
+// Per query tile the softmax threads stage (cp.async, one tile ahead) the
+// tile's rel_w rows [128][W], its rel_h entries for this key tile's grid rows
+// [128][KHT], lse and D.
+template <int WP, bool BF16>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                       const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       const BwdArgs args) {
+  using KT = KeyTile<WP, 64>;
+  constexpr int KHT = KT::KHT, BN = KT::BN, KS = kBwdStages;
+  using SM = BwdSmem<BN>;
+  constexpr int fmt = BF16 ? kBF16 : kF16;
+  extern __shared__ uint8_t smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const BwdCta cta = bwd_setup<BN>(smem_raw, warp);
+  uint8_t* smem = cta.smem;
+  uint64_t* bars = cta.bars;
+  volatile int* abort_flag = cta.abort_flag;
+  const uint32_t tbase = cta.tbase;
+  int* status = args.status;
+  const int n_kv = args.n_kv, n_qt = args.n_qtiles, H = args.H, W = args.W, N = args.N;
+  const int bh = blockIdx.x / n_kv, j = blockIdx.x - bh * n_kv;
+  auto sQ = [&](int s) { return smem + SM::kRing + s * SM::kStage; };
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(&bars[kBwQFull], 2 * BN * 128);
+      tma_load_4d(smem + SM::kA, &tm_k, &bars[kBwQFull], 0, 0, j * KHT, bh);
+      tma_load_4d(smem + SM::kB, &tm_v, &bars[kBwQFull], 0, 0, j * KHT, bh);
+      for (int i = 0; i < n_qt; ++i) {
+        const int s = i % KS;
+        if (!mbar_wait(&bars[kBwRingEmpty + s], ((i / KS) & 1) ^ 1, abort_flag, status)) break;
+        mbar_arrive_expect_tx(&bars[kBwRingFull + s], 2 * kTileBytes);
+        tma_load_3d(sQ(s), &tm_q, &bars[kBwRingFull + s], 0, i * kBlockM, bh);
+        tma_load_3d(sQ(s) + kTileBytes, &tm_do, &bars[kBwRingFull + s], 0, i * kBlockM, bh);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    constexpr uint32_t id_s = idesc_f16(kBlockM, kBlockM, fmt, fmt, 0, 0);  // S^T, dP^T: both K-major
+    constexpr uint32_t id_acc = idesc_f16(kBlockM, 64, fmt, fmt, 0, 1);     // P^T dO, dZ^T q: N-major tiles
+    const uint64_t d_k = sdesc_sw128(smem_u32(smem + SM::kA), 16, 1024);
+    const uint64_t d_v = sdesc_sw128(smem_u32(smem + SM::kB), 16, 1024);
+    const uint64_t d_ring = sdesc_sw128(smem_u32(smem + SM::kRing), 16, 1024);
+    constexpr uint32_t kStageStep = SM::kStage >> 4, kDoOfs = kTileBytes >> 4;
+    auto issue_acc = [&](int ii) {
+      const int sp = ii % KS;
+      #pragma unroll
+      for (int k = 0; k < kBlockM / 16; ++k) {
+        const uint32_t acc = (ii > 0 || k > 0) ? 1u : 0u;
+        umma_ts_w(tbase + 384, tbase + 256 + 8 * k, d_ring + sp * kStageStep + kDoOfs + 128 * k, id_acc, acc);
+        umma_ts_w(tbase + 448, tbase + 320 + 8 * k, d_ring + sp * kStageStep + 128 * k, id_acc, acc);
+      }
+      umma_commit_w(&bars[kBwMmaDone]);
+      umma_commit_w(&bars[kBwRingEmpty + sp]);
+    };
+    bool ok = warp_all(mbar_wait(&bars[kBwQFull], 0, abort_flag, status));
+    for (int i = 0; ok && i < n_qt; ++i) {
+      const int s = i % KS;
+      ok = warp_all(mbar_wait(&bars[kBwRingFull + s], (i / KS) & 1, abort_flag, status));
+      if (!ok) break;
+      if (i > 0) {
+        ok = warp_all(mbar_wait(&bars[kBwPFull], (i - 1) & 1, abort_flag, status));
+        if (!ok) break;
+        tc_fence_after();
+        issue_acc(i - 1);
+      }
+      tc_fence_after();
+      #pragma unroll
+      for (int k = 0; k < 4; ++k)
+        umma_ss_w(tbase + 0, d_k + 2 * k, d_ring + s * kStageStep + 2 * k, id_s, k > 0);
+      #pragma unroll
+      for (int k = 0; k < 4; ++k)
+        umma_ss_w(tbase + 128, d_v + 2 * k, d_ring + s * kStageStep + kDoOfs + 2 * k, id_s, k > 0);
+      umma_commit_w(&bars[kBwSFull]);
+    }
+    if (ok && warp_all(mbar_wait(&bars[kBwPFull], (n_qt - 1) & 1, abort_flag, status))) {
+      tc_fence_after();
+      issue_acc(n_qt - 1);
+    }
+    umma_commit_w(&bars[kBwQFull]);
+    mbar_wait_budget(&bars[kBwQFull], 1, kWaitBudgetCycles);
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- softmax threads
+    const int wq = warp & 3;
+    const int m = wq * 32 + lane;          // key slot of the tile
+    const int t = m;                       // index among the 128 staging threads
+    const int g = m / WP, kw = m % WP;
+    const int kh = j * KHT + g;
+    const bool key_valid = m < BN && kw < W && kh < H;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tbase + lane_off, tdP = tS + 128, tP = tS + 256, tdZ = tS + 320, tdV = tS + 384,
+                   tdK = tS + 448;
+    const float sl2 = args.scale_log2;
+    float* stage_base = reinterpret_cast<float*>(smem + SM::kStaging);
+    constexpr int kBufFloats = 128 * 76;
+    // buffer b: rel_w [128][W] at 0, rel_h [128][KHT] at 128*64, lse at 128*72, D at 128*73
+    auto stage = [&](int i, int b) {
+      float* buf = stage_base + b * kBufFloats;
+      const int n0 = i * kBlockM;
+      const int rows = min(kBlockM, N - n0);
+      const size_t base = static_cast<size_t>(bh) * N + n0;
+      for (int e = t; e < kBlockM * W; e += kBlockM) {
+        const int rr = e / W;
+        cp_async4(buf + e, args.rel_w + (rr < rows ? base * W + e : 0), rr < rows ? 4u : 0u);
+      }
+      for (int e = t; e < kBlockM * KHT; e += kBlockM) {
+        const int rr = e / KHT, gg = e - rr * KHT, khh = j * KHT + gg;
+        const bool v = rr < rows && khh < H;
+        cp_async4(buf + 128 * 64 + e, args.rel_h + (v ? (base + rr) * H + khh : 0), v ? 4u : 0u);
+      }
+      cp_async4(buf + 128 * 72 + t, args.lse + (t < rows ? base + t : 0), t < rows ? 4u : 0u);
+      cp_async4(buf + 128 * 73 + t, args.D + (t < rows ? base + t : 0), t < rows ? 4u : 0u);
+    };
+    uint32_t stg_phase = 0;
+    auto group_sync = [&]() -> bool {
+      mbar_arrive(&bars[kBwStg]);
+      const bool w = mbar_wait(&bars[kBwStg], stg_phase & 1, abort_flag, status);
+      ++stg_phase;
+      return warp_all(w);
+    };
+    bool ok = true;
+    stage(0, 0);
+    for (int i = 0; i < n_qt; ++i) {
+      // this tile's staging has landed everywhere, and every thread is done
+      // with the previous tile's buffer, which the next prefetch overwrites
+      cp_async_wait_all();
+      ok = group_sync();
+      if (!ok) break;
+      if (i + 1 < n_qt) stage(i + 1, (i + 1) & 1);
+      const float* buf = stage_base + (i & 1) * kBufFloats;
+      const float* rw = buf;
+      const float* rh = buf + 128 * 64;
+      const float* lse = buf + 128 * 72;
+      const float* Dv = buf + 128 * 73;
+      const int rows = min(kBlockM, N - i * kBlockM);
+      ok = warp_all(mbar_wait(&bars[kBwSFull], i & 1, abort_flag, status));
+      if (!ok) break;
+      tc_fence_after();
+      if (i > 0) {
+        ok = warp_all(mbar_wait(&bars[kBwMmaDone], (i - 1) & 1, abort_flag, status));
+        if (!ok) break;
+        tc_fence_after();
+      }
+      #pragma unroll 1
+      for (int cb = 0; cb < kBlockM; cb += 16) {
+        uint32_t us[16], up[16];
+        tmem_ld16(tS + cb, us);
+        tmem_ld16(tdP + cb, up);
+        tmem_wait_ld();
+        uint32_t pp[8], pz[8];
+        #pragma unroll
+        for (int k = 0; k < 16; k += 2) {
+          float p2[2], z2[2];
+          #pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int nn = cb + k + h;
+            const bool v = key_valid && nn < rows;
+            const float b = v ? (rh[nn * KHT + g] + rw[nn * W + kw]) : 0.f;
+            const float x = fmaf(__uint_as_float(us[k + h]), sl2, fmaf(b, kLog2e, -lse[nn]));
+            const float p = v ? ex2_approx(x) : 0.f;
+            p2[h] = p;
+            z2[h] = v ? p * (__uint_as_float(up[k + h]) - Dv[nn]) : 0.f;
+          }
+          pp[k / 2] = pack_in(p2[0], p2[1], fmt);
+          pz[k / 2] = pack_in(z2[0], z2[1], fmt);
+        }
+        tmem_st8(tP + cb / 2, pp);
+        tmem_st8(tdZ + cb / 2, pz);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars[kBwPFull]);
+    }
+    cp_async_wait_all();
+    if (ok) ok = warp_all(mbar_wait(&bars[kBwMmaDone], (n_qt - 1) & 1, abort_flag, status));
+    if (ok) {
+      tc_fence_after();
+      uint32_t a[32];
+      const size_t tok = static_cast<size_t>(bh) * N + static_cast<size_t>(kh) * W + kw;
+      const float sc = args.scale;
+      // tcgen05.ld is warp-collective: every lane loads, lanes with a key store
+      #pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        tmem_ld32(tdV + 32 * h, a);
+        tmem_wait_ld();
+        if (key_valid) {
+          #pragma unroll
+          for (int c = 0; c < 8; ++c)
+            st_grad4(args.dv, tok * 64 + 32 * h + 4 * c, __uint_as_float(a[4 * c]), __uint_as_float(a[4 * c + 1]),
+                     __uint_as_float(a[4 * c + 2]), __uint_as_float(a[4 * c + 3]), args.grad_fmt);
+        }
+        tmem_ld32(tdK + 32 * h, a);
+        tmem_wait_ld();
+        if (key_valid) {
+          #pragma unroll
+          for (int c = 0; c < 8; ++c)
+            st_grad4(args.dk, tok * 64 + 32 * h + 4 * c, sc * __uint_as_float(a[4 * c]),
+                     sc * __uint_as_float(a[4 * c + 1]), sc * __uint_as_float(a[4 * c + 2]),
+                     sc * __uint_as_float(a[4 * c + 3]), args.grad_fmt);
+        }
+      }
+    }
+  }
+  bwd_teardown(tbase, warp);
+}
+
+// ---------------------------------------------------------------------------
+// Bias kernel: one CTA of 256 threads per (head, query tile).  Adds the bias
+// part of dq to dq_s and writes dq; writes this tile's partial table gradients.
+constexpr int kBiasThreads = 256;
+constexpr int kTStride = 65;   // floats per staged table row (odd: rows start in different banks)
+
+__host__ __device__ constexpr int bias_smem_floats(int H, int W) {
+  return (2 * H - 1 + 2 * W - 1) * kTStride + 128 * (H + 1) + 128 * (W + 1) + 128 * 65 + 2 * 128;
+}
+
+__global__ void __launch_bounds__(kBiasThreads, 1) relpos_bwd_bias_kernel(const BwdArgs args) {
+  extern __shared__ float fsm[];
+  const int H = args.H, W = args.W, N = args.N;
+  const int bh = blockIdx.x / args.n_qtiles, qt = blockIdx.x - bh * args.n_qtiles;
+  const int n0 = qt * kBlockM;
+  const int rows = min(kBlockM, N - n0);
+  const int LH = 2 * H - 1, LW = 2 * W - 1;
+  float* Th = fsm;
+  float* Tw = Th + LH * kTStride;
+  float* dRh = Tw + LW * kTStride;                 // [128][H + 1]
+  float* dRw = dRh + 128 * (H + 1);                // [128][W + 1]
+  float* Qf = dRw + 128 * (W + 1);                 // [128][65]
+  int* qhv = reinterpret_cast<int*>(Qf + 128 * 65);
+  int* qwv = qhv + 128;
+  const int t = threadIdx.x;
+  const size_t base = static_cast<size_t>(bh) * N + n0;
+  for (int e = t; e < LH * 64; e += kBiasThreads) Th[(e >> 6) * kTStride + (e & 63)] = ld_in(args.th, e, args.in_fmt);
+  for (int e = t; e < LW * 64; e += kBiasThreads) Tw[(e >> 6) * kTStride + (e & 63)] = ld_in(args.tw, e, args.in_fmt);
+  for (int e = t; e < 128 * H; e += kBiasThreads) {
+    const int rr = e / H, c = e - rr * H;
+    dRh[rr * (H + 1) + c] = rr < rows ? args.drel_h[base * H + e] : 0.f;
+  }
+  for (int e = t; e < 128 * W; e += kBiasThreads) {
+    const int rr = e / W, c = e - rr * W;
+    dRw[rr * (W + 1) + c] = rr < rows ? args.drel_w[base * W + e] : 0.f;
+  }
+  for (int e = t; e < 128 * 64; e += kBiasThreads) {
+    const int rr = e >> 6;
+    Qf[rr * 65 + (e & 63)] = rr < rows ? ld_in(args.q, base * 64 + e, args.in_fmt) : 0.f;
+  }
+  if (t < 128) {
+    const int n = n0 + t;
+    qhv[t] = n / W;
+    qwv[t] = n - (n / W) * W;
+  }
+  __syncthreads();
+  // dq = dq_s + sum_kh drel_h T_h[qh - kh + H - 1] + sum_kw drel_w T_w[qw - kw + W - 1]
+  {
+    const int rr = t >> 1, c0 = (t & 1) * 32;
+    if (rr < rows) {
+      const int qh = qhv[rr], qw = qwv[rr];
+      float acc[32];
+      const float* src = args.dq_s + (base + rr) * 64 + c0;
+      #pragma unroll
+      for (int c = 0; c < 32; ++c) acc[c] = src[c];
+      for (int kh = 0; kh < H; ++kh) {
+        const float w = dRh[rr * (H + 1) + kh];
+        const float* tr = Th + (qh - kh + H - 1) * kTStride + c0;
+        #pragma unroll
+        for (int c = 0; c < 32; ++c) acc[c] = fmaf(w, tr[c], acc[c]);
+      }
+      for (int kw = 0; kw < W; ++kw) {
+        const float w = dRw[rr * (W + 1) + kw];
+        const float* tr = Tw + (qw - kw + W - 1) * kTStride + c0;
+        #pragma unroll
+        for (int c = 0; c < 32; ++c) acc[c] = fmaf(w, tr[c], acc[c]);
+      }
+      #pragma unroll
+      for (int c = 0; c < 32; c += 4)
+        st_grad4(args.dq, (base + rr) * 64 + c0 + c, acc[c], acc[c + 1], acc[c + 2], acc[c + 3], args.grad_fmt);
+    }
+  }
+  // partial table gradients of this tile: part_h[i][c] = sum over rows with
+  // kh = qh - i + H - 1 in range of drel_h[row][kh] q[row][c] (and the same for w)
+  float* part = args.parts + static_cast<size_t>(blockIdx.x) * (LH + LW) * 64;
+  for (int o = t; o < (LH + LW) * 64; o += kBiasThreads) {
+    const int i = o >> 6, c = o & 63;
+    float acc = 0.f;
+    if (i < LH) {
+      for (int rr = 0; rr < rows; ++rr) {
+        const int kh = qhv[rr] - i + H - 1;
+        if (kh >= 0 && kh < H) acc = fmaf(dRh[rr * (H + 1) + kh], Qf[rr * 65 + c], acc);
+      }
+    } else {
+      const int iw = i - LH;
+      for (int rr = 0; rr < rows; ++rr) {
+        const int kw = qwv[rr] - iw + W - 1;
+        if (kw >= 0 && kw < W) acc = fmaf(dRw[rr * (W + 1) + kw], Qf[rr * 65 + c], acc);
+      }
+    }
+    part[o] = acc;
+  }
+}
+
+// Tables kernel: dT = sum of the per-tile partials, in block order.
+__global__ void relpos_bwd_tables_kernel(const BwdArgs args, int n_blocks) {
+  const int LH = 2 * args.H - 1, LW = 2 * args.W - 1;
+  const int total = (LH + LW) * 64;
+  const int o = blockIdx.x * blockDim.x + threadIdx.x;
+  if (o >= total) return;
+  float acc = 0.f;
+  for (int b = 0; b < n_blocks; ++b) acc += args.parts[static_cast<size_t>(b) * total + o];
+  if (o < LH * 64) args.dth[o] = acc;
+  else args.dtw[o - LH * 64] = acc;
+}
+
+}  // namespace dera

@@ -60,6 +60,7 @@ struct AttnArgs {
   int in_fmt;          // kF16 | kBF16
   int bias_fmt;        // kF32 | kBF16 | kF16 (compact entry)
   int out_fmt;         // kF32 | in_fmt
+  float* lse;          // [BH, N] base-2 log-sum-exp of each row's logits, or null
 };
 
 struct ProjArgs {
@@ -69,6 +70,37 @@ struct ProjArgs {
   int BH, H, W, N;
   int bias_fmt;        // kF32 | kBF16 | kF16
 };
+
+// Arguments of the backward kernels (csrc/backward.cuh).
+struct BwdArgs {
+  const float* rel_h;   // [BH, N, H] compact bias (fp32, natural units)
+  const float* rel_w;   // [BH, N, W]
+  const float* lse;     // [BH, N] base-2 log-sum-exp of each row's logits (forward)
+  const void* out;      // [BH, N, 64] forward output (input dtype)
+  const void* dout;     // [BH, N, 64] upstream gradient (input dtype)
+  float* D;             // [BH, N] dO . out per row (rows kernel writes, cols kernel reads)
+  float* dq_s;          // [BH, N, 64] scale * dZ k (rows kernel)
+  float* drel_h;        // [BH, N, H]
+  float* drel_w;        // [BH, N, W]
+  void* dq;             // [BH, N, 64] grad dtype (bias kernel)
+  void* dk;             // [BH, N, 64] grad dtype (cols kernel)
+  void* dv;             // [BH, N, 64]
+  const void* th;       // [2H-1, 64] table (input dtype)
+  const void* tw;       // [2W-1, 64]
+  const void* q;        // [BH, N, 64] (bias kernel reads rows directly)
+  float* parts;         // [n_qblocks][(2H-1) + (2W-1)][64] per-CTA table-gradient partials
+  float* dth;           // [2H-1, 64] fp32
+  float* dtw;           // [2W-1, 64] fp32
+  int* status;
+  int BH, H, W, N;
+  int n_qtiles, n_kv;
+  float scale, scale_log2;
+  int in_fmt, out_fmt, grad_fmt;
+};
+
+// Warp-uniform wait result: tcgen05.ld/st are warp-collective, so a warp
+// either proceeds as a whole or stops as a whole.
+__device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xffffffffu, ok); }
 
 __device__ __forceinline__ float load_elem(const void* p, size_t i, int fmt) {
   if (fmt == kF32) return __ldg(reinterpret_cast<const float*>(p) + i);

@@ -268,10 +268,34 @@ dera_status current_device(int* dev) {
     if (s_ != DERA_OK) return s_;   \
   } while (0)
 
+// Workspace of the backward: fp32 regions, each 256-byte aligned.
+struct BwdLayout {
+  size_t rel_h, rel_w, D, dq_s, drel_h, drel_w, parts, total;
+  int n_qtiles;
+  BwdLayout(int BH, int H, int W) {
+    const size_t rows = static_cast<size_t>(BH) * H * W;
+    n_qtiles = (H * W + kBlockM - 1) / kBlockM;
+    size_t o = 0;
+    auto take = [&](size_t floats) {
+      const size_t at = o;
+      o += align256(floats * sizeof(float));
+      return at;
+    };
+    rel_h = take(rows * H);
+    rel_w = take(rows * W);
+    D = take(rows);
+    dq_s = take(rows * 64);
+    drel_h = take(rows * H);
+    drel_w = take(rows * W);
+    parts = take(static_cast<size_t>(BH) * n_qtiles * (2 * H - 1 + 2 * W - 1) * 64);
+    total = o;
+  }
+};
+
 dera_status run_attention(const void* q, const void* k, const void* v, const void* a, const void* b, void* out,
                           int BH, int H, int W, int d, float scale, dera_dtype in_dtype, dera_dtype bias_dtype,
                           dera_dtype out_dtype, bool fused, void* workspace, size_t workspace_bytes,
-                          void* stream) {
+                          void* stream, float* lse = nullptr) {
   int dev = 0;
   DERA_TRY(current_device(&dev));
   const int N = H * W;
@@ -312,6 +336,7 @@ dera_status run_attention(const void* q, const void* k, const void* v, const voi
   args.in_fmt = fmt_of(in_dtype);
   args.bias_fmt = fmt_of(bias_dtype);
   args.out_fmt = fmt_of(out_dtype);
+  args.lse = lse;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (plan.split) {
     args.counters = static_cast<unsigned long long*>(workspace);
@@ -452,6 +477,129 @@ dera_status dera_relpos_fused(const void* q, const void* k, const void* v, const
   }
   return run_attention(q, k, v, rel_pos_h, rel_pos_w, out, BH, H, W, head_dim, scale, in_dtype, in_dtype, out_dtype, true,
                        workspace, workspace_bytes, stream);
+}
+
+dera_status dera_relpos_fused_lse(const void* q, const void* k, const void* v, const void* rel_pos_h,
+                                  const void* rel_pos_w, void* out, float* lse, int BH, int H, int W,
+                                  int head_dim, float scale, dera_dtype in_dtype, dera_dtype out_dtype,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  DERA_TRY(check_shape(BH, H, W, head_dim));
+  if (!is16(in_dtype) || !(out_dtype == DERA_F32 || out_dtype == in_dtype)) return DERA_ERR_DTYPE;
+  if (BH == 0) return DERA_OK;
+  DERA_TRY(check_host({q, k, v, rel_pos_h, rel_pos_w, out, lse}));
+  int dev = 0;
+  DERA_TRY(current_device(&dev));
+  for (const void* p : {q, k, v, rel_pos_h, rel_pos_w, static_cast<const void*>(out), static_cast<const void*>(lse)})
+    DERA_TRY(check_ptr(p, dev));
+  if (workspace) {
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return DERA_ERR_ALIGN;
+    DERA_TRY(check_ptr(workspace, dev));
+  }
+  return run_attention(q, k, v, rel_pos_h, rel_pos_w, out, BH, H, W, head_dim, scale, in_dtype, in_dtype, out_dtype, true,
+                       workspace, workspace_bytes, stream, lse);
+}
+
+dera_status dera_relpos_backward_workspace_size(int BH, int H, int W, int head_dim, size_t* bytes) {
+  if (!bytes) return DERA_ERR_NULL;
+  DERA_TRY(check_shape(BH, H, W, head_dim));
+  if (head_dim != 64) return DERA_ERR_HEAD_DIM;
+  *bytes = BwdLayout(BH, H, W).total;
+  return DERA_OK;
+}
+
+dera_status dera_relpos_fused_backward(const void* q, const void* k, const void* v, const void* rel_pos_h,
+                                       const void* rel_pos_w, const void* out, const float* lse,
+                                       const void* dout, void* dq, void* dk, void* dv, float* drel_pos_h,
+                                       float* drel_pos_w, int BH, int H, int W, int head_dim, float scale,
+                                       dera_dtype in_dtype, dera_dtype out_dtype, dera_dtype grad_dtype,
+                                       void* workspace, size_t workspace_bytes, void* stream) {
+  DERA_TRY(check_shape(BH, H, W, head_dim));
+  if (head_dim != 64) return DERA_ERR_HEAD_DIM;
+  if (!is16(in_dtype) || !(out_dtype == DERA_F32 || out_dtype == in_dtype) ||
+      !(grad_dtype == DERA_F32 || grad_dtype == in_dtype))
+    return DERA_ERR_DTYPE;
+  DERA_TRY(check_host({q, k, v, rel_pos_h, rel_pos_w, out, lse, dout, dq, dk, dv, drel_pos_h, drel_pos_w}));
+  int dev = 0;
+  DERA_TRY(current_device(&dev));
+  const BwdLayout L(BH, H, W);
+  if (BH == 0) {
+    // no rows: the table gradients are zero
+    const size_t th_bytes = static_cast<size_t>(2 * H - 1) * 64 * sizeof(float);
+    const size_t tw_bytes = static_cast<size_t>(2 * W - 1) * 64 * sizeof(float);
+    cudaStream_t s0 = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(drel_pos_h, 0, th_bytes, s0) != cudaSuccess ||
+        cudaMemsetAsync(drel_pos_w, 0, tw_bytes, s0) != cudaSuccess)
+      return DERA_ERR_CUDA;
+    return DERA_OK;
+  }
+  if (!workspace || workspace_bytes < L.total) return DERA_ERR_SCRATCH;
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return DERA_ERR_ALIGN;
+  for (const void* p : {q, k, v, rel_pos_h, rel_pos_w, out, static_cast<const void*>(lse), dout,
+                        static_cast<const void*>(dq), static_cast<const void*>(dk), static_cast<const void*>(dv),
+                        static_cast<const void*>(drel_pos_h), static_cast<const void*>(drel_pos_w),
+                        static_cast<const void*>(workspace)})
+    DERA_TRY(check_ptr(p, dev));
+  const int N = H * W;
+  char* ws = static_cast<char*>(workspace);
+  float* rel_h = reinterpret_cast<float*>(ws + L.rel_h);
+  float* rel_w = reinterpret_cast<float*>(ws + L.rel_w);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* st = status_ptr(dev);
+  if (!st) return DERA_ERR_CUDA;
+  // the compact bias, fp32, by the forward's projection kernel
+  {
+    CUtensorMap mq, mh, mw;
+    if (!map_rows(&mq, q, in_dtype, BH, N, 64) || !map_table(&mh, rel_pos_h, in_dtype, H, 64) ||
+        !map_table(&mw, rel_pos_w, in_dtype, W, 64))
+      return DERA_ERR_CUDA;
+    ProjArgs pa;
+    pa.rel_h = rel_h;
+    pa.rel_w = rel_w;
+    pa.status = st;
+    pa.BH = BH;
+    pa.H = H;
+    pa.W = W;
+    pa.N = N;
+    pa.bias_fmt = kF32;
+    if (launch_project(mq, mh, mw, pa, fmt_of(in_dtype), 64, sm_count(dev), s) != cudaSuccess) return DERA_ERR_CUDA;
+  }
+  const int WP = padded_width(W), KHT = rows_per_tile(WP, 64);
+  BwdMaps maps;
+  if (!map_rows(&maps.q, q, in_dtype, BH, N, 64) || !map_rows(&maps.dout, dout, in_dtype, BH, N, 64) ||
+      !map_keys(&maps.k, k, in_dtype, BH, H, W, 64, WP, KHT) || !map_keys(&maps.v, v, in_dtype, BH, H, W, 64, WP, KHT))
+    return DERA_ERR_CUDA;
+  BwdArgs a;
+  a.rel_h = rel_h;
+  a.rel_w = rel_w;
+  a.lse = lse;
+  a.out = out;
+  a.dout = dout;
+  a.D = reinterpret_cast<float*>(ws + L.D);
+  a.dq_s = reinterpret_cast<float*>(ws + L.dq_s);
+  a.drel_h = reinterpret_cast<float*>(ws + L.drel_h);
+  a.drel_w = reinterpret_cast<float*>(ws + L.drel_w);
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.th = rel_pos_h;
+  a.tw = rel_pos_w;
+  a.q = q;
+  a.parts = reinterpret_cast<float*>(ws + L.parts);
+  a.dth = drel_pos_h;
+  a.dtw = drel_pos_w;
+  a.status = st;
+  a.BH = BH;
+  a.H = H;
+  a.W = W;
+  a.N = N;
+  a.n_qtiles = L.n_qtiles;
+  a.n_kv = (H + KHT - 1) / KHT;
+  a.scale = scale;
+  a.scale_log2 = scale * kLog2e;
+  a.in_fmt = fmt_of(in_dtype);
+  a.out_fmt = fmt_of(out_dtype);
+  a.grad_fmt = fmt_of(grad_dtype);
+  return launch_backward(maps, a, WP, s) == cudaSuccess ? DERA_OK : DERA_ERR_CUDA;
 }
 
 dera_status dera_relpos_device_status(int* status, int reset) {

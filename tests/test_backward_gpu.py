@@ -1,0 +1,121 @@
+"""The backward (dera_relpos_fused_backward) and the training forward (dera_relpos_fused_lse)
+against the CPU float64 oracle's chain-rule gradient.
+
+Tolerance (derived, then confirmed by the margins printed at the end of the run): P and dZ enter
+the tensor-core products rounded to the input dtype (relative 2^-9 for bf16, 2^-11 for fp16) with
+fp32 accumulation, so each gradient carries a relative rounding error of that order, amplified where
+a sum cancels.  The checks are rel-L2 <= 1e-2 (bf16) / 4e-3 (fp16) and a max-abs error of at most
+3e-2 (bf16) / 1e-2 (fp16) of the largest reference value, per gradient.  The table gradients sum
+over every row of every head, in fp32.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import relative_position_bias_gb300 as rpb
+from conftest import record_margin
+from relative_position_bias_gb300 import build as rbuild
+from relative_position_bias_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.bfloat16: (1e-2, 3e-2), torch.float16: (4e-3, 1e-2)}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    rbuild.build()
+    rpb.load_library()
+    yield
+    assert rpb.device_status() == 0, "a kernel hit its bounded-wait budget"
+
+
+def make_case(BH, H, W, dtype, sq=1.0, sk=1.0, sv=1.0, st=0.5, seed=0):
+    g = torch.Generator().manual_seed(seed)
+    N = H * W
+    x = {"q": sq * torch.randn(BH, N, 64, generator=g), "k": sk * torch.randn(BH, N, 64, generator=g),
+         "v": sv * torch.randn(BH, N, 64, generator=g), "rel_pos_h": st * torch.randn(2 * H - 1, 64, generator=g),
+         "rel_pos_w": st * torch.randn(2 * W - 1, 64, generator=g), "dout": torch.randn(BH, N, 64, generator=g)}
+    return {n: t.to(dtype) for n, t in x.items()}
+
+
+CASES = {
+    # name: (BH, H, W, dtype, sigma_q, sigma_k)
+    "grid16-bf16": (2, 16, 16, torch.bfloat16, 1.0, 1.0),
+    "global64-bf16": (2, 64, 64, torch.bfloat16, 0.5, 0.5),
+    "ragged40-f16": (3, 40, 40, torch.float16, 2.0, 2.0),
+    "window14-bf16": (6, 14, 14, torch.bfloat16, 1.0, 1.0),
+    "odd7x30-f16": (2, 7, 30, torch.float16, 1.0, 1.0),
+    "tall33x9-bf16": (2, 33, 9, torch.bfloat16, 1.0, 1.0),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_backward_matches_oracle(name):
+    BH, H, W, dtype, sq, sk = CASES[name]
+    x = make_case(BH, H, W, dtype, sq=sq, sk=sk, seed=sorted(CASES).index(name))
+    d = {n: t.cuda() for n, t in x.items()}
+    scale = 0.125
+    out, lse = rpb.fused_lse(d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], H, W, scale,
+                             out_dtype=torch.float32)
+    grads = rpb.fused_backward(d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], out, lse, d["dout"], H, W,
+                               scale)
+    torch.cuda.synchronize()
+    f = {n: I.to_f64(t) for n, t in x.items()}
+    want = oracle.fused_backward(f["q"], f["k"], f["v"], f["rel_pos_h"], f["rel_pos_w"], H, W, scale, f["dout"])
+    rl2_tol, max_tol = TOL[dtype]
+    for gname, got, ref in zip(["dq", "dk", "dv", "drel_pos_h", "drel_pos_w"], grads, want):
+        g = got.double().cpu().numpy()
+        assert np.isfinite(g).all(), gname
+        err = np.abs(g - ref).max()
+        scale_ref = np.abs(ref).max()
+        rl2 = np.linalg.norm(g - ref) / max(np.linalg.norm(ref), 1e-30)
+        record_margin(f"backward {name} {gname} (max-abs / max|ref|)", err / scale_ref, rl2,
+                      f"{max_tol:g} / {rl2_tol:g}")
+        assert rl2 <= rl2_tol, f"{gname}: rel-L2 {rl2:.3e}"
+        assert err <= max_tol * scale_ref, f"{gname}: max-abs {err:.3e} of max {scale_ref:.3e}"
+
+
+@pytest.mark.parametrize("name", ["grid16-bf16", "ragged40-f16", "window14-bf16"])
+def test_forward_lse(name):
+    """The training forward's out is the plain forward's, bit for bit, and lse is the oracle's."""
+    BH, H, W, dtype, sq, sk = CASES[name]
+    x = make_case(BH, H, W, dtype, sq=sq, sk=sk, seed=3)
+    d = {n: t.cuda() for n, t in x.items()}
+    scale = 0.125
+    out, lse = rpb.fused_lse(d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], H, W, scale,
+                             out_dtype=torch.float32)
+    plain = rpb.fused(d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], H, W, scale, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(out, plain)
+    f = {n: I.to_f64(t) for n, t in x.items()}
+    rh, rw = oracle.project(f["q"], f["rel_pos_h"], f["rel_pos_w"], H, W)
+    want = oracle.lse2(f["q"], f["k"], rh, rw, H, W, scale)
+    err = np.abs(lse.double().cpu().numpy() - want).max()
+    record_margin(f"forward lse {name}", err, 0.0, "1e-3 (base 2)")
+    assert err <= 1e-3, f"lse max-abs {err:.3e}"
+
+
+def test_backward_is_deterministic():
+    """No atomics: two calls give bit-identical gradients."""
+    BH, H, W, dtype, sq, sk = CASES["global64-bf16"]
+    x = make_case(BH, H, W, dtype, sq=sq, sk=sk, seed=5)
+    d = {n: t.cuda() for n, t in x.items()}
+    out, lse = rpb.fused_lse(d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], H, W, 0.125)
+    a = rpb.fused_backward(d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], out, lse, d["dout"], H, W, 0.125,
+                           grad_dtype=torch.bfloat16)
+    b = rpb.fused_backward(d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], out, lse, d["dout"], H, W, 0.125,
+                           grad_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    for x1, x2 in zip(a, b):
+        assert torch.equal(x1, x2)
+    # a bf16 gradient is the fp32 one rounded
+    c = rpb.fused_backward(d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], out, lse, d["dout"], H, W, 0.125)
+    torch.cuda.synchronize()
+    for x16, x32 in zip(a[:3], c[:3]):
+        assert torch.equal(x16, x32.to(torch.bfloat16))

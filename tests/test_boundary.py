@@ -15,7 +15,8 @@ from relative_position_bias_gb300 import build as rbuild
 
 EXPECTED = {"dera_relpos_project", "dera_relpos_attention", "dera_relpos_fused", "dera_status_string",
             "dera_relpos_device_status", "dera_relpos_selftest_wait_timeout", "dera_relpos_abi_version",
-            "dera_relpos_workspace_size", "dera_relpos_fused_noalloc"}
+            "dera_relpos_workspace_size", "dera_relpos_fused_noalloc", "dera_relpos_fused_lse",
+            "dera_relpos_backward_workspace_size", "dera_relpos_fused_backward"}
 
 FAKE = 0x10000          # aligned, never dereferenced: every call below fails before any CUDA work
 FAKE_MISALIGNED = 0x10008
@@ -42,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.dera_relpos_abi_version() == 2
+    assert lib.dera_relpos_abi_version() == 3
     for code, name in api.STATUS_NAMES.items():
         assert lib.dera_status_string(code).decode().startswith(name)
     assert lib.dera_status_string(99).decode() == "DERA_ERR_UNKNOWN"
@@ -117,3 +118,35 @@ def test_binding_raises_on_library_errors():
     with pytest.raises(rpb.DeraError) as ei:
         rpb.fused(q, q, q, th, th, 4, 4, out_dtype=torch.float32)
     assert ei.value.status in (6, 8)
+
+
+def _bwd(lib, *, ptrs=(FAKE,) * 13, BH=1, H=4, W=4, d=64, in_dt=1, out_dt=2, grad_dt=2, ws=FAKE, ws_bytes=1 << 30):
+    return lib.dera_relpos_fused_backward(*ptrs, BH, H, W, d, 0.125, in_dt, out_dt, grad_dt, ws, ws_bytes, None)
+
+
+def test_backward_rejects_before_any_cuda_work(lib):
+    """Shape, head_dim, dtype, null and alignment errors of the backward entry, all decided on the host."""
+    codes = {n: c for c, n in api.STATUS_NAMES.items()}
+    assert _bwd(lib, d=128) == codes["DERA_ERR_HEAD_DIM"]
+    assert _bwd(lib, H=65) == codes["DERA_ERR_SHAPE"]
+    assert _bwd(lib, in_dt=2) == codes["DERA_ERR_DTYPE"]           # fp32 inputs
+    assert _bwd(lib, out_dt=0) == codes["DERA_ERR_DTYPE"]          # fp16 out with bf16 inputs
+    assert _bwd(lib, grad_dt=0) == codes["DERA_ERR_DTYPE"]
+    assert _bwd(lib, ptrs=(FAKE,) * 12 + (None,)) == codes["DERA_ERR_NULL"]
+    assert _bwd(lib, ptrs=(FAKE_MISALIGNED,) + (FAKE,) * 12) == codes["DERA_ERR_ALIGN"]
+    lse = lib.dera_relpos_fused_lse(*(FAKE,) * 7, 1, 4, 4, 64, 0.125, 1, 2, None, 0, None)
+    assert lse == codes["DERA_OK"] or lse in (codes["DERA_ERR_CUDA"], codes["DERA_ERR_DEVICE"])
+    assert lib.dera_relpos_fused_lse(*(FAKE,) * 6, None, 1, 4, 4, 64, 0.125, 1, 2, None, 0, None) == codes["DERA_ERR_NULL"]
+
+
+def test_backward_workspace_size_formula(lib):
+    """fp32 regions, each 256-byte aligned: rel_h, rel_w, D, dq_s, drel_h, drel_w, per-tile partials."""
+    def a256(x):
+        return (x + 255) // 256 * 256
+    for BH, H, W in [(1, 4, 4), (12, 64, 64), (3, 40, 40), (2, 14, 14), (5, 7, 30)]:
+        rows, nq = BH * H * W, -(-(H * W) // 128)
+        want = (a256(4 * rows * H) + a256(4 * rows * W) + a256(4 * rows) + a256(4 * rows * 64)
+                + a256(4 * rows * H) + a256(4 * rows * W) + a256(4 * BH * nq * (2 * H - 1 + 2 * W - 1) * 64))
+        assert rpb.backward_workspace_size(BH, H, W, 64) == want
+    with pytest.raises(rpb.DeraError):
+        rpb.backward_workspace_size(1, 4, 4, 128)
