@@ -421,6 +421,86 @@ def run_ours(args, w, rank: int, world: int) -> dict | None:
     return line
 
 
+def backward_flops(BH: int, N: int, d: int = 64) -> float:
+    """Algorithmic FLOPs of the attention backward: dv = P^T dO, dP = dO v^T, dq = dZ k, dk = dZ^T q and
+    the recomputation of S = q k^T, 2*N*N*d each per (batch, head) (2.5 times the forward's)."""
+    return 10.0 * BH * N * N * d
+
+
+def run_backward(args, w, rank: int, world: int) -> dict | None:
+    """`--entry backward`: one step = dera_relpos_fused_backward (projection, rows, cols, bias and
+    table kernels) on the workload, with the training forward's out and lse and a random dout
+    already in HBM; gradients in the input dtype."""
+    import torch
+    import relative_position_bias_gb300 as rpb
+    from relative_position_bias_gb300 import build as rbuild
+    from relative_position_bias_gb300 import inputs as I
+
+    if w.d != 64:
+        raise SystemExit("the backward supports head_dim 64")
+    rbuild.build()
+    rpb.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    x = I.make_inputs(w, seed=rank)
+    d = {k: t.to(dev) for k, t in x.items()}
+    g = torch.Generator().manual_seed(1000 + rank)
+    dout = torch.randn(w.BH, w.N, w.d, generator=g).to(w.torch_dtype).to(dev)
+    fargs = (d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W, w.scale)
+    out, lse = rpb.fused_lse(*fargs)
+    ws = torch.empty(rpb.backward_workspace_size(w.BH, w.H, w.W, w.d), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        return rpb.fused_backward(d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], out, lse, dout, w.H, w.W,
+                                  w.scale, grad_dtype=w.torch_dtype, workspace=ws)
+
+    def timed(fn, n):
+        for _ in range(args.warmup):
+            flush.fill_(1)
+            fn()
+        torch.cuda.synchronize()
+        evs = []
+        for i in range(n):
+            flush.fill_(i & 0xFF)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    with ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else 0) as clocks:
+        ms = timed(step, args.steps)
+    fwd_ms = timed(lambda: rpb.fused_lse(*fargs), max(3, min(args.steps, 100)))
+    total_s = aggregate_max(sum(ms) / 1e3)
+    flops = backward_flops(w.BH, w.N, w.d)
+    value = job_value(flops, args.steps, world, total_s)
+    if rank != 0:
+        return None
+    ms_mean = 1e3 * total_s / args.steps
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = flops / (ms_mean / 1e3) / 1e12
+    cfg = workload_config(w, "backward", world)
+    return {
+        "metric": "TFLOP/s of the attention backward (dq, dk, dv and the table gradients) on the workload",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_mean, "statistic": "mean over the timed steps", "ms_median": statistics.median(ms),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": cfg,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "traffic": None, "kernel": "the whole backward call (5 kernels)",
+                     "peak_source": f"bf16_tflops (burst) of {peak_src}", "flops_per_launch": flops,
+                     "flops_executed": 14.0 * w.BH * w.N * w.N * w.d},
+        "training_forward": {"ms": statistics.median(fwd_ms),
+                             "tflops": attention_flops(w.BH, w.N, w.d) / (statistics.median(fwd_ms) * 1e-3) / 1e12},
+        "gpu_launches": 5 * args.steps,
+        "clocks": clocks.summary(),
+    }
+
+
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -428,7 +508,7 @@ def main(argv=None) -> int:
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="global64")
-    ap.add_argument("--entry", choices=["fused", "two_step"], default="fused")
+    ap.add_argument("--entry", choices=["fused", "two_step", "backward"], default="fused")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
@@ -453,7 +533,7 @@ def main(argv=None) -> int:
         import torch.distributed as dist
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         dist.init_process_group("nccl")
-    line = run_ours(args, w, rank, world)
+    line = run_backward(args, w, rank, world) if args.entry == "backward" else run_ours(args, w, rank, world)
     if line is not None:
         print(json.dumps(line), flush=True)
     if world > 1:

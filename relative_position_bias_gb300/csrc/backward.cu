@@ -10,19 +10,18 @@ namespace {
 
 template <int WP, bool BF16>
 cudaError_t launch_bwd_attn(const BwdMaps& maps, const BwdArgs& args, cudaStream_t stream) {
-  using SM = BwdSmem<KeyTile<WP, 64>::BN>;
   auto rows = relpos_bwd_rows_kernel<WP, BF16>;
   auto cols = relpos_bwd_cols_kernel<WP, BF16>;
-  cudaError_t e = cudaFuncSetAttribute(rows, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
+  cudaError_t e = cudaFuncSetAttribute(rows, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdRowsSmem::kAlloc);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(cols, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kAlloc);
+  e = cudaFuncSetAttribute(cols, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdColsSmem::kAlloc);
   if (e != cudaSuccess) return e;
   const unsigned grid_rows = static_cast<unsigned>(args.BH) * static_cast<unsigned>(args.n_qtiles);
-  rows<<<grid_rows, kBwdThreads, SM::kAlloc, stream>>>(maps.q, maps.dout, maps.k, maps.v, args);
+  rows<<<grid_rows, kBwdRowsThreads, BwdRowsSmem::kAlloc, stream>>>(maps.q, maps.dout, maps.k, maps.v, args);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const unsigned grid_cols = static_cast<unsigned>(args.BH) * static_cast<unsigned>(args.n_kv);
-  cols<<<grid_cols, kBwdThreads, SM::kAlloc, stream>>>(maps.q, maps.dout, maps.k, maps.v, args);
+  cols<<<grid_cols, kBwdColsThreads, BwdColsSmem::kAlloc, stream>>>(maps.q, maps.dout, maps.k, maps.v, args);
   return cudaGetLastError();
 }
 
@@ -51,7 +50,7 @@ cudaError_t launch_backward(const BwdMaps& maps, const BwdArgs& args, int WP, cu
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int total = (2 * args.H - 1 + 2 * args.W - 1) * 64;
-  relpos_bwd_tables_kernel<<<(total + 255) / 256, 256, 0, stream>>>(args, static_cast<int>(blocks));
+  relpos_bwd_tables_kernel<<<(total + 31) / 32, 256, 0, stream>>>(args, static_cast<int>(blocks));
   return cudaGetLastError();
 }
 

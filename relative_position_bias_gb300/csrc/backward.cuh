@@ -35,23 +35,21 @@
 
 namespace dera {
 
-constexpr int kBwdThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 one thread per TMEM lane
+constexpr int kBwdColsThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 softmax (two per TMEM lane quarter)
 constexpr int kBwdStages = 3;      // K/V (rows kernel) or Q/dO (cols kernel) ring depth
 
 
 // Shared-memory layout shared by the two attention kernels (1024-byte aligned
 // operand tiles first).
-template <int BN>
+template <int KS, int kStagingBytes_>
 struct BwdSmem {
   static constexpr int kTile = kTileBytes;                  // 128 rows x 128 B
   static constexpr int kA = 0;                              // rows: Q tile; cols: K tile
   static constexpr int kB = kA + kTile;                     // rows: dO tile; cols: V tile
-  static constexpr int kRing = kB + kTile;                  // stages of two 16 KB tiles
+  static constexpr int kRing = kB + kTile;                  // KS stages of two 16 KB tiles
   static constexpr int kStage = 2 * kTile;
-  static constexpr int kStaging = kRing + kBwdStages * kStage;
-  // rows kernel: per-thread bias rows, 128 x 65 floats; cols kernel: two
-  // buffers of per-query-tile bias, lse and D (see the cols kernel)
-  static constexpr int kStagingBytes = 2 * 128 * 76 * 4;
+  static constexpr int kStaging = kRing + KS * kStage;
+  static constexpr int kStagingBytes = kStagingBytes_;
   static constexpr int kBars = kStaging + kStagingBytes;
   static constexpr int kNumBars = 24;
   static constexpr int kMisc = kBars + kNumBars * 8;
@@ -91,7 +89,15 @@ enum : int {
   kBwStg = kBwMmaDone + 1,                 // staging barrier of the softmax threads (count 128)
   kBwCount = kBwStg + 1
 };
-static_assert(kBwCount <= BwdSmem<128>::kNumBars, "barrier slots");
+// rows kernel: a two-stage K/V ring; staging holds the rel_h rows and the
+// bias-gradient accumulators, 3 x 128 rows of 65 floats
+using BwdRowsSmem = BwdSmem<2, 3 * 128 * 65 * 4>;
+// cols kernel: a three-stage Q/dO ring; staging holds two buffers of one query
+// tile's rel_w, rel_h entries, lse and D, transposed (74 rows of 132 floats each)
+constexpr int kColsStageRow = 132;
+constexpr int kColsStageFloats = 74 * kColsStageRow;
+using BwdColsSmem = BwdSmem<3, 2 * kColsStageFloats * 4>;
+static_assert(kBwCount <= BwdRowsSmem::kNumBars, "barrier slots");
 
 // Common set-up of the two attention kernels: barriers, TMEM (all 512
 // columns), and the aligned shared-memory base.
@@ -102,9 +108,8 @@ struct BwdCta {
   uint32_t tbase;
 };
 
-template <int BN>
-__device__ __forceinline__ BwdCta bwd_setup(uint8_t* smem_raw, int warp) {
-  using SM = BwdSmem<BN>;
+template <class SM>
+__device__ __forceinline__ BwdCta bwd_setup(uint8_t* smem_raw, int warp, int n_compute) {
   BwdCta c;
   const uint32_t raw_u = smem_u32(smem_raw);
   c.smem = smem_raw + (((raw_u + 1023u) & ~1023u) - raw_u);
@@ -114,14 +119,14 @@ __device__ __forceinline__ BwdCta bwd_setup(uint8_t* smem_raw, int warp) {
   if (threadIdx.x == 0) {
     *c.abort_flag = 0;
     mbar_init(&c.bars[kBwQFull], 1);
-    for (int s = 0; s < kBwdStages; ++s) {
+    for (int s = 0; s < kBwdStages; ++s) {   // the rows kernel uses the first two
       mbar_init(&c.bars[kBwRingFull + s], 1);
       mbar_init(&c.bars[kBwRingEmpty + s], 1);
     }
     mbar_init(&c.bars[kBwSFull], 1);
-    mbar_init(&c.bars[kBwPFull], kBlockM);
+    mbar_init(&c.bars[kBwPFull], n_compute);
     mbar_init(&c.bars[kBwMmaDone], 1);
-    mbar_init(&c.bars[kBwStg], kBlockM);
+    mbar_init(&c.bars[kBwStg], n_compute);
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -145,28 +150,215 @@ __device__ __forceinline__ void bwd_teardown(uint32_t tbase, int warp) {
 }
 
 // ---------------------------------------------------------------------------
-// Rows kernel: one CTA per (head, query tile); thread r of warps 2-5 owns
-// query row r (TMEM lane r).  TMEM columns: S [0, 128), dP [128, 256), dZ in
-// the input dtype as packed pairs [256, 320), the dZ k accumulator [320, 384).
+// Rows kernel: one CTA per (head, query tile).  Warps 2-9 are the softmax
+// threads, two per query row: warps w and w + 4 share TMEM lane quarter w % 4
+// and take the first and the second half of every key tile's 16-column
+// blocks.  TMEM columns: S [0, 128), dP [128, 256), dZ in the input dtype as
+// packed pairs [256, 320), the dZ k accumulator [320, 384).  The two halves
+// add their bias-gradient sums in shared memory (two addends per entry, so
+// the result does not depend on their order).
+constexpr int kBwdRowsThreads = 320;
+
+// Which 16-column blocks of a key tile a half of the rows kernel's softmax
+// threads takes (see rows_softmax), and their order.
+template <int WP, int HALF>
+struct RowsSplit {
+  static constexpr int kBlocks = KeyTile<WP, 64>::BN / 16, kHalf0 = (kBlocks + 1) / 2;
+  __host__ __device__ static constexpr bool mine(int bb) {
+    return WP == 64 ? ((16 * bb) % 64) / 32 == HALF : (HALF == 0 ? bb < kHalf0 : bb >= kHalf0);
+  }
+  __host__ __device__ static constexpr int next(int bb) {
+    for (int x = bb + 1; x < kBlocks; ++x)
+      if (mine(x)) return x;
+    return kBlocks;
+  }
+  __host__ __device__ static constexpr int rank(int bb) {
+    int c = 0;
+    for (int x = 0; x < bb; ++x) c += mine(x) ? 1 : 0;
+    return c;
+  }
+};
+
+// The softmax role of the rows kernel for one half of the threads.  With 64
+// key columns per grid row the halves split every grid row's columns (kw below
+// or above 32), so each thread keeps 32 rel_w terms and 32 column sums in
+// registers; with narrower rows they split each key tile's 16-column blocks
+// into a first and a second half.
+template <int WP, bool BF16, int HALF>
+__device__ __forceinline__ void rows_softmax(const BwdArgs& args, uint8_t* smem, uint64_t* bars,
+                                             volatile int* abort_flag, uint32_t tbase, int warp, int lane, int bh,
+                                             int qt) {
+  using KT = KeyTile<WP, 64>;
+  constexpr int KHT = KT::KHT, BN = KT::BN;
+  using SM = BwdRowsSmem;
+  constexpr int fmt = BF16 ? kBF16 : kF16;
+  constexpr bool kSplitKw = WP == 64;
+  constexpr int kLW = kSplitKw ? 32 : WP;              // rel_w terms a thread keeps
+  constexpr int kKw0 = kSplitKw ? 32 * HALF : 0;       // first of them
+  constexpr int kBlocks = BN / 16;
+  int* status = args.status;
+  const int n_kv = args.n_kv, H = args.H, W = args.W, N = args.N;
+  const int wq = warp & 3;
+  const int r = wq * 32 + lane;
+  const int t = threadIdx.x - 64;          // 0..255
+  const int n = qt * kBlockM + r;
+  const bool row_valid = n < N;
+  const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+  const uint32_t tS = tbase + lane_off, tdP = tS + 128, tdZ = tS + 256, tdQ = tS + 320;
+  const size_t row = static_cast<size_t>(bh) * N + (row_valid ? n : 0);
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  const float sl2 = args.scale_log2;
+  float* stg = reinterpret_cast<float*>(smem + SM::kStaging);
+  float* bh_row = stg + r * 65;                          // rel_h row (base 2)
+  float* dRH_sm = stg + 128 * 65 + r * 65;               // per key grid row: sum over its columns
+  float* dRW_sm = stg + 2 * 128 * 65 + r * 65;           // per key column: sum over grid rows
+  const int Hpad = n_kv * KHT;
+  if (HALF == 0) {
+    for (int kh = 0; kh < Hpad; ++kh)
+      bh_row[kh] = (kh < H) ? (row_valid ? kLog2e * args.rel_h[row * H + kh] : 0.f) : NEG_INF;
+  }
+  for (int e = t; e < 2 * 128 * 65; e += 2 * kBlockM) stg[128 * 65 + e] = 0.f;
+  float bw[kLW];
+  #pragma unroll
+  for (int i = 0; i < kLW; ++i) {
+    const int kw = kKw0 + i;
+    bw[i] = (kw < W) ? (row_valid ? kLog2e * args.rel_w[row * W + kw] : 0.f) : NEG_INF;
+  }
+  const float lse2 = row_valid ? args.lse[row] : 0.f;
+  // D = dO . out for this row (out in fp32 or in the input dtype)
+  float Dn = 0.f;
+  if (row_valid) {
+    for (int c = 0; c < 64; ++c) {
+      const float o = args.out_fmt == kF32 ? reinterpret_cast<const float*>(args.out)[row * 64 + c]
+                                            : ld_in(args.out, row * 64 + c, fmt);
+      Dn = fmaf(ld_in(args.dout, row * 64 + c, fmt), o, Dn);
+    }
+    if (HALF == 0) args.D[row] = Dn;
+  }
+  uint32_t stg_phase = 0;
+  auto group_sync = [&]() -> bool {
+    mbar_arrive(&bars[kBwStg]);
+    const bool w = mbar_wait(&bars[kBwStg], stg_phase & 1, abort_flag, status);
+    ++stg_phase;
+    return warp_all(w);
+  };
+  bool ok = group_sync();   // bh_row written, accumulators cleared
+  float dRW[kLW];
+  #pragma unroll
+  for (int i = 0; i < kLW; ++i) dRW[i] = 0.f;
+  for (int j = 0; ok && j < n_kv; ++j) {
+    float bhv[KHT];
+    #pragma unroll
+    for (int g = 0; g < KHT; ++g) bhv[g] = bh_row[j * KHT + g];
+    ok = warp_all(mbar_wait(&bars[kBwSFull], j & 1, abort_flag, status));
+    if (!ok) break;
+    tc_fence_after();
+    if (j > 0) {
+      // dZ(j-1) has been read by its product before dZ(j) is written
+      ok = warp_all(mbar_wait(&bars[kBwMmaDone], (j - 1) & 1, abort_flag, status));
+      if (!ok) break;
+      tc_fence_after();
+    }
+    float dRH[KHT];
+    #pragma unroll
+    for (int g = 0; g < KHT; ++g) dRH[g] = 0.f;
+    // this half's blocks, the next block's S and dP loads in flight while the
+    // current one is computed
+    using RS = RowsSplit<WP, HALF>;
+    uint32_t us[2][16], up[2][16];
+    tmem_ld16(tS + 16 * RS::next(-1), us[0]);
+    tmem_ld16(tdP + 16 * RS::next(-1), up[0]);
+    #pragma unroll
+    for (int bb = 0; bb < kBlocks; ++bb) {
+      if (!RS::mine(bb)) continue;
+      const int cb = 16 * bb;
+      const int cur = RS::rank(bb) & 1;
+      tmem_wait_ld();
+      if (RS::next(bb) < kBlocks) {
+        tmem_ld16(tS + 16 * RS::next(bb), us[cur ^ 1]);
+        tmem_ld16(tdP + 16 * RS::next(bb), up[cur ^ 1]);
+      }
+      uint32_t pk[8];
+      #pragma unroll
+      for (int k = 0; k < 16; k += 2) {
+        const int col = cb + k;
+        const int g = col / WP, i = col % WP - kKw0;
+        const float x0 = fmaf(__uint_as_float(us[cur][k]), sl2, bw[i] + bhv[g]) - lse2;
+        const float x1 = fmaf(__uint_as_float(us[cur][k + 1]), sl2, bw[i + 1] + bhv[g]) - lse2;
+        float d0 = ex2_approx(x0) * (__uint_as_float(up[cur][k]) - Dn);
+        float d1 = ex2_approx(x1) * (__uint_as_float(up[cur][k + 1]) - Dn);
+        if (!row_valid) d0 = d1 = 0.f;
+        dRW[i] += d0;
+        dRW[i + 1] += d1;
+        dRH[g] += d0 + d1;
+        pk[k / 2] = pack_in(d0, d1, fmt);
+      }
+      tmem_st8(tdZ + cb / 2, pk);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(&bars[kBwPFull]);
+    // two addends per entry (one per half), so their order does not matter
+    #pragma unroll
+    for (int g = 0; g < KHT; ++g)
+      if (j * KHT + g < H) atomicAdd(&dRH_sm[j * KHT + g], dRH[g]);
+  }
+  if (kSplitKw) {
+    // each half owns its columns
+    if (ok && row_valid) {
+      #pragma unroll
+      for (int i = 0; i < kLW; ++i)
+        if (kKw0 + i < W) args.drel_w[row * W + kKw0 + i] = dRW[i];
+    }
+  } else {
+    #pragma unroll
+    for (int i = 0; i < kLW; ++i)
+      if (i < W) atomicAdd(&dRW_sm[i], dRW[i]);
+  }
+  if (ok) ok = group_sync();
+  if (ok && row_valid) {
+    if (HALF == 0) {
+      for (int kh = 0; kh < H; ++kh) args.drel_h[row * H + kh] = dRH_sm[kh];
+    } else if (!kSplitKw) {
+      for (int kw = 0; kw < W; ++kw) args.drel_w[row * W + kw] = dRW_sm[kw];
+    }
+  }
+  if (ok) ok = warp_all(mbar_wait(&bars[kBwMmaDone], (n_kv - 1) & 1, abort_flag, status));
+  if (ok) {
+    tc_fence_after();
+    uint32_t a[32];
+    tmem_ld32(tdQ + 32 * HALF, a);
+    tmem_wait_ld();
+    if (row_valid) {
+      float4* dst = reinterpret_cast<float4*>(args.dq_s + row * 64 + 32 * HALF);
+      const float sc = args.scale;
+      #pragma unroll
+      for (int c = 0; c < 8; ++c)
+        dst[c] = make_float4(sc * __uint_as_float(a[4 * c]), sc * __uint_as_float(a[4 * c + 1]),
+                             sc * __uint_as_float(a[4 * c + 2]), sc * __uint_as_float(a[4 * c + 3]));
+    }
+  }
+}
+
 template <int WP, bool BF16>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kBwdRowsThreads, 1)
 relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        const BwdArgs args) {
   using KT = KeyTile<WP, 64>;
-  constexpr int KHT = KT::KHT, BN = KT::BN, KS = kBwdStages;
-  using SM = BwdSmem<BN>;
+  constexpr int KHT = KT::KHT, BN = KT::BN, KS = 2;
+  using SM = BwdRowsSmem;
   constexpr int fmt = BF16 ? kBF16 : kF16;
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const BwdCta cta = bwd_setup<BN>(smem_raw, warp);
+  const BwdCta cta = bwd_setup<SM>(smem_raw, warp, 2 * kBlockM);
   uint8_t* smem = cta.smem;
   uint64_t* bars = cta.bars;
   volatile int* abort_flag = cta.abort_flag;
   const uint32_t tbase = cta.tbase;
   int* status = args.status;
   const int bh = blockIdx.x / args.n_qtiles, qt = blockIdx.x - bh * args.n_qtiles;
-  const int n_kv = args.n_kv, H = args.H, W = args.W, N = args.N;
+  const int n_kv = args.n_kv;
   auto sK = [&](int s) { return smem + SM::kRing + s * SM::kStage; };
 
   if (warp == 0) {
@@ -233,116 +425,13 @@ relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     umma_commit_w(&bars[kBwQFull]);
     mbar_wait_budget(&bars[kBwQFull], 1, kWaitBudgetCycles);
     __syncwarp();
+  } else if (((warp - 2) >> 2) == 0) {
+    rows_softmax<WP, BF16, 0>(args, smem, bars, abort_flag, tbase, warp, lane, bh, qt);
   } else {
-    // ---------------------------------------------------------------- softmax threads
-    const int wq = warp & 3;
-    const int r = wq * 32 + lane;
-    const int n = qt * kBlockM + r;
-    const bool row_valid = n < N;
-    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tbase + lane_off, tdP = tS + 128, tdZ = tS + 256, tdQ = tS + 320;
-    const size_t row = static_cast<size_t>(bh) * N + (row_valid ? n : 0);
-    const float NEG_INF = -__int_as_float(0x7f800000);
-    const float sl2 = args.scale_log2;
-    // this thread's bias row (base 2): rel_w in registers, rel_h in shared memory
-    float bw[WP];
-    #pragma unroll
-    for (int kw = 0; kw < WP; ++kw)
-      bw[kw] = (kw < W) ? (row_valid ? kLog2e * args.rel_w[row * W + kw] : 0.f) : NEG_INF;
-    float* bh_row = reinterpret_cast<float*>(smem + SM::kStaging) + r * 65;
-    const int Hpad = n_kv * KHT;
-    for (int kh = 0; kh < Hpad; ++kh)
-      bh_row[kh] = (kh < H) ? (row_valid ? kLog2e * args.rel_h[row * H + kh] : 0.f) : NEG_INF;
-    const float lse2 = row_valid ? args.lse[row] : 0.f;
-    // D = dO . out for this row (out in fp32 or in the input dtype)
-    float Dn = 0.f;
-    if (row_valid) {
-      for (int c = 0; c < 64; ++c) {
-        const float o = args.out_fmt == kF32 ? reinterpret_cast<const float*>(args.out)[row * 64 + c]
-                                              : ld_in(args.out, row * 64 + c, fmt);
-        Dn = fmaf(ld_in(args.dout, row * 64 + c, fmt), o, Dn);
-      }
-      args.D[row] = Dn;
-    }
-    float dRW[WP];
-    #pragma unroll
-    for (int kw = 0; kw < WP; ++kw) dRW[kw] = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      float bhv[KHT];
-      #pragma unroll
-      for (int g = 0; g < KHT; ++g) bhv[g] = bh_row[j * KHT + g];
-      ok = warp_all(mbar_wait(&bars[kBwSFull], j & 1, abort_flag, status));
-      if (!ok) break;
-      tc_fence_after();
-      if (j > 0) {
-        // dZ(j-1) has been read by its product before dZ(j) is written
-        ok = warp_all(mbar_wait(&bars[kBwMmaDone], (j - 1) & 1, abort_flag, status));
-        if (!ok) break;
-        tc_fence_after();
-      }
-      float dRH[KHT];
-      #pragma unroll
-      for (int g = 0; g < KHT; ++g) dRH[g] = 0.f;
-      #pragma unroll
-      for (int cb = 0; cb < BN; cb += 16) {
-        uint32_t us[16], up[16];
-        tmem_ld16(tS + cb, us);
-        tmem_ld16(tdP + cb, up);
-        tmem_wait_ld();
-        uint32_t pk[8];
-        #pragma unroll
-        for (int k = 0; k < 16; k += 2) {
-          const int col = cb + k;
-          const int g = col / WP, kw = col % WP;
-          const float x0 = fmaf(__uint_as_float(us[k]), sl2, bw[kw] + bhv[g]) - lse2;
-          const float x1 = fmaf(__uint_as_float(us[k + 1]), sl2, bw[kw + 1] + bhv[g]) - lse2;
-          float d0 = ex2_approx(x0) * (__uint_as_float(up[k]) - Dn);
-          float d1 = ex2_approx(x1) * (__uint_as_float(up[k + 1]) - Dn);
-          if (!row_valid) d0 = d1 = 0.f;
-          dRW[kw] += d0;
-          dRW[kw + 1] += d1;
-          dRH[g] += d0 + d1;
-          pk[k / 2] = pack_in(d0, d1, fmt);
-        }
-        tmem_st8(tdZ + cb / 2, pk);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars[kBwPFull]);
-      if (row_valid) {
-        #pragma unroll
-        for (int g = 0; g < KHT; ++g)
-          if (j * KHT + g < H) args.drel_h[row * H + j * KHT + g] = dRH[g];
-      }
-    }
-    if (ok) ok = warp_all(mbar_wait(&bars[kBwMmaDone], (n_kv - 1) & 1, abort_flag, status));
-    if (ok) {
-      tc_fence_after();
-      uint32_t a[32], b[32];
-      tmem_ld32(tdQ, a);
-      tmem_ld32(tdQ + 32, b);
-      tmem_wait_ld();
-      if (row_valid) {
-        float4* dst = reinterpret_cast<float4*>(args.dq_s + row * 64);
-        const float sc = args.scale;
-        #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          dst[c] = make_float4(sc * __uint_as_float(a[4 * c]), sc * __uint_as_float(a[4 * c + 1]),
-                               sc * __uint_as_float(a[4 * c + 2]), sc * __uint_as_float(a[4 * c + 3]));
-        #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          dst[8 + c] = make_float4(sc * __uint_as_float(b[4 * c]), sc * __uint_as_float(b[4 * c + 1]),
-                                   sc * __uint_as_float(b[4 * c + 2]), sc * __uint_as_float(b[4 * c + 3]));
-        #pragma unroll
-        for (int kw = 0; kw < WP; ++kw)
-          if (kw < W) args.drel_w[row * W + kw] = dRW[kw];
-      }
-    }
+    rows_softmax<WP, BF16, 1>(args, smem, bars, abort_flag, tbase, warp, lane, bh, qt);
   }
   bwd_teardown(tbase, warp);
 }
-
 
 // ---------------------------------------------------------------------------
 // Cols kernel: one CTA per (head, key tile of KHT grid rows); thread m of warps
@@ -354,17 +443,17 @@ relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
 // tile's rel_w rows [128][W], its rel_h entries for this key tile's grid rows
 // [128][KHT], lse and D.
 template <int WP, bool BF16>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kBwdColsThreads, 1)
 relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        const BwdArgs args) {
   using KT = KeyTile<WP, 64>;
   constexpr int KHT = KT::KHT, BN = KT::BN, KS = kBwdStages;
-  using SM = BwdSmem<BN>;
+  using SM = BwdColsSmem;
   constexpr int fmt = BF16 ? kBF16 : kF16;
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const BwdCta cta = bwd_setup<BN>(smem_raw, warp);
+  const BwdCta cta = bwd_setup<SM>(smem_raw, warp, 2 * kBlockM);
   uint8_t* smem = cta.smem;
   uint64_t* bars = cta.bars;
   volatile int* abort_flag = cta.abort_flag;
@@ -442,7 +531,8 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     // ---------------------------------------------------------------- softmax threads
     const int wq = warp & 3;
     const int m = wq * 32 + lane;          // key slot of the tile
-    const int t = m;                       // index among the 128 staging threads
+    const int half = (warp - 2) >> 2;      // query columns [64 half, 64 half + 64) of every tile
+    const int t = threadIdx.x - 64;        // index among the 256 staging threads
     const int g = m / WP, kw = m % WP;
     const int kh = j * KHT + g;
     const bool key_valid = m < BN && kw < W && kh < H;
@@ -451,24 +541,30 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                    tdK = tS + 448;
     const float sl2 = args.scale_log2;
     float* stage_base = reinterpret_cast<float*>(smem + SM::kStaging);
-    constexpr int kBufFloats = 128 * 76;
-    // buffer b: rel_w [128][W] at 0, rel_h [128][KHT] at 128*64, lse at 128*72, D at 128*73
+    // buffer b, transposed so that a thread reads four query columns at once:
+    // rel_w [kw][n] in rows 0..63, rel_h [g][n] in rows 64..71, lse in row 72,
+    // D in row 73 (rows of kColsStageRow floats; columns past N hold zeros)
+    constexpr int kBufFloats = kColsStageFloats, RS = kColsStageRow;
     auto stage = [&](int i, int b) {
       float* buf = stage_base + b * kBufFloats;
       const int n0 = i * kBlockM;
       const int rows = min(kBlockM, N - n0);
       const size_t base = static_cast<size_t>(bh) * N + n0;
-      for (int e = t; e < kBlockM * W; e += kBlockM) {
-        const int rr = e / W;
-        cp_async4(buf + e, args.rel_w + (rr < rows ? base * W + e : 0), rr < rows ? 4u : 0u);
+      for (int e = t; e < kBlockM * W; e += 2 * kBlockM) {
+        const int rr = e / W, c = e - rr * W;
+        cp_async4(buf + c * RS + rr, args.rel_w + (rr < rows ? base * W + e : 0), rr < rows ? 4u : 0u);
       }
-      for (int e = t; e < kBlockM * KHT; e += kBlockM) {
+      for (int e = t; e < kBlockM * KHT; e += 2 * kBlockM) {
         const int rr = e / KHT, gg = e - rr * KHT, khh = j * KHT + gg;
         const bool v = rr < rows && khh < H;
-        cp_async4(buf + 128 * 64 + e, args.rel_h + (v ? (base + rr) * H + khh : 0), v ? 4u : 0u);
+        cp_async4(buf + (64 + gg) * RS + rr, args.rel_h + (v ? (base + rr) * H + khh : 0), v ? 4u : 0u);
       }
-      cp_async4(buf + 128 * 72 + t, args.lse + (t < rows ? base + t : 0), t < rows ? 4u : 0u);
-      cp_async4(buf + 128 * 73 + t, args.D + (t < rows ? base + t : 0), t < rows ? 4u : 0u);
+      if (t < kBlockM) {
+        cp_async4(buf + 72 * RS + t, args.lse + (t < rows ? base + t : 0), t < rows ? 4u : 0u);
+      } else {
+        const int u = t - kBlockM;
+        cp_async4(buf + 73 * RS + u, args.D + (u < rows ? base + u : 0), u < rows ? 4u : 0u);
+      }
     };
     uint32_t stg_phase = 0;
     auto group_sync = [&]() -> bool {
@@ -487,10 +583,10 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
       if (!ok) break;
       if (i + 1 < n_qt) stage(i + 1, (i + 1) & 1);
       const float* buf = stage_base + (i & 1) * kBufFloats;
-      const float* rw = buf;
-      const float* rh = buf + 128 * 64;
-      const float* lse = buf + 128 * 72;
-      const float* Dv = buf + 128 * 73;
+      const float* rwT = buf + kw * RS;           // kw < WP <= 64
+      const float* rhT = buf + (64 + g) * RS;     // g < 8 for every key slot
+      const float* lseT = buf + 72 * RS;
+      const float* DT = buf + 73 * RS;
       const int rows = min(kBlockM, N - i * kBlockM);
       ok = warp_all(mbar_wait(&bars[kBwSFull], i & 1, abort_flag, status));
       if (!ok) break;
@@ -500,28 +596,44 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         if (!ok) break;
         tc_fence_after();
       }
-      #pragma unroll 1
-      for (int cb = 0; cb < kBlockM; cb += 16) {
-        uint32_t us[16], up[16];
-        tmem_ld16(tS + cb, us);
-        tmem_ld16(tdP + cb, up);
+      // this half's four 16-column blocks; the next block's S^T and dP^T
+      // loads are in flight while the current one is computed
+      const int c_first = 64 * half;
+      uint32_t us[2][16], up[2][16];
+      tmem_ld16(tS + c_first, us[0]);
+      tmem_ld16(tdP + c_first, up[0]);
+      #pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int cb = c_first + 16 * q;
         tmem_wait_ld();
+        if (q < 3) {
+          tmem_ld16(tS + cb + 16, us[(q + 1) & 1]);
+          tmem_ld16(tdP + cb + 16, up[(q + 1) & 1]);
+        }
         uint32_t pp[8], pz[8];
         #pragma unroll
-        for (int k = 0; k < 16; k += 2) {
-          float p2[2], z2[2];
+        for (int k4 = 0; k4 < 16; k4 += 4) {
+          const int c4 = cb + k4;
+          const float4 w4 = *reinterpret_cast<const float4*>(rwT + c4);
+          const float4 h4 = *reinterpret_cast<const float4*>(rhT + c4);
+          const float4 l4 = *reinterpret_cast<const float4*>(lseT + c4);
+          const float4 d4 = *reinterpret_cast<const float4*>(DT + c4);
+          const float bw4[4] = {w4.x + h4.x, w4.y + h4.y, w4.z + h4.z, w4.w + h4.w};
+          const float ls4[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float dd4[4] = {d4.x, d4.y, d4.z, d4.w};
+          float p4[4], z4[4];
           #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int nn = cb + k + h;
-            const bool v = key_valid && nn < rows;
-            const float b = v ? (rh[nn * KHT + g] + rw[nn * W + kw]) : 0.f;
-            const float x = fmaf(__uint_as_float(us[k + h]), sl2, fmaf(b, kLog2e, -lse[nn]));
+          for (int h = 0; h < 4; ++h) {
+            const bool v = key_valid && c4 + h < rows;
+            const float x = fmaf(__uint_as_float(us[q & 1][k4 + h]), sl2, fmaf(bw4[h], kLog2e, -ls4[h]));
             const float p = v ? ex2_approx(x) : 0.f;
-            p2[h] = p;
-            z2[h] = v ? p * (__uint_as_float(up[k + h]) - Dv[nn]) : 0.f;
+            p4[h] = p;
+            z4[h] = v ? p * (__uint_as_float(up[q & 1][k4 + h]) - dd4[h]) : 0.f;
           }
-          pp[k / 2] = pack_in(p2[0], p2[1], fmt);
-          pz[k / 2] = pack_in(z2[0], z2[1], fmt);
+          pp[k4 / 2] = pack_in(p4[0], p4[1], fmt);
+          pp[k4 / 2 + 1] = pack_in(p4[2], p4[3], fmt);
+          pz[k4 / 2] = pack_in(z4[0], z4[1], fmt);
+          pz[k4 / 2 + 1] = pack_in(z4[2], z4[3], fmt);
         }
         tmem_st8(tP + cb / 2, pp);
         tmem_st8(tdZ + cb / 2, pz);
@@ -537,25 +649,21 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
       uint32_t a[32];
       const size_t tok = static_cast<size_t>(bh) * N + static_cast<size_t>(kh) * W + kw;
       const float sc = args.scale;
-      // tcgen05.ld is warp-collective: every lane loads, lanes with a key store
+      // tcgen05.ld is warp-collective: every lane loads, lanes with a key store;
+      // the first half of the warps writes dv, the second dk
+      const uint32_t tacc = half == 0 ? tdV : tdK;
+      void* dst = half == 0 ? args.dv : args.dk;
+      const float mul = half == 0 ? 1.0f : sc;
       #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        tmem_ld32(tdV + 32 * h, a);
+        tmem_ld32(tacc + 32 * h, a);
         tmem_wait_ld();
         if (key_valid) {
           #pragma unroll
           for (int c = 0; c < 8; ++c)
-            st_grad4(args.dv, tok * 64 + 32 * h + 4 * c, __uint_as_float(a[4 * c]), __uint_as_float(a[4 * c + 1]),
-                     __uint_as_float(a[4 * c + 2]), __uint_as_float(a[4 * c + 3]), args.grad_fmt);
-        }
-        tmem_ld32(tdK + 32 * h, a);
-        tmem_wait_ld();
-        if (key_valid) {
-          #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            st_grad4(args.dk, tok * 64 + 32 * h + 4 * c, sc * __uint_as_float(a[4 * c]),
-                     sc * __uint_as_float(a[4 * c + 1]), sc * __uint_as_float(a[4 * c + 2]),
-                     sc * __uint_as_float(a[4 * c + 3]), args.grad_fmt);
+            st_grad4(dst, tok * 64 + 32 * h + 4 * c, mul * __uint_as_float(a[4 * c]),
+                     mul * __uint_as_float(a[4 * c + 1]), mul * __uint_as_float(a[4 * c + 2]),
+                     mul * __uint_as_float(a[4 * c + 3]), args.grad_fmt);
         }
       }
     }
@@ -566,15 +674,42 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
 // ---------------------------------------------------------------------------
 // Bias kernel: one CTA of 256 threads per (head, query tile).  Adds the bias
 // part of dq to dq_s and writes dq; writes this tile's partial table gradients.
+// Tables, q rows and the bias gradients of the tile are staged in shared
+// memory in fp32; rows of the tables and of q are 16-byte aligned (stride 68
+// floats) so that each thread reads them four columns at a time.
 constexpr int kBiasThreads = 256;
-constexpr int kTStride = 65;   // floats per staged table row (odd: rows start in different banks)
+constexpr int kTStride = 68;
 
 __host__ __device__ constexpr int bias_smem_floats(int H, int W) {
-  return (2 * H - 1 + 2 * W - 1) * kTStride + 128 * (H + 1) + 128 * (W + 1) + 128 * 65 + 2 * 128;
+  return (2 * H - 1 + 2 * W - 1) * kTStride + 128 * (H + 1) + 128 * (W + 1) + 128 * kTStride + 2 * 128;
+}
+
+// dT partial of one 4 x 4 block: table rows i0..i0+3 of a table of length L
+// (2 Lg - 1 rows for grid side Lg), columns c0..c0+3, over the tile's rows:
+// acc[u][*] = sum_r [0 <= kk < Lg] dR[r][kk] q[r][c0..c0+3], kk = coord(r) - (i0 + u) + Lg - 1.
+__device__ __forceinline__ void table_block(const float* dR, int ld, const int* coord, int Lg, const float* Qf,
+                                            int rows, int i0, int c0, float (&acc)[4][4]) {
+  #pragma unroll
+  for (int u = 0; u < 4; ++u)
+    #pragma unroll
+    for (int k = 0; k < 4; ++k) acc[u][k] = 0.f;
+  for (int rr = 0; rr < rows; ++rr) {
+    const int kk0 = coord[rr] - i0 + Lg - 1;
+    const float4 qv = *reinterpret_cast<const float4*>(Qf + rr * kTStride + c0);
+    #pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int kk = kk0 - u;
+      const float wv = static_cast<unsigned>(kk) < static_cast<unsigned>(Lg) ? dR[rr * ld + kk] : 0.f;
+      acc[u][0] = fmaf(wv, qv.x, acc[u][0]);
+      acc[u][1] = fmaf(wv, qv.y, acc[u][1]);
+      acc[u][2] = fmaf(wv, qv.z, acc[u][2]);
+      acc[u][3] = fmaf(wv, qv.w, acc[u][3]);
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kBiasThreads, 1) relpos_bwd_bias_kernel(const BwdArgs args) {
-  extern __shared__ float fsm[];
+  extern __shared__ __align__(16) float fsm[];
   const int H = args.H, W = args.W, N = args.N;
   const int bh = blockIdx.x / args.n_qtiles, qt = blockIdx.x - bh * args.n_qtiles;
   const int n0 = qt * kBlockM;
@@ -582,10 +717,10 @@ __global__ void __launch_bounds__(kBiasThreads, 1) relpos_bwd_bias_kernel(const 
   const int LH = 2 * H - 1, LW = 2 * W - 1;
   float* Th = fsm;
   float* Tw = Th + LH * kTStride;
-  float* dRh = Tw + LW * kTStride;                 // [128][H + 1]
+  float* Qf = Tw + LW * kTStride;                  // [128][68]
+  float* dRh = Qf + 128 * kTStride;                // [128][H + 1]
   float* dRw = dRh + 128 * (H + 1);                // [128][W + 1]
-  float* Qf = dRw + 128 * (W + 1);                 // [128][65]
-  int* qhv = reinterpret_cast<int*>(Qf + 128 * 65);
+  int* qhv = reinterpret_cast<int*>(dRw + 128 * (W + 1));
   int* qwv = qhv + 128;
   const int t = threadIdx.x;
   const size_t base = static_cast<size_t>(bh) * N + n0;
@@ -601,7 +736,7 @@ __global__ void __launch_bounds__(kBiasThreads, 1) relpos_bwd_bias_kernel(const 
   }
   for (int e = t; e < 128 * 64; e += kBiasThreads) {
     const int rr = e >> 6;
-    Qf[rr * 65 + (e & 63)] = rr < rows ? ld_in(args.q, base * 64 + e, args.in_fmt) : 0.f;
+    Qf[rr * kTStride + (e & 63)] = rr < rows ? ld_in(args.q, base * 64 + e, args.in_fmt) : 0.f;
   }
   if (t < 128) {
     const int n = n0 + t;
@@ -609,64 +744,82 @@ __global__ void __launch_bounds__(kBiasThreads, 1) relpos_bwd_bias_kernel(const 
     qwv[t] = n - (n / W) * W;
   }
   __syncthreads();
-  // dq = dq_s + sum_kh drel_h T_h[qh - kh + H - 1] + sum_kw drel_w T_w[qw - kw + W - 1]
+  // dq = dq_s + sum_kh drel_h T_h[qh - kh + H - 1] + sum_kw drel_w T_w[qw - kw + W - 1];
+  // a warp holds 32 consecutive rows (mostly one qh, so one T_h row) and one half of the columns
   {
-    const int rr = t >> 1, c0 = (t & 1) * 32;
+    const int rr = t & 127, c0 = (t >> 7) * 32;
     if (rr < rows) {
       const int qh = qhv[rr], qw = qwv[rr];
-      float acc[32];
-      const float* src = args.dq_s + (base + rr) * 64 + c0;
+      float4 acc[8];
+      const float4* src = reinterpret_cast<const float4*>(args.dq_s + (base + rr) * 64 + c0);
       #pragma unroll
-      for (int c = 0; c < 32; ++c) acc[c] = src[c];
+      for (int c = 0; c < 8; ++c) acc[c] = src[c];
       for (int kh = 0; kh < H; ++kh) {
-        const float w = dRh[rr * (H + 1) + kh];
-        const float* tr = Th + (qh - kh + H - 1) * kTStride + c0;
+        const float wv = dRh[rr * (H + 1) + kh];
+        const float4* tr = reinterpret_cast<const float4*>(Th + (qh - kh + H - 1) * kTStride + c0);
         #pragma unroll
-        for (int c = 0; c < 32; ++c) acc[c] = fmaf(w, tr[c], acc[c]);
+        for (int c = 0; c < 8; ++c) {
+          const float4 v = tr[c];
+          acc[c] = make_float4(fmaf(wv, v.x, acc[c].x), fmaf(wv, v.y, acc[c].y), fmaf(wv, v.z, acc[c].z),
+                               fmaf(wv, v.w, acc[c].w));
+        }
       }
       for (int kw = 0; kw < W; ++kw) {
-        const float w = dRw[rr * (W + 1) + kw];
-        const float* tr = Tw + (qw - kw + W - 1) * kTStride + c0;
+        const float wv = dRw[rr * (W + 1) + kw];
+        const float4* tr = reinterpret_cast<const float4*>(Tw + (qw - kw + W - 1) * kTStride + c0);
         #pragma unroll
-        for (int c = 0; c < 32; ++c) acc[c] = fmaf(w, tr[c], acc[c]);
+        for (int c = 0; c < 8; ++c) {
+          const float4 v = tr[c];
+          acc[c] = make_float4(fmaf(wv, v.x, acc[c].x), fmaf(wv, v.y, acc[c].y), fmaf(wv, v.z, acc[c].z),
+                               fmaf(wv, v.w, acc[c].w));
+        }
       }
       #pragma unroll
-      for (int c = 0; c < 32; c += 4)
-        st_grad4(args.dq, (base + rr) * 64 + c0 + c, acc[c], acc[c + 1], acc[c + 2], acc[c + 3], args.grad_fmt);
+      for (int c = 0; c < 8; ++c)
+        st_grad4(args.dq, (base + rr) * 64 + c0 + 4 * c, acc[c].x, acc[c].y, acc[c].z, acc[c].w, args.grad_fmt);
     }
   }
-  // partial table gradients of this tile: part_h[i][c] = sum over rows with
-  // kh = qh - i + H - 1 in range of drel_h[row][kh] q[row][c] (and the same for w)
+  // this tile's partial table gradients, in blocks of 4 table rows x 4 columns
   float* part = args.parts + static_cast<size_t>(blockIdx.x) * (LH + LW) * 64;
-  for (int o = t; o < (LH + LW) * 64; o += kBiasThreads) {
-    const int i = o >> 6, c = o & 63;
-    float acc = 0.f;
-    if (i < LH) {
-      for (int rr = 0; rr < rows; ++rr) {
-        const int kh = qhv[rr] - i + H - 1;
-        if (kh >= 0 && kh < H) acc = fmaf(dRh[rr * (H + 1) + kh], Qf[rr * 65 + c], acc);
-      }
-    } else {
-      const int iw = i - LH;
-      for (int rr = 0; rr < rows; ++rr) {
-        const int kw = qwv[rr] - iw + W - 1;
-        if (kw >= 0 && kw < W) acc = fmaf(dRw[rr * (W + 1) + kw], Qf[rr * 65 + c], acc);
-      }
-    }
-    part[o] = acc;
+  const int hb = (LH + 3) / 4, wb = (LW + 3) / 4;
+  for (int b = t; b < (hb + wb) * 16; b += kBiasThreads) {
+    const int ib = b >> 4, c0 = (b & 15) * 4;
+    const bool is_h = ib < hb;
+    const int i0 = 4 * (is_h ? ib : ib - hb);
+    const int L = is_h ? LH : LW;
+    float acc[4][4];
+    if (is_h) table_block(dRh, H + 1, qhv, H, Qf, rows, i0, c0, acc);
+    else table_block(dRw, W + 1, qwv, W, Qf, rows, i0, c0, acc);
+    float* dst = part + (is_h ? 0 : LH * 64);
+    #pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i0 + u < L)
+        *reinterpret_cast<float4*>(dst + (i0 + u) * 64 + c0) = make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
   }
 }
 
-// Tables kernel: dT = sum of the per-tile partials, in block order.
+// Tables kernel: dT = the sum of the per-tile partials.  A CTA of 256 threads
+// takes 32 consecutive outputs (coalesced reads); thread (o, c) adds the
+// partials of tiles c, c + 8, ..., and the eight chunk sums are added in a
+// fixed order, so the result never depends on scheduling.
 __global__ void relpos_bwd_tables_kernel(const BwdArgs args, int n_blocks) {
+  __shared__ float red[8][32];
   const int LH = 2 * args.H - 1, LW = 2 * args.W - 1;
   const int total = (LH + LW) * 64;
-  const int o = blockIdx.x * blockDim.x + threadIdx.x;
-  if (o >= total) return;
+  const int ol = threadIdx.x & 31, chunk = threadIdx.x >> 5;
+  const int o = blockIdx.x * 32 + ol;
   float acc = 0.f;
-  for (int b = 0; b < n_blocks; ++b) acc += args.parts[static_cast<size_t>(b) * total + o];
-  if (o < LH * 64) args.dth[o] = acc;
-  else args.dtw[o - LH * 64] = acc;
+  if (o < total)
+    for (int b = chunk; b < n_blocks; b += 8) acc += args.parts[static_cast<size_t>(b) * total + o];
+  red[chunk][ol] = acc;
+  __syncthreads();
+  if (chunk == 0 && o < total) {
+    float v = red[0][ol];
+    #pragma unroll
+    for (int c = 1; c < 8; ++c) v += red[c][ol];
+    if (o < LH * 64) args.dth[o] = v;
+    else args.dtw[o - LH * 64] = v;
+  }
 }
 
 }  // namespace dera
