@@ -150,13 +150,13 @@ __device__ __forceinline__ void bwd_teardown(uint32_t tbase, int warp) {
 }
 
 // ---------------------------------------------------------------------------
-// Rows kernel: one CTA per (head, query tile).  Warps 2-9 are the softmax
-// threads, two per query row: warps w and w + 4 share TMEM lane quarter w % 4
-// and take the first and the second half of every key tile's 16-column
-// blocks.  TMEM columns: S [0, 128), dP [128, 256), dZ in the input dtype as
-// packed pairs [256, 320), the dZ k accumulator [320, 384).  The two halves
-// add their bias-gradient sums in shared memory (two addends per entry, so
-// the result does not depend on their order).
+// Rows kernel: one CTA per (head, query tile).  From warp 2 on, the softmax
+// threads: one per query row (TMEM lane), or, with two groups, two per row
+// (warps w and w + 4 share TMEM lane quarter w % 4 and take the first and the
+// second half of every key tile's 16-column blocks).  TMEM columns: S [0, 128),
+// dP [128, 256), dZ in the input dtype as packed pairs [256, 320), the dZ k
+// accumulator [320, 384).  The bias-gradient sums meet in shared memory, with
+// at most two addends per entry, so their order does not change the result.
 // Softmax thread groups of the rows kernel: 1 (one thread per query row) or 2
 // (two per row, each taking half of every key tile's columns).  One measured as
 // fast on the 64x64 grid and 5-10 % faster on the 40x40 grid and 14x14 windows.
@@ -184,9 +184,10 @@ struct RowsSplit {
   }
 };
 
-// The softmax role of the rows kernel for one half of the threads.  With 64
-// key columns per grid row the halves split every grid row's columns (kw below
-// or above 32), so each thread keeps 32 rel_w terms and 32 column sums in
+// The softmax role of the rows kernel for one group of threads: HALF 2 is the
+// single group (every column); with two groups, HALF 0 and 1.  With 64 key
+// columns per grid row the halves split every grid row's columns (kw below or
+// above 32), so each thread keeps 32 rel_w terms and 32 column sums in
 // registers; with narrower rows they split each key tile's 16-column blocks
 // into a first and a second half.
 template <int WP, bool BF16, int HALF>
