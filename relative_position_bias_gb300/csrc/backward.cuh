@@ -91,7 +91,9 @@ enum : int {
 };
 // rows kernel: a two-stage K/V ring; staging holds the rel_h rows and the
 // bias-gradient accumulators, 3 x 128 rows of 65 floats
-using BwdRowsSmem = BwdSmem<2, 3 * 128 * 65 * 4>;
+// (one group of softmax threads: a three-stage ring, and only the rel_h rows)
+constexpr int kRowsGroupsCfg = 1;
+using BwdRowsSmem = BwdSmem<kRowsGroupsCfg == 1 ? 3 : 2, (kRowsGroupsCfg == 1 ? 1 : 3) * 128 * 65 * 4>;
 // cols kernel: a three-stage Q/dO ring; staging holds two buffers of one query
 // tile's rel_w, rel_h entries, lse and D, transposed (74 rows of 132 floats each)
 constexpr int kColsStageRow = 132;
@@ -160,7 +162,7 @@ __device__ __forceinline__ void bwd_teardown(uint32_t tbase, int warp) {
 // Softmax thread groups of the rows kernel: 1 (one thread per query row) or 2
 // (two per row, each taking half of every key tile's columns).  One measured as
 // fast on the 64x64 grid and 5-10 % faster on the 40x40 grid and 14x14 windows.
-constexpr int kRowsGroups = 1;
+constexpr int kRowsGroups = kRowsGroupsCfg;
 constexpr int kBwdRowsThreads = 64 + 128 * kRowsGroups;
 
 // Which 16-column blocks of a key tile a half of the rows kernel's softmax
@@ -224,7 +226,8 @@ __device__ __forceinline__ void rows_softmax(const BwdArgs& args, uint8_t* smem,
     for (int kh = 0; kh < Hpad; ++kh)
       bh_row[kh] = (kh < H) ? (row_valid ? kLog2e * args.rel_h[row * H + kh] : 0.f) : NEG_INF;
   }
-  for (int e = t; e < 2 * 128 * 65; e += kRowsGroups * kBlockM) stg[128 * 65 + e] = 0.f;
+  if (!kAll)
+    for (int e = t; e < 2 * 128 * 65; e += kRowsGroups * kBlockM) stg[128 * 65 + e] = 0.f;
   float bw[kLW];
   #pragma unroll
   for (int i = 0; i < kLW; ++i) {
@@ -249,7 +252,7 @@ __device__ __forceinline__ void rows_softmax(const BwdArgs& args, uint8_t* smem,
     ++stg_phase;
     return warp_all(w);
   };
-  bool ok = group_sync();   // bh_row written, accumulators cleared
+  bool ok = kAll ? true : group_sync();   // bh_row written, accumulators cleared
   float dRW[kLW];
   #pragma unroll
   for (int i = 0; i < kLW; ++i) dRW[i] = 0.f;
@@ -305,12 +308,26 @@ __device__ __forceinline__ void rows_softmax(const BwdArgs& args, uint8_t* smem,
     tmem_wait_st();
     tc_fence_before();
     mbar_arrive(&bars[kBwPFull]);
-    // two addends per entry (one per half), so their order does not matter
-    #pragma unroll
-    for (int g = 0; g < KHT; ++g)
-      if (j * KHT + g < H) atomicAdd(&dRH_sm[j * KHT + g], dRH[g]);
+    if (kAll) {
+      if (row_valid) {
+        #pragma unroll
+        for (int g = 0; g < KHT; ++g)
+          if (j * KHT + g < H) args.drel_h[row * H + j * KHT + g] = dRH[g];
+      }
+    } else {
+      // two addends per entry (one per half), so their order does not matter
+      #pragma unroll
+      for (int g = 0; g < KHT; ++g)
+        if (j * KHT + g < H) atomicAdd(&dRH_sm[j * KHT + g], dRH[g]);
+    }
   }
-  if (kSplitKw) {
+  if (kAll) {
+    if (ok && row_valid) {
+      #pragma unroll
+      for (int i = 0; i < kLW; ++i)
+        if (i < W) args.drel_w[row * W + i] = dRW[i];
+    }
+  } else if (kSplitKw) {
     // each half owns its columns
     if (ok && row_valid) {
       #pragma unroll
@@ -322,12 +339,14 @@ __device__ __forceinline__ void rows_softmax(const BwdArgs& args, uint8_t* smem,
     for (int i = 0; i < kLW; ++i)
       if (i < W) atomicAdd(&dRW_sm[i], dRW[i]);
   }
-  if (ok) ok = group_sync();
-  if (ok && row_valid) {
-    if (HALF != 1)
-      for (int kh = 0; kh < H; ++kh) args.drel_h[row * H + kh] = dRH_sm[kh];
-    if (HALF != 0 && !kSplitKw)
-      for (int kw = 0; kw < W; ++kw) args.drel_w[row * W + kw] = dRW_sm[kw];
+  if (!kAll) {
+    if (ok) ok = group_sync();
+    if (ok && row_valid) {
+      if (HALF == 0)
+        for (int kh = 0; kh < H; ++kh) args.drel_h[row * H + kh] = dRH_sm[kh];
+      if (HALF == 1 && !kSplitKw)
+        for (int kw = 0; kw < W; ++kw) args.drel_w[row * W + kw] = dRW_sm[kw];
+    }
   }
   if (ok) ok = warp_all(mbar_wait(&bars[kBwMmaDone], (n_kv - 1) & 1, abort_flag, status));
   if (ok) {
@@ -356,7 +375,7 @@ relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        const BwdArgs args) {
   using KT = KeyTile<WP, 64>;
-  constexpr int KHT = KT::KHT, BN = KT::BN, KS = 2;
+  constexpr int KHT = KT::KHT, BN = KT::BN, KS = kRowsGroups == 1 ? 3 : 2;
   using SM = BwdRowsSmem;
   constexpr int fmt = BF16 ? kBF16 : kF16;
   extern __shared__ uint8_t smem_raw[];
@@ -600,6 +619,7 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
       const float* lseT = buf + 72 * RS;
       const float* DT = buf + 73 * RS;
       const int rows = min(kBlockM, N - i * kBlockM);
+      const bool full = rows == kBlockM;
       ok = warp_all(mbar_wait(&bars[kBwSFull], i & 1, abort_flag, status));
       if (!ok) break;
       tc_fence_after();
@@ -633,14 +653,16 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
           const float bw4[4] = {w4.x + h4.x, w4.y + h4.y, w4.z + h4.z, w4.w + h4.w};
           const float ls4[4] = {l4.x, l4.y, l4.z, l4.w};
           const float dd4[4] = {d4.x, d4.y, d4.z, d4.w};
+          // Query columns past N must not reach dv or dk; key slots without a key
+          // need no mask, since their P^T and dZ^T rows only reach their own
+          // (unstored) rows of dv and dk.
           float p4[4], z4[4];
           #pragma unroll
           for (int h = 0; h < 4; ++h) {
-            const bool v = key_valid && c4 + h < rows;
             const float x = fmaf(__uint_as_float(us[q & 1][k4 + h]), sl2, fmaf(bw4[h], kLog2e, -ls4[h]));
-            const float p = v ? ex2_approx(x) : 0.f;
+            const float p = (full || c4 + h < rows) ? ex2_approx(x) : 0.f;
             p4[h] = p;
-            z4[h] = v ? p * (__uint_as_float(up[q & 1][k4 + h]) - dd4[h]) : 0.f;
+            z4[h] = p * (__uint_as_float(up[q & 1][k4 + h]) - dd4[h]);
           }
           pp[k4 / 2] = pack_in(p4[0], p4[1], fmt);
           pp[k4 / 2 + 1] = pack_in(p4[2], p4[3], fmt);
@@ -705,6 +727,7 @@ __device__ __forceinline__ void table_block(const float* dR, int ld, const int* 
   for (int u = 0; u < 4; ++u)
     #pragma unroll
     for (int k = 0; k < 4; ++k) acc[u][k] = 0.f;
+  #pragma unroll 4
   for (int rr = 0; rr < rows; ++rr) {
     const int kk0 = coord[rr] - i0 + Lg - 1;
     const float4 qv = *reinterpret_cast<const float4*>(Qf + rr * kTStride + c0);
