@@ -581,9 +581,18 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
       const int n0 = i * kBlockM;
       const int rows = min(kBlockM, N - n0);
       const size_t base = static_cast<size_t>(bh) * N + n0;
+      // the tile's rel_w rows are one contiguous block: element e = rr W + c,
+      // its (rr, c) advanced without a division per element
+      const int step_r = (2 * kBlockM) / W, step_c = (2 * kBlockM) - step_r * W;
+      int rr = t / W, c = t - (t / W) * W;
       for (int e = t; e < kBlockM * W; e += 2 * kBlockM) {
-        const int rr = e / W, c = e - rr * W;
         cp_async4(buf + c * RS + rr, args.rel_w + (rr < rows ? base * W + e : 0), rr < rows ? 4u : 0u);
+        rr += step_r;
+        c += step_c;
+        if (c >= W) {
+          c -= W;
+          ++rr;
+        }
       }
       for (int e = t; e < kBlockM * KHT; e += 2 * kBlockM) {
         const int rr = e / KHT, gg = e - rr * KHT, khh = j * KHT + gg;
