@@ -8,8 +8,12 @@ range and nothing is exchanged while computing.  Only a consumer that needs the
 whole output gathers it afterwards (``gather=True``), with one all-gather of
 the output slices over the process group.
 
+The backward splits the same way, with one exchange step: the tables are
+shared by every (batch, head), so their gradients are the sum over ranks of
+each rank's partial gradients (``fused_backward_shard``).
+
 This module holds no arithmetic of the method: it slices, calls the library
-entry point on the slice, and (optionally) gathers.
+entry point on the slice, gathers, and adds the ranks' table-gradient partials.
 """
 from __future__ import annotations
 
@@ -68,3 +72,38 @@ def fused_shard(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, rel_pos_h: to
         a, b = bh_range(BH, r, world)
         out[a:b] = bufs[r][:b - a]
     return out
+
+
+def fused_backward_shard(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, rel_pos_h: torch.Tensor,
+                         rel_pos_w: torch.Tensor, out: torch.Tensor, lse: torch.Tensor, dout: torch.Tensor, H: int,
+                         W: int, scale: float | None = None, *, rank: int | None = None, world: int | None = None,
+                         group=None, compute: Callable[..., tuple] | None = None, **kwargs):
+    """This rank's share of one backward call: ``(dq, dk, dv, drel_pos_h, drel_pos_w)``.
+
+    Every tensor with a leading BH dimension (q, k, v, out, lse, dout) is the whole call's; only
+    the rank's range is read, and dq, dk, dv come back for that range.  The tables are shared by
+    every (batch, head), so their gradients are the sum of all ranks' partial gradients: the one
+    exchange step of the backward.  The partials are all-gathered and added in rank order, so
+    every rank holds the same table gradients, bit for bit, whatever the backend.  `compute`
+    defaults to the library's backward entry point; extra keyword arguments go to it."""
+    if rank is None or world is None:
+        if dist.is_available() and dist.is_initialized():
+            rank, world = dist.get_rank(group), dist.get_world_size(group)
+        else:
+            rank, world = 0, 1
+    BH = q.shape[0]
+    lo, hi = bh_range(BH, rank, world)
+    fn = compute or api.fused_backward
+    dq, dk, dv, dth, dtw = fn(q[lo:hi], k[lo:hi], v[lo:hi], rel_pos_h, rel_pos_w, out[lo:hi], lse[lo:hi],
+                              dout[lo:hi], H, W, scale, **kwargs)
+    if world == 1:
+        return dq, dk, dv, dth, dtw
+    summed = []
+    for part in (dth, dtw):
+        bufs = [torch.empty_like(part) for _ in range(world)]
+        dist.all_gather(bufs, part.contiguous(), group=group)
+        total = bufs[0].clone()
+        for r in range(1, world):
+            total += bufs[r]
+        summed.append(total)
+    return dq, dk, dv, summed[0], summed[1]

@@ -137,3 +137,42 @@ def test_sharded_call_gathers_to_the_single_rank_result(tmp_path, world, BH):
         assert torch.equal(rec["part"], want[rec["lo"]:rec["hi"]])
         covered.extend(range(rec["lo"], rec["hi"]))
     assert covered == list(range(BH))
+
+
+# --------------------------------------------------------------------------- the backward's exchange step
+def _oracle_backward(q, k, v, th, tw, out, lse, dout, H, W, scale, **_):
+    """CPU stand-in for one rank's backward (the float64 oracle on the slice; out and lse unused)."""
+    g = oracle.fused_backward(q.double().numpy(), k.double().numpy(), v.double().numpy(), th.double().numpy(),
+                              tw.double().numpy(), H, W, scale, dout.double().numpy())
+    return tuple(torch.from_numpy(x) for x in g)
+
+
+def _bwd_worker(rank: int, world: int, port: int, out_dir: str, BH: int):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    q, k, v, th, tw, H, W, scale = _shard_case(BH)
+    dout = torch.randn(q.shape, generator=torch.Generator().manual_seed(11))
+    out = torch.zeros_like(q)
+    lse = torch.zeros(q.shape[:2])
+    g = shard.fused_backward_shard(q, k, v, th, tw, out, lse, dout, H, W, scale, compute=_oracle_backward)
+    lo, hi = shard.bh_range(BH, rank, world)
+    torch.save({"lo": lo, "hi": hi, "g": g}, os.path.join(out_dir, f"b{rank}.pt"))
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world,BH", [(2, 7), (3, 5), (3, 2)])
+def test_sharded_backward_sums_the_table_gradients(tmp_path, world, BH):
+    """dq, dk, dv of a rank are its slice of the whole call's; the table gradients, summed over the
+    ranks' partials in rank order, equal the whole call's and are the same on every rank."""
+    mp.spawn(_bwd_worker, args=(world, _free_port(), str(tmp_path), BH), nprocs=world, join=True)
+    q, k, v, th, tw, H, W, scale = _shard_case(BH)
+    dout = torch.randn(q.shape, generator=torch.Generator().manual_seed(11))
+    want = _oracle_backward(q, k, v, th, tw, None, None, dout, H, W, scale)
+    recs = [torch.load(tmp_path / f"b{r}.pt") for r in range(world)]
+    for r, rec in enumerate(recs):
+        lo, hi = rec["lo"], rec["hi"]
+        for i in range(3):
+            assert torch.equal(rec["g"][i], want[i][lo:hi]), f"rank {r}: gradient {i} is not its slice"
+        for i in (3, 4):
+            assert torch.allclose(rec["g"][i], want[i], rtol=0, atol=1e-12)
+            assert torch.equal(rec["g"][i], recs[0]["g"][i])   # every rank holds the same sum

@@ -48,3 +48,27 @@ def test_rank_slices_concatenate_to_the_whole_call(name, world):
     # both are within 4e-3 of the float64 oracle (the parity tests), so within 8e-3 of each other
     assert err.max() <= 8e-3, f"max-abs {err.max():.3e}"
     assert np.linalg.norm(got - want) / np.linalg.norm(want) <= 1e-2
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_backward_rank_slices(world):
+    """The backward's dq, dk, dv for a rank's BH range are exactly the whole call's rows (every
+    CTA works within one (batch, head)); the ranks' table-gradient partials add up to the whole
+    call's table gradients."""
+    w = I.WORKLOADS["global64"]
+    x = I.make_inputs(w)
+    d = {k: t.cuda() for k, t in x.items()}
+    fargs = (d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W, w.scale)
+    out, lse = rpb.fused_lse(*fargs, out_dtype=torch.float32)
+    dout = torch.randn(w.BH, w.N, w.d, generator=torch.Generator().manual_seed(4)).to(w.torch_dtype).cuda()
+    whole = rpb.fused_backward(d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], out, lse, dout, w.H, w.W,
+                               w.scale)
+    parts = [shard.fused_backward_shard(d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], out, lse, dout,
+                                        w.H, w.W, w.scale, rank=r, world=world) for r in range(world)]
+    torch.cuda.synchronize()
+    for i in range(3):
+        assert torch.equal(torch.cat([p[i] for p in parts]), whole[i])
+    for i in (3, 4):
+        total = sum(p[i].double() for p in parts)
+        ref = whole[i].double()
+        assert float((total - ref).abs().max()) <= 1e-4 * float(ref.abs().max())
