@@ -77,15 +77,18 @@ def fused_shard(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, rel_pos_h: to
 def fused_backward_shard(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, rel_pos_h: torch.Tensor,
                          rel_pos_w: torch.Tensor, out: torch.Tensor, lse: torch.Tensor, dout: torch.Tensor, H: int,
                          W: int, scale: float | None = None, *, rank: int | None = None, world: int | None = None,
-                         group=None, compute: Callable[..., tuple] | None = None, **kwargs):
+                         group=None, reduce_tables: bool = True, compute: Callable[..., tuple] | None = None,
+                         **kwargs):
     """This rank's share of one backward call: ``(dq, dk, dv, drel_pos_h, drel_pos_w)``.
 
     Every tensor with a leading BH dimension (q, k, v, out, lse, dout) is the whole call's; only
     the rank's range is read, and dq, dk, dv come back for that range.  The tables are shared by
     every (batch, head), so their gradients are the sum of all ranks' partial gradients: the one
     exchange step of the backward.  The partials are all-gathered and added in rank order, so
-    every rank holds the same table gradients, bit for bit, whatever the backend.  `compute`
-    defaults to the library's backward entry point; extra keyword arguments go to it."""
+    every rank holds the same table gradients, bit for bit, whatever the backend.  With
+    ``reduce_tables=False`` the rank's partial table gradients come back instead (no process
+    group needed).  `compute` defaults to the library's backward entry point; extra keyword
+    arguments go to it."""
     if rank is None or world is None:
         if dist.is_available() and dist.is_initialized():
             rank, world = dist.get_rank(group), dist.get_world_size(group)
@@ -96,7 +99,7 @@ def fused_backward_shard(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, rel_
     fn = compute or api.fused_backward
     dq, dk, dv, dth, dtw = fn(q[lo:hi], k[lo:hi], v[lo:hi], rel_pos_h, rel_pos_w, out[lo:hi], lse[lo:hi],
                               dout[lo:hi], H, W, scale, **kwargs)
-    if world == 1:
+    if world == 1 or not reduce_tables:
         return dq, dk, dv, dth, dtw
     summed = []
     for part in (dth, dtw):
