@@ -203,7 +203,8 @@ DERA_API dera_status dera_relpos_backward_workspace_size(int BH, int H, int W, i
  *      Nothing is accumulated with atomics: the result is the same on every run.
  * Errors: DERA_ERR_HEAD_DIM unless head_dim is 64; DERA_ERR_SCRATCH if the
  *      workspace is NULL or smaller than the size above; otherwise as for
- *      dera_relpos_fused.
+ *      dera_relpos_fused.  With BH = 0 only drel_pos_h and drel_pos_w are
+ *      read (as pointers) and written, with zeros; the other pointers may be NULL.
  */
 DERA_API dera_status dera_relpos_fused_backward(const void* q, const void* k, const void* v, const void* rel_pos_h,
                                        const void* rel_pos_w, const void* out, const float* lse,

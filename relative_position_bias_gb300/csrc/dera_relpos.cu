@@ -518,12 +518,13 @@ dera_status dera_relpos_fused_backward(const void* q, const void* k, const void*
   if (!is16(in_dtype) || !(out_dtype == DERA_F32 || out_dtype == in_dtype) ||
       !(grad_dtype == DERA_F32 || grad_dtype == in_dtype))
     return DERA_ERR_DTYPE;
-  DERA_TRY(check_host({q, k, v, rel_pos_h, rel_pos_w, out, lse, dout, dq, dk, dv, drel_pos_h, drel_pos_w}));
   int dev = 0;
-  DERA_TRY(current_device(&dev));
-  const BwdLayout L(BH, H, W);
   if (BH == 0) {
-    // no rows: the table gradients are zero
+    // no rows: only the table gradients are written, as zeros
+    DERA_TRY(check_host({drel_pos_h, drel_pos_w}));
+    DERA_TRY(current_device(&dev));
+    for (const void* p : {static_cast<const void*>(drel_pos_h), static_cast<const void*>(drel_pos_w)})
+      DERA_TRY(check_ptr(p, dev));
     const size_t th_bytes = static_cast<size_t>(2 * H - 1) * 64 * sizeof(float);
     const size_t tw_bytes = static_cast<size_t>(2 * W - 1) * 64 * sizeof(float);
     cudaStream_t s0 = static_cast<cudaStream_t>(stream);
@@ -532,6 +533,9 @@ dera_status dera_relpos_fused_backward(const void* q, const void* k, const void*
       return DERA_ERR_CUDA;
     return DERA_OK;
   }
+  DERA_TRY(check_host({q, k, v, rel_pos_h, rel_pos_w, out, lse, dout, dq, dk, dv, drel_pos_h, drel_pos_w}));
+  DERA_TRY(current_device(&dev));
+  const BwdLayout L(BH, H, W);
   if (!workspace || workspace_bytes < L.total) return DERA_ERR_SCRATCH;
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return DERA_ERR_ALIGN;
   for (const void* p : {q, k, v, rel_pos_h, rel_pos_w, out, static_cast<const void*>(lse), dout,
