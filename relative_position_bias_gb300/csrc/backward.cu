@@ -1,6 +1,5 @@
 // Launchers of the backward kernels (csrc/backward.cuh): the two attention
-// kernels for every padded width and input dtype, then the bias and table
-// kernels.
+// kernels for every padded width and input dtype, then the table reduction.
 #include "backward.cuh"
 #include "launch.cuh"
 
@@ -17,7 +16,8 @@ cudaError_t launch_bwd_attn(const BwdMaps& maps, const BwdArgs& args, cudaStream
   e = cudaFuncSetAttribute(cols, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdColsSmem::kAlloc);
   if (e != cudaSuccess) return e;
   const unsigned grid_rows = static_cast<unsigned>(args.BH) * static_cast<unsigned>(args.n_qtiles);
-  rows<<<grid_rows, kBwdRowsThreads, BwdRowsSmem::kAlloc, stream>>>(maps.q, maps.dout, maps.k, maps.v, args);
+  rows<<<grid_rows, kBwdRowsThreads, BwdRowsSmem::kAlloc, stream>>>(maps.q, maps.dout, maps.k, maps.v, maps.th,
+                                                                     maps.tw, args);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const unsigned grid_cols = static_cast<unsigned>(args.BH) * static_cast<unsigned>(args.n_kv);
@@ -42,13 +42,7 @@ cudaError_t launch_backward(const BwdMaps& maps, const BwdArgs& args, int WP, cu
     default: e = launch_bwd_attn_w<64>(maps, args, stream); break;
   }
   if (e != cudaSuccess) return e;
-  const int bias_bytes = bias_smem_floats(args.H, args.W) * static_cast<int>(sizeof(float));
-  e = cudaFuncSetAttribute(relpos_bwd_bias_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bias_bytes);
-  if (e != cudaSuccess) return e;
   const unsigned blocks = static_cast<unsigned>(args.BH) * static_cast<unsigned>(args.n_qtiles);
-  relpos_bwd_bias_kernel<<<blocks, kBiasThreads, bias_bytes, stream>>>(args);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
   const int total = (2 * args.H - 1 + 2 * args.W - 1) * 64;
   relpos_bwd_tables_kernel<<<(total + 31) / 32, 256, 0, stream>>>(args, static_cast<int>(blocks));
   return cudaGetLastError();

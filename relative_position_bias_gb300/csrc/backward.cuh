@@ -87,13 +87,15 @@ enum : int {
   kBwPFull = kBwSFull + 1,                 // softmax threads wrote dZ (and P^T), read S and dP (count 128)
   kBwMmaDone = kBwPFull + 1,               // the products that read dZ (and P^T) of a tile are complete
   kBwStg = kBwMmaDone + 1,                 // staging barrier of the softmax threads (count 128)
-  kBwCount = kBwStg + 1
+  kBwAllDone = kBwStg + 1,                 // rows kernel: every product of the key-tile loop is complete
+  kBwTFull = kBwAllDone + 1,               // rows kernel: both tables landed
+  kBwGFull = kBwTFull + 1,                 // rows kernel: the softmax threads wrote dG and dG^T (count 128)
+  kBwBDone = kBwGFull + 1,                 // rows kernel: the bias products of one table are complete
+  kBwCount = kBwBDone + 1
 };
-// rows kernel: a two-stage K/V ring; staging holds the rel_h rows and the
-// bias-gradient accumulators, 3 x 128 rows of 65 floats
-// (one group of softmax threads: a three-stage ring, and only the rel_h rows)
-constexpr int kRowsGroupsCfg = 1;
-using BwdRowsSmem = BwdSmem<kRowsGroupsCfg == 1 ? 3 : 2, (kRowsGroupsCfg == 1 ? 1 : 3) * 128 * 65 * 4>;
+// rows kernel: a three-stage K/V ring; staging holds each thread's rel_h row
+// (later its drel_h row) and its drel_w row, 2 x 128 rows of 65 floats
+using BwdRowsSmem = BwdSmem<3, 2 * 128 * 65 * 4>;
 // cols kernel: a three-stage Q/dO ring; staging holds two buffers of one query
 // tile's rel_w, rel_h entries, lse and D, transposed (74 rows of 132 floats each)
 constexpr int kColsStageRow = 132;
@@ -129,6 +131,10 @@ __device__ __forceinline__ BwdCta bwd_setup(uint8_t* smem_raw, int warp, int n_c
     mbar_init(&c.bars[kBwPFull], n_compute);
     mbar_init(&c.bars[kBwMmaDone], 1);
     mbar_init(&c.bars[kBwStg], n_compute);
+    mbar_init(&c.bars[kBwAllDone], 1);
+    mbar_init(&c.bars[kBwTFull], 1);
+    mbar_init(&c.bars[kBwGFull], n_compute);
+    mbar_init(&c.bars[kBwBDone], 1);
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -152,235 +158,41 @@ __device__ __forceinline__ void bwd_teardown(uint32_t tbase, int warp) {
 }
 
 // ---------------------------------------------------------------------------
-// Rows kernel: one CTA per (head, query tile).  From warp 2 on, the softmax
-// threads: one per query row (TMEM lane), or, with two groups, two per row
-// (warps w and w + 4 share TMEM lane quarter w % 4 and take the first and the
-// second half of every key tile's 16-column blocks).  TMEM columns: S [0, 128),
-// dP [128, 256), dZ in the input dtype as packed pairs [256, 320), the dZ k
-// accumulator [320, 384).  The bias-gradient sums meet in shared memory, with
-// at most two addends per entry, so their order does not change the result.
-// Softmax thread groups of the rows kernel: 1 (one thread per query row) or 2
-// (two per row, each taking half of every key tile's columns).  One measured as
-// fast on the 64x64 grid and 5-10 % faster on the 40x40 grid and 14x14 windows.
-constexpr int kRowsGroups = kRowsGroupsCfg;
-constexpr int kBwdRowsThreads = 64 + 128 * kRowsGroups;
+// Rows kernel: one CTA per (head, query tile), 192 threads: warp 0 TMA, warp 1
+// MMA, warps 2-5 the softmax threads, one per query row (TMEM lane).
+//  - Key-tile loop: S = q k^T and dP = dO v^T (SS) into TMEM; P and dZ on the
+//    softmax threads; dZ k (TS) accumulated in TMEM.  The sums of dZ over each
+//    key grid row's columns (drel_h) and over the grid rows (drel_w) stay on
+//    chip.
+//  - Epilogue, on the tensor core, one table at a time: the bias gradient,
+//    unskewed into dG[r][i] = drel[r][coord(r) - i + L - 1] (input dtype),
+//    gives dq's part through the projection, dG T, and the tile's table-gradient
+//    partial, dG^T q.  dG and its transpose sit in two ring stages so that both
+//    products read a K-major A; the tables arrive in the third.
+// TMEM columns: S [0, 128), dP [128, 256), dZ [256, 320), dZ k [320, 384); in
+// the epilogue dG T [0, 64), dG_h^T q [128, 192), dG_w^T q [192, 256).
+constexpr int kBwdRowsThreads = 192;
 
-// Which 16-column blocks of a key tile a half of the rows kernel's softmax
-// threads takes (see rows_softmax), and their order.
-template <int WP, int HALF>
-struct RowsSplit {
-  static constexpr int kBlocks = KeyTile<WP, 64>::BN / 16, kHalf0 = (kBlocks + 1) / 2;
-  __host__ __device__ static constexpr bool mine(int bb) {
-    if (HALF == 2) return true;   // one group takes every block
-    return WP == 64 ? ((16 * bb) % 64) / 32 == HALF : (HALF == 0 ? bb < kHalf0 : bb >= kHalf0);
-  }
-  __host__ __device__ static constexpr int next(int bb) {
-    for (int x = bb + 1; x < kBlocks; ++x)
-      if (mine(x)) return x;
-    return kBlocks;
-  }
-  __host__ __device__ static constexpr int rank(int bb) {
-    int c = 0;
-    for (int x = 0; x < bb; ++x) c += mine(x) ? 1 : 0;
-    return c;
-  }
-};
-
-// The softmax role of the rows kernel for one group of threads: HALF 2 is the
-// single group (every column); with two groups, HALF 0 and 1.  With 64 key
-// columns per grid row the halves split every grid row's columns (kw below or
-// above 32), so each thread keeps 32 rel_w terms and 32 column sums in
-// registers; with narrower rows they split each key tile's 16-column blocks
-// into a first and a second half.
-template <int WP, bool BF16, int HALF>
-__device__ __forceinline__ void rows_softmax(const BwdArgs& args, uint8_t* smem, uint64_t* bars,
-                                             volatile int* abort_flag, uint32_t tbase, int warp, int lane, int bh,
-                                             int qt) {
-  using KT = KeyTile<WP, 64>;
-  constexpr int KHT = KT::KHT, BN = KT::BN;
-  using SM = BwdRowsSmem;
-  constexpr int fmt = BF16 ? kBF16 : kF16;
-  constexpr bool kAll = HALF == 2;   // a single group of softmax threads
-  constexpr bool kSplitKw = WP == 64 && !kAll;
-  constexpr int kLW = kSplitKw ? 32 : WP;              // rel_w terms a thread keeps
-  constexpr int kKw0 = kSplitKw ? 32 * HALF : 0;       // first of them
-  constexpr int kBlocks = BN / 16;
-  int* status = args.status;
-  const int n_kv = args.n_kv, H = args.H, W = args.W, N = args.N;
-  const int wq = warp & 3;
-  const int r = wq * 32 + lane;
-  const int t = threadIdx.x - 64;          // index among the softmax threads
-  const int n = qt * kBlockM + r;
-  const bool row_valid = n < N;
-  const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-  const uint32_t tS = tbase + lane_off, tdP = tS + 128, tdZ = tS + 256, tdQ = tS + 320;
-  const size_t row = static_cast<size_t>(bh) * N + (row_valid ? n : 0);
-  const float NEG_INF = -__int_as_float(0x7f800000);
-  const float sl2 = args.scale_log2;
-  float* stg = reinterpret_cast<float*>(smem + SM::kStaging);
-  float* bh_row = stg + r * 65;                          // rel_h row (base 2)
-  float* dRH_sm = stg + 128 * 65 + r * 65;               // per key grid row: sum over its columns
-  float* dRW_sm = stg + 2 * 128 * 65 + r * 65;           // per key column: sum over grid rows
-  const int Hpad = n_kv * KHT;
-  if (HALF != 1) {
-    for (int kh = 0; kh < Hpad; ++kh)
-      bh_row[kh] = (kh < H) ? (row_valid ? kLog2e * args.rel_h[row * H + kh] : 0.f) : NEG_INF;
-  }
-  if (!kAll)
-    for (int e = t; e < 2 * 128 * 65; e += kRowsGroups * kBlockM) stg[128 * 65 + e] = 0.f;
-  float bw[kLW];
-  #pragma unroll
-  for (int i = 0; i < kLW; ++i) {
-    const int kw = kKw0 + i;
-    bw[i] = (kw < W) ? (row_valid ? kLog2e * args.rel_w[row * W + kw] : 0.f) : NEG_INF;
-  }
-  const float lse2 = row_valid ? args.lse[row] : 0.f;
-  // D = dO . out for this row (out in fp32 or in the input dtype)
-  float Dn = 0.f;
-  if (row_valid) {
-    for (int c = 0; c < 64; ++c) {
-      const float o = args.out_fmt == kF32 ? reinterpret_cast<const float*>(args.out)[row * 64 + c]
-                                            : ld_in(args.out, row * 64 + c, fmt);
-      Dn = fmaf(ld_in(args.dout, row * 64 + c, fmt), o, Dn);
-    }
-    if (HALF != 1) args.D[row] = Dn;
-  }
-  uint32_t stg_phase = 0;
-  auto group_sync = [&]() -> bool {
-    mbar_arrive(&bars[kBwStg]);
-    const bool w = mbar_wait(&bars[kBwStg], stg_phase & 1, abort_flag, status);
-    ++stg_phase;
-    return warp_all(w);
-  };
-  bool ok = kAll ? true : group_sync();   // bh_row written, accumulators cleared
-  float dRW[kLW];
-  #pragma unroll
-  for (int i = 0; i < kLW; ++i) dRW[i] = 0.f;
-  for (int j = 0; ok && j < n_kv; ++j) {
-    float bhv[KHT];
-    #pragma unroll
-    for (int g = 0; g < KHT; ++g) bhv[g] = bh_row[j * KHT + g];
-    ok = warp_all(mbar_wait(&bars[kBwSFull], j & 1, abort_flag, status));
-    if (!ok) break;
-    tc_fence_after();
-    if (j > 0) {
-      // dZ(j-1) has been read by its product before dZ(j) is written
-      ok = warp_all(mbar_wait(&bars[kBwMmaDone], (j - 1) & 1, abort_flag, status));
-      if (!ok) break;
-      tc_fence_after();
-    }
-    float dRH[KHT];
-    #pragma unroll
-    for (int g = 0; g < KHT; ++g) dRH[g] = 0.f;
-    // this half's blocks, the next block's S and dP loads in flight while the
-    // current one is computed
-    using RS = RowsSplit<WP, HALF>;
-    uint32_t us[2][16], up[2][16];
-    tmem_ld16(tS + 16 * RS::next(-1), us[0]);
-    tmem_ld16(tdP + 16 * RS::next(-1), up[0]);
-    #pragma unroll
-    for (int bb = 0; bb < kBlocks; ++bb) {
-      if (!RS::mine(bb)) continue;
-      const int cb = 16 * bb;
-      const int cur = RS::rank(bb) & 1;
-      tmem_wait_ld();
-      if (RS::next(bb) < kBlocks) {
-        tmem_ld16(tS + 16 * RS::next(bb), us[cur ^ 1]);
-        tmem_ld16(tdP + 16 * RS::next(bb), up[cur ^ 1]);
-      }
-      uint32_t pk[8];
-      #pragma unroll
-      for (int k = 0; k < 16; k += 2) {
-        const int col = cb + k;
-        const int g = col / WP, i = col % WP - kKw0;
-        const float x0 = fmaf(__uint_as_float(us[cur][k]), sl2, bw[i] + bhv[g]) - lse2;
-        const float x1 = fmaf(__uint_as_float(us[cur][k + 1]), sl2, bw[i + 1] + bhv[g]) - lse2;
-        float d0 = ex2_approx(x0) * (__uint_as_float(up[cur][k]) - Dn);
-        float d1 = ex2_approx(x1) * (__uint_as_float(up[cur][k + 1]) - Dn);
-        if (!row_valid) d0 = d1 = 0.f;
-        dRW[i] += d0;
-        dRW[i + 1] += d1;
-        dRH[g] += d0 + d1;
-        pk[k / 2] = pack_in(d0, d1, fmt);
-      }
-      tmem_st8(tdZ + cb / 2, pk);
-    }
-    tmem_wait_st();
-    tc_fence_before();
-    mbar_arrive(&bars[kBwPFull]);
-    if (kAll) {
-      if (row_valid) {
-        #pragma unroll
-        for (int g = 0; g < KHT; ++g)
-          if (j * KHT + g < H) args.drel_h[row * H + j * KHT + g] = dRH[g];
-      }
-    } else {
-      // two addends per entry (one per half), so their order does not matter
-      #pragma unroll
-      for (int g = 0; g < KHT; ++g)
-        if (j * KHT + g < H) atomicAdd(&dRH_sm[j * KHT + g], dRH[g]);
-    }
-  }
-  if (kAll) {
-    if (ok && row_valid) {
-      #pragma unroll
-      for (int i = 0; i < kLW; ++i)
-        if (i < W) args.drel_w[row * W + i] = dRW[i];
-    }
-  } else if (kSplitKw) {
-    // each half owns its columns
-    if (ok && row_valid) {
-      #pragma unroll
-      for (int i = 0; i < kLW; ++i)
-        if (kKw0 + i < W) args.drel_w[row * W + kKw0 + i] = dRW[i];
-    }
-  } else {
-    #pragma unroll
-    for (int i = 0; i < kLW; ++i)
-      if (i < W) atomicAdd(&dRW_sm[i], dRW[i]);
-  }
-  if (!kAll) {
-    if (ok) ok = group_sync();
-    if (ok && row_valid) {
-      if (HALF == 0)
-        for (int kh = 0; kh < H; ++kh) args.drel_h[row * H + kh] = dRH_sm[kh];
-      if (HALF == 1 && !kSplitKw)
-        for (int kw = 0; kw < W; ++kw) args.drel_w[row * W + kw] = dRW_sm[kw];
-    }
-  }
-  if (ok) ok = warp_all(mbar_wait(&bars[kBwMmaDone], (n_kv - 1) & 1, abort_flag, status));
-  if (ok) {
-    tc_fence_after();
-    #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      if (!kAll && hh != HALF) continue;
-      uint32_t a[32];
-      tmem_ld32(tdQ + 32 * hh, a);
-      tmem_wait_ld();
-      if (row_valid) {
-        float4* dst = reinterpret_cast<float4*>(args.dq_s + row * 64 + 32 * hh);
-        const float sc = args.scale;
-        #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          dst[c] = make_float4(sc * __uint_as_float(a[4 * c]), sc * __uint_as_float(a[4 * c + 1]),
-                               sc * __uint_as_float(a[4 * c + 2]), sc * __uint_as_float(a[4 * c + 3]));
-      }
-    }
-  }
+// Byte offset of 16-bit element (row, k) of a K-major, 128-byte-swizzled
+// operand of 128 rows whose K extent is 128 (two 64-element atoms of 16 KB).
+__device__ __forceinline__ uint32_t sw128_off(int row, int k) {
+  const int a = k >> 6, kk = k & 63;
+  return static_cast<uint32_t>(a * kTileBytes + row * 128 + ((((kk >> 3) ^ (row & 7))) << 4) + ((kk & 7) << 1));
 }
 
 template <int WP, bool BF16>
 __global__ void __launch_bounds__(kBwdRowsThreads, 1)
 relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_th, const __grid_constant__ CUtensorMap tm_tw,
                        const BwdArgs args) {
   using KT = KeyTile<WP, 64>;
-  constexpr int KHT = KT::KHT, BN = KT::BN, KS = kRowsGroups == 1 ? 3 : 2;
+  constexpr int KHT = KT::KHT, BN = KT::BN, KS = 3;
   using SM = BwdRowsSmem;
   constexpr int fmt = BF16 ? kBF16 : kF16;
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const BwdCta cta = bwd_setup<SM>(smem_raw, warp, kRowsGroups * kBlockM);
+  const BwdCta cta = bwd_setup<SM>(smem_raw, warp, kBlockM);
   uint8_t* smem = cta.smem;
   uint64_t* bars = cta.bars;
   volatile int* abort_flag = cta.abort_flag;
@@ -411,16 +223,16 @@ relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     constexpr uint32_t id_s = idesc_f16(kBlockM, BN, fmt, fmt, 0, 0);   // S, dP: both K-major
-    constexpr uint32_t id_dq = idesc_f16(kBlockM, 64, fmt, fmt, 0, 1);  // dZ k: the k tile N-major
+    constexpr uint32_t id_n = idesc_f16(kBlockM, 64, fmt, fmt, 0, 1);   // A K-major, B N-major (64 columns)
     const uint64_t d_q = sdesc_sw128(smem_u32(smem + SM::kA), 16, 1024);
     const uint64_t d_do = sdesc_sw128(smem_u32(smem + SM::kB), 16, 1024);
     const uint64_t d_ring = sdesc_sw128(smem_u32(smem + SM::kRing), 16, 1024);
-    constexpr uint32_t kStageStep = SM::kStage >> 4, kVOfs = kTileBytes >> 4;
+    constexpr uint32_t kStageStep = SM::kStage >> 4, kVOfs = kTileBytes >> 4, kAtom = kTileBytes >> 4;
     auto issue_dq = [&](int jj) {
       const int sp = jj % KS;
       #pragma unroll
       for (int k = 0; k < BN / 16; ++k)
-        umma_ts_w(tbase + 320, tbase + 256 + 8 * k, d_ring + sp * kStageStep + 128 * k, id_dq,
+        umma_ts_w(tbase + 320, tbase + 256 + 8 * k, d_ring + sp * kStageStep + 128 * k, id_n,
                   (jj > 0 || k > 0) ? 1u : 0u);
       umma_commit_w(&bars[kBwMmaDone]);
       umma_commit_w(&bars[kBwRingEmpty + sp]);
@@ -446,20 +258,203 @@ relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         umma_ss_w(tbase + 128, d_do + 2 * k, d_ring + s * kStageStep + kVOfs + 2 * k, id_s, k > 0);
       umma_commit_w(&bars[kBwSFull]);
     }
-    if (ok && warp_all(mbar_wait(&bars[kBwPFull], (n_kv - 1) & 1, abort_flag, status))) {
+    if (ok) ok = warp_all(mbar_wait(&bars[kBwPFull], (n_kv - 1) & 1, abort_flag, status));
+    if (ok) {
       tc_fence_after();
       issue_dq(n_kv - 1);
+      // the ring is idle once every product above is complete: the tables go to stage 0
+      umma_commit_w(&bars[kBwAllDone]);
+      ok = warp_all(mbar_wait(&bars[kBwAllDone], 0, abort_flag, status));
+    }
+    if (ok) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars[kBwTFull], 2 * kTileBytes);
+        tma_load_2d(sK(0), &tm_th, &bars[kBwTFull], 0, 0);
+        tma_load_2d(sK(0) + kTileBytes, &tm_tw, &bars[kBwTFull], 0, 0);
+      }
+      __syncwarp();
+      ok = warp_all(mbar_wait(&bars[kBwTFull], 0, abort_flag, status));
+    }
+    const uint64_t d_g = sdesc_sw128(smem_u32(sK(1)), 16, 1024);    // dG: rows r, K = table rows i
+    const uint64_t d_gt = sdesc_sw128(smem_u32(sK(2)), 16, 1024);   // dG^T: rows i, K = query rows r
+    for (int tb = 0; ok && tb < 2; ++tb) {
+      ok = warp_all(mbar_wait(&bars[kBwGFull], tb, abort_flag, status));
+      if (!ok) break;
+      tc_fence_after();
+      const uint64_t d_t = sdesc_sw128(smem_u32(sK(0) + tb * kTileBytes), 16, 1024);
+      #pragma unroll
+      for (int k = 0; k < 8; ++k)   // dq's bias part, both tables into one accumulator
+        umma_ss_w(tbase + 0, d_g + (k / 4) * kAtom + 2 * (k % 4), d_t + 128 * k, id_n, (tb > 0 || k > 0) ? 1u : 0u);
+      #pragma unroll
+      for (int k = 0; k < 8; ++k)   // this tile's partial table gradient
+        umma_ss_w(tbase + 128 + 64 * tb, d_gt + (k / 4) * kAtom + 2 * (k % 4), d_q + 128 * k, id_n, k > 0);
+      umma_commit_w(&bars[kBwBDone]);
     }
     // every product issued above completes before TMEM is released
     umma_commit_w(&bars[kBwQFull]);
     mbar_wait_budget(&bars[kBwQFull], 1, kWaitBudgetCycles);
     __syncwarp();
-  } else if (kRowsGroups == 1) {
-    rows_softmax<WP, BF16, 2>(args, smem, bars, abort_flag, tbase, warp, lane, bh, qt);
-  } else if (((warp - 2) >> 2) == 0) {
-    rows_softmax<WP, BF16, 0>(args, smem, bars, abort_flag, tbase, warp, lane, bh, qt);
   } else {
-    rows_softmax<WP, BF16, 1>(args, smem, bars, abort_flag, tbase, warp, lane, bh, qt);
+    // ---------------------------------------------------------------- softmax threads
+    const int H = args.H, W = args.W, N = args.N;
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const int n = qt * kBlockM + r;
+    const bool row_valid = n < N;
+    const int qh = row_valid ? n / W : 0, qw = row_valid ? n - (n / W) * W : 0;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tbase + lane_off, tdP = tS + 128, tdZ = tS + 256, tdQ = tS + 320;
+    const size_t row = static_cast<size_t>(bh) * N + (row_valid ? n : 0);
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    const float sl2 = args.scale_log2;
+    float* stg = reinterpret_cast<float*>(smem + SM::kStaging);
+    float* bh_row = stg + r * 65;             // rel_h (base 2); each entry becomes drel_h once read
+    float* dw_row = stg + 128 * 65 + r * 65;  // drel_w
+    const int Hpad = n_kv * KHT;
+    for (int kh = 0; kh < Hpad; ++kh)
+      bh_row[kh] = (kh < H) ? (row_valid ? kLog2e * args.rel_h[row * H + kh] : 0.f) : NEG_INF;
+    float bw[WP];
+    #pragma unroll
+    for (int kw = 0; kw < WP; ++kw)
+      bw[kw] = (kw < W) ? (row_valid ? kLog2e * args.rel_w[row * W + kw] : 0.f) : NEG_INF;
+    const float lse2 = row_valid ? args.lse[row] : 0.f;
+    // D = dO . out for this row (out in fp32 or in the input dtype)
+    float Dn = 0.f;
+    if (row_valid) {
+      for (int c = 0; c < 64; ++c) {
+        const float o = args.out_fmt == kF32 ? reinterpret_cast<const float*>(args.out)[row * 64 + c]
+                                              : ld_in(args.out, row * 64 + c, fmt);
+        Dn = fmaf(ld_in(args.dout, row * 64 + c, fmt), o, Dn);
+      }
+      args.D[row] = Dn;
+    }
+    float dRW[WP];
+    #pragma unroll
+    for (int kw = 0; kw < WP; ++kw) dRW[kw] = 0.f;
+    bool ok = true;
+    for (int j = 0; ok && j < n_kv; ++j) {
+      float bhv[KHT];
+      #pragma unroll
+      for (int g = 0; g < KHT; ++g) bhv[g] = bh_row[j * KHT + g];
+      ok = warp_all(mbar_wait(&bars[kBwSFull], j & 1, abort_flag, status));
+      if (!ok) break;
+      tc_fence_after();
+      if (j > 0) {
+        // dZ(j-1) has been read by its product before dZ(j) is written
+        ok = warp_all(mbar_wait(&bars[kBwMmaDone], (j - 1) & 1, abort_flag, status));
+        if (!ok) break;
+        tc_fence_after();
+      }
+      float dRH[KHT];
+      #pragma unroll
+      for (int g = 0; g < KHT; ++g) dRH[g] = 0.f;
+      // 16-column blocks, the next block's S and dP loads in flight while the
+      // current one is computed
+      uint32_t us[2][16], up[2][16];
+      tmem_ld16(tS, us[0]);
+      tmem_ld16(tdP, up[0]);
+      #pragma unroll
+      for (int bb = 0; bb < BN / 16; ++bb) {
+        const int cb = 16 * bb, cur = bb & 1;
+        tmem_wait_ld();
+        if (bb + 1 < BN / 16) {
+          tmem_ld16(tS + cb + 16, us[cur ^ 1]);
+          tmem_ld16(tdP + cb + 16, up[cur ^ 1]);
+        }
+        uint32_t pk[8];
+        #pragma unroll
+        for (int k = 0; k < 16; k += 2) {
+          const int col = cb + k;
+          const int g = col / WP, kw = col % WP;
+          const float x0 = fmaf(__uint_as_float(us[cur][k]), sl2, bw[kw] + bhv[g]) - lse2;
+          const float x1 = fmaf(__uint_as_float(us[cur][k + 1]), sl2, bw[kw + 1] + bhv[g]) - lse2;
+          float d0 = ex2_approx(x0) * (__uint_as_float(up[cur][k]) - Dn);
+          float d1 = ex2_approx(x1) * (__uint_as_float(up[cur][k + 1]) - Dn);
+          if (!row_valid) d0 = d1 = 0.f;
+          dRW[kw] += d0;
+          dRW[kw + 1] += d1;
+          dRH[g] += d0 + d1;
+          pk[k / 2] = pack_in(d0, d1, fmt);
+        }
+        tmem_st8(tdZ + cb / 2, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars[kBwPFull]);
+      #pragma unroll
+      for (int g = 0; g < KHT; ++g)
+        if (j * KHT + g < H) bh_row[j * KHT + g] = dRH[g];
+    }
+    #pragma unroll
+    for (int kw = 0; kw < WP; ++kw)
+      if (kw < W) dw_row[kw] = dRW[kw];
+    if (ok) ok = warp_all(mbar_wait(&bars[kBwMmaDone], (n_kv - 1) & 1, abort_flag, status));
+    // Epilogue: every product of the loop is complete, so ring stages 1 and 2
+    // are free.  Per table: dG row r (stage 1) and column r of dG^T (stage 2),
+    // then the two products.
+    uint8_t* g_st = sK(1);
+    uint8_t* gt_st = sK(2);
+    for (int tb = 0; ok && tb < 2; ++tb) {
+      const int L = tb == 0 ? H : W, coord = tb == 0 ? qh : qw;
+      const float* drow = tb == 0 ? bh_row : dw_row;
+      if (tb == 1) {
+        // the first table's products have read both stages
+        ok = warp_all(mbar_wait(&bars[kBwBDone], 0, abort_flag, status));
+        if (!ok) break;
+      }
+      for (int i = 0; i < 128; i += 2) {
+        const int k0 = coord - i + L - 1, k1 = k0 - 1;
+        const float v0 = (row_valid && k0 >= 0 && k0 < L) ? drow[k0] : 0.f;
+        const float v1 = (row_valid && k1 >= 0 && k1 < L) ? drow[k1] : 0.f;
+        const uint32_t pk = pack_in(v0, v1, fmt);
+        *reinterpret_cast<uint32_t*>(g_st + sw128_off(r, i)) = pk;
+        *reinterpret_cast<unsigned short*>(gt_st + sw128_off(i, r)) = static_cast<unsigned short>(pk & 0xFFFFu);
+        *reinterpret_cast<unsigned short*>(gt_st + sw128_off(i + 1, r)) = static_cast<unsigned short>(pk >> 16);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars[kBwGFull]);
+    }
+    if (ok) ok = warp_all(mbar_wait(&bars[kBwBDone], 1, abort_flag, status));
+    if (ok) {
+      tc_fence_after();
+      uint32_t a[32], b[32];
+      const float sc = args.scale;
+      #pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        tmem_ld32(tdQ + 32 * h, a);
+        tmem_ld32(tS + 32 * h, b);
+        tmem_wait_ld();
+        if (row_valid) {
+          #pragma unroll
+          for (int c = 0; c < 8; ++c)
+            st_grad4(args.dq, row * 64 + 32 * h + 4 * c,
+                     fmaf(sc, __uint_as_float(a[4 * c]), __uint_as_float(b[4 * c])),
+                     fmaf(sc, __uint_as_float(a[4 * c + 1]), __uint_as_float(b[4 * c + 1])),
+                     fmaf(sc, __uint_as_float(a[4 * c + 2]), __uint_as_float(b[4 * c + 2])),
+                     fmaf(sc, __uint_as_float(a[4 * c + 3]), __uint_as_float(b[4 * c + 3])), args.grad_fmt);
+        }
+      }
+      // table-gradient partials: TMEM lane r holds table row i = r
+      const int LH = 2 * H - 1, LW = 2 * W - 1;
+      float* part = args.parts + static_cast<size_t>(blockIdx.x) * (LH + LW) * 64;
+      #pragma unroll
+      for (int tb = 0; tb < 2; ++tb) {
+        const int Lrows = tb == 0 ? LH : LW;
+        float* dst = part + (tb == 0 ? 0 : LH * 64) + r * 64;
+        #pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          tmem_ld32(tS + 128 + 64 * tb + 32 * h, a);
+          tmem_wait_ld();
+          if (r < Lrows) {
+            #pragma unroll
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<float4*>(dst + 32 * h + 4 * c) =
+                  make_float4(__uint_as_float(a[4 * c]), __uint_as_float(a[4 * c + 1]), __uint_as_float(a[4 * c + 2]),
+                              __uint_as_float(a[4 * c + 3]));
+          }
+        }
+      }
+    }
   }
   bwd_teardown(tbase, warp);
 }
@@ -712,134 +707,6 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     }
   }
   bwd_teardown(tbase, warp);
-}
-
-// ---------------------------------------------------------------------------
-// Bias kernel: one CTA of 256 threads per (head, query tile).  Adds the bias
-// part of dq to dq_s and writes dq; writes this tile's partial table gradients.
-// Tables, q rows and the bias gradients of the tile are staged in shared
-// memory in fp32; rows of the tables and of q are 16-byte aligned (stride 68
-// floats) so that each thread reads them four columns at a time.
-constexpr int kBiasThreads = 256;
-constexpr int kTStride = 68;
-
-__host__ __device__ constexpr int bias_smem_floats(int H, int W) {
-  return (2 * H - 1 + 2 * W - 1) * kTStride + 128 * (H + 1) + 128 * (W + 1) + 128 * kTStride + 2 * 128;
-}
-
-// dT partial of one 4 x 4 block: table rows i0..i0+3 of a table of length L
-// (2 Lg - 1 rows for grid side Lg), columns c0..c0+3, over the tile's rows:
-// acc[u][*] = sum_r [0 <= kk < Lg] dR[r][kk] q[r][c0..c0+3], kk = coord(r) - (i0 + u) + Lg - 1.
-__device__ __forceinline__ void table_block(const float* dR, int ld, const int* coord, int Lg, const float* Qf,
-                                            int rows, int i0, int c0, float (&acc)[4][4]) {
-  #pragma unroll
-  for (int u = 0; u < 4; ++u)
-    #pragma unroll
-    for (int k = 0; k < 4; ++k) acc[u][k] = 0.f;
-  #pragma unroll 4
-  for (int rr = 0; rr < rows; ++rr) {
-    const int kk0 = coord[rr] - i0 + Lg - 1;
-    const float4 qv = *reinterpret_cast<const float4*>(Qf + rr * kTStride + c0);
-    #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int kk = kk0 - u;
-      const float wv = static_cast<unsigned>(kk) < static_cast<unsigned>(Lg) ? dR[rr * ld + kk] : 0.f;
-      acc[u][0] = fmaf(wv, qv.x, acc[u][0]);
-      acc[u][1] = fmaf(wv, qv.y, acc[u][1]);
-      acc[u][2] = fmaf(wv, qv.z, acc[u][2]);
-      acc[u][3] = fmaf(wv, qv.w, acc[u][3]);
-    }
-  }
-}
-
-__global__ void __launch_bounds__(kBiasThreads, 1) relpos_bwd_bias_kernel(const BwdArgs args) {
-  extern __shared__ __align__(16) float fsm[];
-  const int H = args.H, W = args.W, N = args.N;
-  const int bh = blockIdx.x / args.n_qtiles, qt = blockIdx.x - bh * args.n_qtiles;
-  const int n0 = qt * kBlockM;
-  const int rows = min(kBlockM, N - n0);
-  const int LH = 2 * H - 1, LW = 2 * W - 1;
-  float* Th = fsm;
-  float* Tw = Th + LH * kTStride;
-  float* Qf = Tw + LW * kTStride;                  // [128][68]
-  float* dRh = Qf + 128 * kTStride;                // [128][H + 1]
-  float* dRw = dRh + 128 * (H + 1);                // [128][W + 1]
-  int* qhv = reinterpret_cast<int*>(dRw + 128 * (W + 1));
-  int* qwv = qhv + 128;
-  const int t = threadIdx.x;
-  const size_t base = static_cast<size_t>(bh) * N + n0;
-  for (int e = t; e < LH * 64; e += kBiasThreads) Th[(e >> 6) * kTStride + (e & 63)] = ld_in(args.th, e, args.in_fmt);
-  for (int e = t; e < LW * 64; e += kBiasThreads) Tw[(e >> 6) * kTStride + (e & 63)] = ld_in(args.tw, e, args.in_fmt);
-  for (int e = t; e < 128 * H; e += kBiasThreads) {
-    const int rr = e / H, c = e - rr * H;
-    dRh[rr * (H + 1) + c] = rr < rows ? args.drel_h[base * H + e] : 0.f;
-  }
-  for (int e = t; e < 128 * W; e += kBiasThreads) {
-    const int rr = e / W, c = e - rr * W;
-    dRw[rr * (W + 1) + c] = rr < rows ? args.drel_w[base * W + e] : 0.f;
-  }
-  for (int e = t; e < 128 * 64; e += kBiasThreads) {
-    const int rr = e >> 6;
-    Qf[rr * kTStride + (e & 63)] = rr < rows ? ld_in(args.q, base * 64 + e, args.in_fmt) : 0.f;
-  }
-  if (t < 128) {
-    const int n = n0 + t;
-    qhv[t] = n / W;
-    qwv[t] = n - (n / W) * W;
-  }
-  __syncthreads();
-  // dq = dq_s + sum_kh drel_h T_h[qh - kh + H - 1] + sum_kw drel_w T_w[qw - kw + W - 1];
-  // a warp holds 32 consecutive rows (mostly one qh, so one T_h row) and one half of the columns
-  {
-    const int rr = t & 127, c0 = (t >> 7) * 32;
-    if (rr < rows) {
-      const int qh = qhv[rr], qw = qwv[rr];
-      float4 acc[8];
-      const float4* src = reinterpret_cast<const float4*>(args.dq_s + (base + rr) * 64 + c0);
-      #pragma unroll
-      for (int c = 0; c < 8; ++c) acc[c] = src[c];
-      for (int kh = 0; kh < H; ++kh) {
-        const float wv = dRh[rr * (H + 1) + kh];
-        const float4* tr = reinterpret_cast<const float4*>(Th + (qh - kh + H - 1) * kTStride + c0);
-        #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const float4 v = tr[c];
-          acc[c] = make_float4(fmaf(wv, v.x, acc[c].x), fmaf(wv, v.y, acc[c].y), fmaf(wv, v.z, acc[c].z),
-                               fmaf(wv, v.w, acc[c].w));
-        }
-      }
-      for (int kw = 0; kw < W; ++kw) {
-        const float wv = dRw[rr * (W + 1) + kw];
-        const float4* tr = reinterpret_cast<const float4*>(Tw + (qw - kw + W - 1) * kTStride + c0);
-        #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const float4 v = tr[c];
-          acc[c] = make_float4(fmaf(wv, v.x, acc[c].x), fmaf(wv, v.y, acc[c].y), fmaf(wv, v.z, acc[c].z),
-                               fmaf(wv, v.w, acc[c].w));
-        }
-      }
-      #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        st_grad4(args.dq, (base + rr) * 64 + c0 + 4 * c, acc[c].x, acc[c].y, acc[c].z, acc[c].w, args.grad_fmt);
-    }
-  }
-  // this tile's partial table gradients, in blocks of 4 table rows x 4 columns
-  float* part = args.parts + static_cast<size_t>(blockIdx.x) * (LH + LW) * 64;
-  const int hb = (LH + 3) / 4, wb = (LW + 3) / 4;
-  for (int b = t; b < (hb + wb) * 16; b += kBiasThreads) {
-    const int ib = b >> 4, c0 = (b & 15) * 4;
-    const bool is_h = ib < hb;
-    const int i0 = 4 * (is_h ? ib : ib - hb);
-    const int L = is_h ? LH : LW;
-    float acc[4][4];
-    if (is_h) table_block(dRh, H + 1, qhv, H, Qf, rows, i0, c0, acc);
-    else table_block(dRw, W + 1, qwv, W, Qf, rows, i0, c0, acc);
-    float* dst = part + (is_h ? 0 : LH * 64);
-    #pragma unroll
-    for (int u = 0; u < 4; ++u)
-      if (i0 + u < L)
-        *reinterpret_cast<float4*>(dst + (i0 + u) * 64 + c0) = make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
-  }
 }
 
 // Tables kernel: dT = the sum of the per-tile partials.  A CTA of 256 threads

@@ -79,16 +79,10 @@ struct BwdArgs {
   const void* out;      // [BH, N, 64] forward output (input dtype)
   const void* dout;     // [BH, N, 64] upstream gradient (input dtype)
   float* D;             // [BH, N] dO . out per row (rows kernel writes, cols kernel reads)
-  float* dq_s;          // [BH, N, 64] scale * dZ k (rows kernel)
-  float* drel_h;        // [BH, N, H]
-  float* drel_w;        // [BH, N, W]
-  void* dq;             // [BH, N, 64] grad dtype (bias kernel)
+  void* dq;             // [BH, N, 64] grad dtype (rows kernel)
   void* dk;             // [BH, N, 64] grad dtype (cols kernel)
   void* dv;             // [BH, N, 64]
-  const void* th;       // [2H-1, 64] table (input dtype)
-  const void* tw;       // [2W-1, 64]
-  const void* q;        // [BH, N, 64] (bias kernel reads rows directly)
-  float* parts;         // [n_qblocks][(2H-1) + (2W-1)][64] per-CTA table-gradient partials
+  float* parts;         // [BH * n_qtiles][(2H-1) + (2W-1)][64] per-query-tile table-gradient partials
   float* dth;           // [2H-1, 64] fp32
   float* dtw;           // [2W-1, 64] fp32
   int* status;

@@ -270,7 +270,7 @@ dera_status current_device(int* dev) {
 
 // Workspace of the backward: fp32 regions, each 256-byte aligned.
 struct BwdLayout {
-  size_t rel_h, rel_w, D, dq_s, drel_h, drel_w, parts, total;
+  size_t rel_h, rel_w, D, parts, total;
   int n_qtiles;
   BwdLayout(int BH, int H, int W) {
     const size_t rows = static_cast<size_t>(BH) * H * W;
@@ -284,9 +284,6 @@ struct BwdLayout {
     rel_h = take(rows * H);
     rel_w = take(rows * W);
     D = take(rows);
-    dq_s = take(rows * 64);
-    drel_h = take(rows * H);
-    drel_w = take(rows * W);
     parts = take(static_cast<size_t>(BH) * n_qtiles * (2 * H - 1 + 2 * W - 1) * 64);
     total = o;
   }
@@ -570,7 +567,8 @@ dera_status dera_relpos_fused_backward(const void* q, const void* k, const void*
   const int WP = padded_width(W), KHT = rows_per_tile(WP, 64);
   BwdMaps maps;
   if (!map_rows(&maps.q, q, in_dtype, BH, N, 64) || !map_rows(&maps.dout, dout, in_dtype, BH, N, 64) ||
-      !map_keys(&maps.k, k, in_dtype, BH, H, W, 64, WP, KHT) || !map_keys(&maps.v, v, in_dtype, BH, H, W, 64, WP, KHT))
+      !map_keys(&maps.k, k, in_dtype, BH, H, W, 64, WP, KHT) || !map_keys(&maps.v, v, in_dtype, BH, H, W, 64, WP, KHT) ||
+      !map_table(&maps.th, rel_pos_h, in_dtype, H, 64) || !map_table(&maps.tw, rel_pos_w, in_dtype, W, 64))
     return DERA_ERR_CUDA;
   BwdArgs a;
   a.rel_h = rel_h;
@@ -579,15 +577,9 @@ dera_status dera_relpos_fused_backward(const void* q, const void* k, const void*
   a.out = out;
   a.dout = dout;
   a.D = reinterpret_cast<float*>(ws + L.D);
-  a.dq_s = reinterpret_cast<float*>(ws + L.dq_s);
-  a.drel_h = reinterpret_cast<float*>(ws + L.drel_h);
-  a.drel_w = reinterpret_cast<float*>(ws + L.drel_w);
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
-  a.th = rel_pos_h;
-  a.tw = rel_pos_w;
-  a.q = q;
   a.parts = reinterpret_cast<float*>(ws + L.parts);
   a.dth = drel_pos_h;
   a.dtw = drel_pos_w;

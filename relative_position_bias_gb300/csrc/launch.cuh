@@ -22,11 +22,11 @@ cudaError_t launch_project(const CUtensorMap& q, const CUtensorMap& th, const CU
 cudaError_t launch_wait_selftest(int* status, long long budget, cudaStream_t stream);
 
 struct BwdMaps {
-  CUtensorMap q, dout, k, v;
+  CUtensorMap q, dout, k, v, th, tw;
 };
 
-// The backward's attention, bias and table kernels for head_dim 64, in stream
-// order; the compact rel_h, rel_w in args must already be written.
+// The backward's attention kernels and its table reduction for head_dim 64, in
+// stream order; the compact rel_h, rel_w in args must already be written.
 cudaError_t launch_backward(const BwdMaps& maps, const BwdArgs& args, int WP, cudaStream_t stream);
 
 }  // namespace dera
