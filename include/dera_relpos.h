@@ -197,9 +197,10 @@ DERA_API dera_status dera_relpos_backward_workspace_size(int BH, int H, int W, i
  * workspace: device memory of at least dera_relpos_backward_workspace_size bytes,
  *      256-byte aligned, owned by the caller, not used by another call in flight;
  *      its contents need no initialisation.
- * Precision: P is recomputed from lse in fp32; dZ and P enter the tensor-core
- *      products rounded to in_dtype (relative 2^-9 for bf16, 2^-11 for fp16), with
- *      fp32 accumulation; the bias and table gradients are accumulated in fp32.
+ * Precision: P is recomputed from lse in fp32; dZ, P and the bias gradients
+ *      (drel_h, drel_w) enter the tensor-core products rounded to in_dtype (relative
+ *      2^-9 for bf16, 2^-11 for fp16), with fp32 accumulation; the per-tile table
+ *      gradients are added in fp32.
  *      Nothing is accumulated with atomics: the result is the same on every run.
  * Errors: DERA_ERR_HEAD_DIM unless head_dim is 64; DERA_ERR_SCRATCH if the
  *      workspace is NULL or smaller than the size above; otherwise as for

@@ -14,18 +14,19 @@
 // P is recomputed from the forward's base-2 log-sum-exp of each row:
 //   P[n, m] = 2^(Z[n, m] log2(e) - lse2[n]).
 //
-// Four kernels, in stream order (the projection kernel of the forward first
+// Three kernels, in stream order (the projection kernel of the forward first
 // writes the compact rel_h, rel_w in fp32):
 //   relpos_bwd_rows   one CTA per (head, 128-row query tile), key tiles streamed:
 //                     S = q k^T and dP = dO v^T on the tensor core, P and dZ on
-//                     the softmax warps (one thread per query row), dq_s += dZ k
-//                     on the tensor core; writes D, scale * dq_s, drel_h, drel_w.
+//                     the softmax threads (one per query row), dZ k accumulated
+//                     on the tensor core; then, also on the tensor core, dq's
+//                     part through the projection and the tile's partial table
+//                     gradients from the on-chip bias gradients; writes D, dq
+//                     and the partials.
 //   relpos_bwd_cols   one CTA per (head, key tile), query tiles streamed:
 //                     S^T = k q^T and dP^T = v dO^T, P^T and dZ^T per key row,
 //                     dv += P^T dO and dk += dZ^T q accumulated in TMEM.
-//   relpos_bwd_bias   one CTA per (head, query tile): dq = dq_s + the bias part,
-//                     and this tile's share of dT_h, dT_w (a partial per CTA).
-//   relpos_bwd_tables sums the per-CTA partials in a fixed order.
+//   relpos_bwd_tables sums the per-tile partials in a fixed order.
 // Nothing is accumulated with atomics, so the result does not depend on the
 // order in which CTAs run.
 #pragma once
