@@ -332,6 +332,7 @@ relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     float dRW[WP];
     #pragma unroll
     for (int kw = 0; kw < WP; ++kw) dRW[kw] = 0.f;
+    const float2 sl2v = make_float2(sl2, sl2), nlse2 = make_float2(-lse2, -lse2), nD2 = make_float2(-Dn, -Dn);
     bool ok = true;
     for (int j = 0; ok && j < n_kv; ++j) {
       float bhv[KHT];
@@ -365,17 +366,20 @@ relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         uint32_t pk[8];
         #pragma unroll
         for (int k = 0; k < 16; k += 2) {
+          // a pair of columns of one grid row, through the packed fp32x2 units
           const int col = cb + k;
           const int g = col / WP, kw = col % WP;
-          const float x0 = fmaf(__uint_as_float(us[cur][k]), sl2, bw[kw] + bhv[g]) - lse2;
-          const float x1 = fmaf(__uint_as_float(us[cur][k + 1]), sl2, bw[kw + 1] + bhv[g]) - lse2;
-          float d0 = ex2_approx(x0) * (__uint_as_float(up[cur][k]) - Dn);
-          float d1 = ex2_approx(x1) * (__uint_as_float(up[cur][k + 1]) - Dn);
-          if (!row_valid) d0 = d1 = 0.f;
-          dRW[kw] += d0;
-          dRW[kw + 1] += d1;
-          dRH[g] += d0 + d1;
-          pk[k / 2] = pack_in(d0, d1, fmt);
+          const float2 s2 = make_float2(__uint_as_float(us[cur][k]), __uint_as_float(us[cur][k + 1]));
+          const float2 dp2 = make_float2(__uint_as_float(up[cur][k]), __uint_as_float(up[cur][k + 1]));
+          const float2 b2 = fadd2(make_float2(bw[kw], bw[kw + 1]), make_float2(bhv[g], bhv[g]));
+          const float2 x = fadd2(ffma2(s2, sl2v, b2), nlse2);
+          float2 d = __fmul2_rn(make_float2(ex2_approx(x.x), ex2_approx(x.y)), fadd2(dp2, nD2));
+          if (!row_valid) d = make_float2(0.f, 0.f);
+          const float2 acc = fadd2(make_float2(dRW[kw], dRW[kw + 1]), d);
+          dRW[kw] = acc.x;
+          dRW[kw + 1] = acc.y;
+          dRH[g] += d.x + d.y;
+          pk[k / 2] = pack_in(d.x, d.y, fmt);
         }
         tmem_st8(tdZ + cb / 2, pk);
       }
@@ -636,6 +640,7 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
       // this half's four 16-column blocks; the next block's S^T and dP^T
       // loads are in flight while the current one is computed
       const int c_first = 64 * half;
+      const float2 sl2v = make_float2(sl2, sl2), l2ev = make_float2(kLog2e, kLog2e);
       uint32_t us[2][16], up[2][16];
       tmem_ld16(tS + c_first, us[0]);
       tmem_ld16(tdP + c_first, up[0]);
@@ -655,24 +660,29 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
           const float4 h4 = *reinterpret_cast<const float4*>(rhT + c4);
           const float4 l4 = *reinterpret_cast<const float4*>(lseT + c4);
           const float4 d4 = *reinterpret_cast<const float4*>(DT + c4);
-          const float bw4[4] = {w4.x + h4.x, w4.y + h4.y, w4.z + h4.z, w4.w + h4.w};
-          const float ls4[4] = {l4.x, l4.y, l4.z, l4.w};
-          const float dd4[4] = {d4.x, d4.y, d4.z, d4.w};
           // Query columns past N must not reach dv or dk; key slots without a key
           // need no mask, since their P^T and dZ^T rows only reach their own
-          // (unstored) rows of dv and dk.
-          float p4[4], z4[4];
+          // (unstored) rows of dv and dk.  Pairs of columns go through the packed
+          // fp32x2 units.
           #pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const float x = fmaf(__uint_as_float(us[q & 1][k4 + h]), sl2, fmaf(bw4[h], kLog2e, -ls4[h]));
-            const float p = (full || c4 + h < rows) ? ex2_approx(x) : 0.f;
-            p4[h] = p;
-            z4[h] = p * (__uint_as_float(up[q & 1][k4 + h]) - dd4[h]);
+          for (int hp = 0; hp < 4; hp += 2) {
+            const float2 w2 = hp == 0 ? make_float2(w4.x, w4.y) : make_float2(w4.z, w4.w);
+            const float2 h2 = hp == 0 ? make_float2(h4.x, h4.y) : make_float2(h4.z, h4.w);
+            const float2 nl2 = hp == 0 ? make_float2(-l4.x, -l4.y) : make_float2(-l4.z, -l4.w);
+            const float2 nd2 = hp == 0 ? make_float2(-d4.x, -d4.y) : make_float2(-d4.z, -d4.w);
+            const float2 s2 = make_float2(__uint_as_float(us[q & 1][k4 + hp]), __uint_as_float(us[q & 1][k4 + hp + 1]));
+            const float2 dp2 =
+                make_float2(__uint_as_float(up[q & 1][k4 + hp]), __uint_as_float(up[q & 1][k4 + hp + 1]));
+            const float2 x = ffma2(s2, sl2v, ffma2(fadd2(w2, h2), l2ev, nl2));
+            float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            if (!full) {
+              if (c4 + hp >= rows) p.x = 0.f;
+              if (c4 + hp + 1 >= rows) p.y = 0.f;
+            }
+            const float2 z = __fmul2_rn(p, fadd2(dp2, nd2));
+            pp[(k4 + hp) / 2] = pack_in(p.x, p.y, fmt);
+            pz[(k4 + hp) / 2] = pack_in(z.x, z.y, fmt);
           }
-          pp[k4 / 2] = pack_in(p4[0], p4[1], fmt);
-          pp[k4 / 2 + 1] = pack_in(p4[2], p4[3], fmt);
-          pz[k4 / 2] = pack_in(z4[0], z4[1], fmt);
-          pz[k4 / 2 + 1] = pack_in(z4[2], z4[3], fmt);
         }
         tmem_st8(tP + cb / 2, pp);
         tmem_st8(tdZ + cb / 2, pz);
