@@ -247,10 +247,10 @@ relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         // the softmax threads have read S(j-1), dP(j-1) and written dZ(j-1)
         ok = warp_all(mbar_wait(&bars[kBwPFull], (j - 1) & 1, abort_flag, status));
         if (!ok) break;
-        tc_fence_after();
-        issue_dq(j - 1);
       }
       tc_fence_after();
+      // S(j) and dP(j) first, so the softmax threads start on tile j while
+      // dZ(j-1) k runs; they store dZ(j) only once that product has read dZ(j-1)
       #pragma unroll
       for (int k = 0; k < 4; ++k)
         umma_ss_w(tbase + 0, d_q + 2 * k, d_ring + s * kStageStep + 2 * k, id_s, k > 0);
@@ -258,6 +258,7 @@ relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
       for (int k = 0; k < 4; ++k)
         umma_ss_w(tbase + 128, d_do + 2 * k, d_ring + s * kStageStep + kVOfs + 2 * k, id_s, k > 0);
       umma_commit_w(&bars[kBwSFull]);
+      if (j > 0) issue_dq(j - 1);
     }
     if (ok) ok = warp_all(mbar_wait(&bars[kBwPFull], (n_kv - 1) & 1, abort_flag, status));
     if (ok) {
@@ -341,12 +342,6 @@ relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
       ok = warp_all(mbar_wait(&bars[kBwSFull], j & 1, abort_flag, status));
       if (!ok) break;
       tc_fence_after();
-      if (j > 0) {
-        // dZ(j-1) has been read by its product before dZ(j) is written
-        ok = warp_all(mbar_wait(&bars[kBwMmaDone], (j - 1) & 1, abort_flag, status));
-        if (!ok) break;
-        tc_fence_after();
-      }
       float dRH[KHT];
       #pragma unroll
       for (int g = 0; g < KHT; ++g) dRH[g] = 0.f;
@@ -381,8 +376,18 @@ relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
           dRH[g] += d.x + d.y;
           pk[k / 2] = pack_in(d.x, d.y, fmt);
         }
+        if (bb == 0 && j > 0) {
+          // dZ(j-1) has been read by its product before dZ(j) is written
+          ok = warp_all(mbar_wait(&bars[kBwMmaDone], (j - 1) & 1, abort_flag, status));
+          if (!ok) {
+            tmem_wait_ld();   // the next block's loads are in flight
+            break;
+          }
+          tc_fence_after();
+        }
         tmem_st8(tdZ + cb / 2, pk);
       }
+      if (!ok) break;
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars[kBwPFull]);
@@ -539,10 +544,10 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
       if (i > 0) {
         ok = warp_all(mbar_wait(&bars[kBwPFull], (i - 1) & 1, abort_flag, status));
         if (!ok) break;
-        tc_fence_after();
-        issue_acc(i - 1);
       }
       tc_fence_after();
+      // S^T(i) and dP^T(i) first, so the softmax threads start on query tile i
+      // while dv and dk take tile i - 1
       #pragma unroll
       for (int k = 0; k < 4; ++k)
         umma_ss_w(tbase + 0, d_k + 2 * k, d_ring + s * kStageStep + 2 * k, id_s, k > 0);
@@ -550,6 +555,7 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
       for (int k = 0; k < 4; ++k)
         umma_ss_w(tbase + 128, d_v + 2 * k, d_ring + s * kStageStep + kDoOfs + 2 * k, id_s, k > 0);
       umma_commit_w(&bars[kBwSFull]);
+      if (i > 0) issue_acc(i - 1);
     }
     if (ok && warp_all(mbar_wait(&bars[kBwPFull], (n_qt - 1) & 1, abort_flag, status))) {
       tc_fence_after();
@@ -632,11 +638,6 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
       ok = warp_all(mbar_wait(&bars[kBwSFull], i & 1, abort_flag, status));
       if (!ok) break;
       tc_fence_after();
-      if (i > 0) {
-        ok = warp_all(mbar_wait(&bars[kBwMmaDone], (i - 1) & 1, abort_flag, status));
-        if (!ok) break;
-        tc_fence_after();
-      }
       // this half's four 16-column blocks; the next block's S^T and dP^T
       // loads are in flight while the current one is computed
       const int c_first = 64 * half;
@@ -684,9 +685,19 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             pz[(k4 + hp) / 2] = pack_in(z.x, z.y, fmt);
           }
         }
+        if (q == 0 && i > 0) {
+          // P^T(i-1) and dZ^T(i-1) have been read by dv and dk before they are overwritten
+          ok = warp_all(mbar_wait(&bars[kBwMmaDone], (i - 1) & 1, abort_flag, status));
+          if (!ok) {
+            tmem_wait_ld();   // the next block's loads are in flight
+            break;
+          }
+          tc_fence_after();
+        }
         tmem_st8(tP + cb / 2, pp);
         tmem_st8(tdZ + cb / 2, pz);
       }
+      if (!ok) break;
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars[kBwPFull]);
