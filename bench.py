@@ -52,14 +52,23 @@ def load_peaks() -> tuple[dict, str]:
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def source_hash() -> str:
-    """Hash of the CUDA sources, to tell whether stored ncu counters still describe the kernel."""
+# The sources each timed kernel is compiled from: stored counters stay valid while these are
+# unchanged, whatever happens to the other kernels' files.
+KERNEL_SOURCES = {
+    "relpos_attn_kernel": ("attention.cuh", "attention_inst.cuh", "attention_w16.cu", "attention_w32.cu",
+                           "attention_w40.cu", "attention_w64.cu", "common.cuh", "ptx.cuh", "launch.cuh"),
+    "relpos_bwd": ("backward.cu", "backward.cuh", "common.cuh", "ptx.cuh", "launch.cuh"),
+}
+
+
+def source_hash(kernel: str = "relpos_attn_kernel") -> str:
+    """Hash of the CUDA sources a kernel is built from, to tell whether stored ncu counters still
+    describe it."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "relative_position_bias_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in sorted(KERNEL_SOURCES[kernel.split("<")[0]]):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -72,7 +81,7 @@ def stored_traffic(kernel: str, workload: str):
     except (OSError, ValueError):
         return None
     e = entries.get(f"{kernel}/{workload}")
-    if not e or e.get("source_hash") != source_hash():
+    if not e or e.get("source_hash") != source_hash(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 

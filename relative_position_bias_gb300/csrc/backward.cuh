@@ -98,7 +98,8 @@ enum : int {
 // (later its drel_h row) and its drel_w row, 2 x 128 rows of 65 floats
 using BwdRowsSmem = BwdSmem<3, 2 * 128 * 65 * 4>;
 // cols kernel: a three-stage Q/dO ring; staging holds two buffers of one query
-// tile's rel_w, rel_h entries, lse and D, transposed (74 rows of 132 floats each)
+// tile's rel_w (query rows of WP floats, at most 128 x 64 floats) and, transposed
+// into rows of 132 floats, its rel_h entries, lse and D (74 such rows in all)
 constexpr int kColsStageRow = 132;
 constexpr int kColsStageFloats = 74 * kColsStageRow;
 using BwdColsSmem = BwdSmem<3, 2 * kColsStageFloats * 4>;
@@ -469,6 +470,12 @@ relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
   bwd_teardown(tbase, warp);
 }
 
+// 16-byte global -> shared copy that does not pass through registers (both
+// addresses 16-byte aligned).
+__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Cols kernel: one CTA per (head, key tile of KHT grid rows); thread m of warps
 // 2-5 owns key slot m of the tile (TMEM lane m; slots past the tile's BN keys,
@@ -476,8 +483,8 @@ relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
 // columns: S^T [0, 128), dP^T [128, 256), P^T and dZ^T in the input dtype as
 // packed pairs [256, 320) and [320, 384), dv [384, 448), dk [448, 512).
 // Per query tile the softmax threads stage (cp.async, one tile ahead) the
-// tile's rel_w rows [128][W], its rel_h entries for this key tile's grid rows
-// [128][KHT], lse and D.
+// tile's rel_w rows [128][WP], its rel_h entries for this key tile's grid rows
+// [KHT][128], lse and D.
 template <int WP, bool BF16>
 __global__ void __launch_bounds__(kBwdColsThreads, 1)
 relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -578,26 +585,37 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                    tdK = tS + 448;
     const float sl2 = args.scale_log2;
     float* stage_base = reinterpret_cast<float*>(smem + SM::kStaging);
-    // buffer b, transposed so that a thread reads four query columns at once:
-    // rel_w [kw][n] in rows 0..63, rel_h [g][n] in rows 64..71, lse in row 72,
-    // D in row 73 (rows of kColsStageRow floats; columns past N hold zeros)
+    // buffer b: rel_w [n][kw] in query rows of WP floats (the first 128 WP
+    // floats), then, transposed so that a thread reads four query columns at
+    // once, rel_h [g][n] in rows 64..71, lse in row 72 and D in row 73 (rows of
+    // kColsStageRow floats; lse and D hold zeros past N).  rel_w entries past
+    // N or past W are never written: they reach only masked query columns or
+    // key slots without a key.
     constexpr int kBufFloats = kColsStageFloats, RS = kColsStageRow;
+    static_assert(kBlockM * WP <= 64 * RS, "rel_w rows fit below the transposed rows");
     auto stage = [&](int i, int b) {
       float* buf = stage_base + b * kBufFloats;
       const int n0 = i * kBlockM;
       const int rows = min(kBlockM, N - n0);
       const size_t base = static_cast<size_t>(bh) * N + n0;
-      // the tile's rel_w rows are one contiguous block: element e = rr W + c,
-      // its (rr, c) advanced without a division per element
-      const int step_r = (2 * kBlockM) / W, step_c = (2 * kBlockM) - step_r * W;
-      int rr = t / W, c = t - (t / W) * W;
-      for (int e = t; e < kBlockM * W; e += 2 * kBlockM) {
-        cp_async4(buf + c * RS + rr, args.rel_w + (rr < rows ? base * W + e : 0), rr < rows ? 4u : 0u);
-        rr += step_r;
-        c += step_c;
-        if (c >= W) {
-          c -= W;
-          ++rr;
+      if (W == WP) {
+        // the tile's rel_w rows are one contiguous, 16-byte aligned block
+        // (WP is a multiple of 4) copied as it lies
+        const float4* src = reinterpret_cast<const float4*>(args.rel_w + base * W);
+        for (int e = t; e < rows * (WP / 4); e += 2 * kBlockM) cp_async16(buf + 4 * e, src + e);
+      } else {
+        // element e = rr W + c of the block goes to row rr, column c; (rr, c)
+        // advanced without a division per element
+        const int step_r = (2 * kBlockM) / W, step_c = (2 * kBlockM) - step_r * W;
+        int rr = t / W, c = t - (t / W) * W;
+        for (int e = t; e < rows * W; e += 2 * kBlockM) {
+          cp_async4(buf + rr * WP + c, args.rel_w + base * W + e, 4u);
+          rr += step_r;
+          c += step_c;
+          if (c >= W) {
+            c -= W;
+            ++rr;
+          }
         }
       }
       for (int e = t; e < kBlockM * KHT; e += 2 * kBlockM) {
@@ -629,7 +647,7 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
       if (!ok) break;
       if (i + 1 < n_qt) stage(i + 1, (i + 1) & 1);
       const float* buf = stage_base + (i & 1) * kBufFloats;
-      const float* rwT = buf + kw * RS;           // kw < WP <= 64
+      const float* rw = buf + 64 * half * WP + kw;   // rel_w of this half's first query column
       const float* rhT = buf + (64 + g) * RS;     // g < 8 for every key slot
       const float* lseT = buf + 72 * RS;
       const float* DT = buf + 73 * RS;
@@ -657,7 +675,8 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         #pragma unroll
         for (int k4 = 0; k4 < 16; k4 += 4) {
           const int c4 = cb + k4;
-          const float4 w4 = *reinterpret_cast<const float4*>(rwT + c4);
+          const int cr = 16 * q + k4;   // query column c4, counted from this half's first
+          const float4 w4 = make_float4(rw[cr * WP], rw[(cr + 1) * WP], rw[(cr + 2) * WP], rw[(cr + 3) * WP]);
           const float4 h4 = *reinterpret_cast<const float4*>(rhT + c4);
           const float4 l4 = *reinterpret_cast<const float4*>(lseT + c4);
           const float4 d4 = *reinterpret_cast<const float4*>(DT + c4);
