@@ -59,10 +59,11 @@ struct BwdSmem {
   static_assert(kAlloc <= 232448, "shared memory");
 };
 
-__device__ __forceinline__ float ld_in(const void* p, size_t i, int fmt) {
-  const unsigned short raw = reinterpret_cast<const unsigned short*>(p)[i];
-  if (fmt == kBF16) return __uint_as_float(static_cast<uint32_t>(raw) << 16);
-  return __half2float(__ushort_as_half(raw));
+// The two 16-bit values of a packed pair, low half first.
+__device__ __forceinline__ float2 unpack_in(uint32_t u, int fmt) {
+  if (fmt == kBF16) return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+  return make_float2(__half2float(__ushort_as_half(static_cast<unsigned short>(u & 0xFFFFu))),
+                     __half2float(__ushort_as_half(static_cast<unsigned short>(u >> 16))));
 }
 
 __device__ __forceinline__ uint32_t pack_in(float lo, float hi, int fmt) {
@@ -314,20 +315,84 @@ relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     float* bh_row = stg + r * 65;             // rel_h (base 2); each entry becomes drel_h once read
     float* dw_row = stg + 128 * 65 + r * 65;  // drel_w
     const int Hpad = n_kv * KHT;
-    for (int kh = 0; kh < Hpad; ++kh)
-      bh_row[kh] = (kh < H) ? (row_valid ? kLog2e * args.rel_h[row * H + kh] : 0.f) : NEG_INF;
+    // The row loads below are independent 16-byte loads where the row allows
+    // (rows of the 16-byte aligned workspace whose length is a multiple of 4;
+    // dO and out rows of 64 elements), so that they are all in flight at once.
+    if (row_valid && (H & 3) == 0) {
+      const float4* src = reinterpret_cast<const float4*>(args.rel_h + row * H);
+      #pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        if (4 * c < H) {
+          const float4 v = src[c];
+          bh_row[4 * c] = kLog2e * v.x;
+          bh_row[4 * c + 1] = kLog2e * v.y;
+          bh_row[4 * c + 2] = kLog2e * v.z;
+          bh_row[4 * c + 3] = kLog2e * v.w;
+        }
+      }
+      for (int kh = H; kh < Hpad; ++kh) bh_row[kh] = NEG_INF;
+    } else {
+      for (int kh = 0; kh < Hpad; ++kh)
+        bh_row[kh] = (kh < H) ? (row_valid ? kLog2e * args.rel_h[row * H + kh] : 0.f) : NEG_INF;
+    }
     float bw[WP];
-    #pragma unroll
-    for (int kw = 0; kw < WP; ++kw)
-      bw[kw] = (kw < W) ? (row_valid ? kLog2e * args.rel_w[row * W + kw] : 0.f) : NEG_INF;
+    if (row_valid && (W & 3) == 0) {
+      const float4* src = reinterpret_cast<const float4*>(args.rel_w + row * W);
+      #pragma unroll
+      for (int c = 0; c < WP / 4; ++c) {
+        const float4 v = 4 * c < W ? src[c] : make_float4(NEG_INF, NEG_INF, NEG_INF, NEG_INF);
+        bw[4 * c] = 4 * c < W ? kLog2e * v.x : NEG_INF;
+        bw[4 * c + 1] = 4 * c < W ? kLog2e * v.y : NEG_INF;
+        bw[4 * c + 2] = 4 * c < W ? kLog2e * v.z : NEG_INF;
+        bw[4 * c + 3] = 4 * c < W ? kLog2e * v.w : NEG_INF;
+      }
+    } else {
+      #pragma unroll
+      for (int kw = 0; kw < WP; ++kw)
+        bw[kw] = (kw < W) ? (row_valid ? kLog2e * args.rel_w[row * W + kw] : 0.f) : NEG_INF;
+    }
     const float lse2 = row_valid ? args.lse[row] : 0.f;
-    // D = dO . out for this row (out in fp32 or in the input dtype)
+    // D = dO . out for this row (out in fp32 or in the input dtype), summed in
+    // column order
     float Dn = 0.f;
     if (row_valid) {
-      for (int c = 0; c < 64; ++c) {
-        const float o = args.out_fmt == kF32 ? reinterpret_cast<const float*>(args.out)[row * 64 + c]
-                                              : ld_in(args.out, row * 64 + c, fmt);
-        Dn = fmaf(ld_in(args.dout, row * 64 + c, fmt), o, Dn);
+      const uint4* dsrc = reinterpret_cast<const uint4*>(args.dout) + row * 8;
+      uint4 dv[8];
+      #pragma unroll
+      for (int c = 0; c < 8; ++c) dv[c] = dsrc[c];
+      if (args.out_fmt == kF32) {
+        const float4* osrc = reinterpret_cast<const float4*>(args.out) + row * 16;
+        float4 ov[16];
+        #pragma unroll
+        for (int c = 0; c < 16; ++c) ov[c] = osrc[c];
+        #pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t dw[4] = {dv[c].x, dv[c].y, dv[c].z, dv[c].w};
+          const float o[8] = {ov[2 * c].x, ov[2 * c].y, ov[2 * c].z, ov[2 * c].w,
+                              ov[2 * c + 1].x, ov[2 * c + 1].y, ov[2 * c + 1].z, ov[2 * c + 1].w};
+          #pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 d2 = unpack_in(dw[e], fmt);
+            Dn = fmaf(d2.x, o[2 * e], Dn);
+            Dn = fmaf(d2.y, o[2 * e + 1], Dn);
+          }
+        }
+      } else {
+        const uint4* osrc = reinterpret_cast<const uint4*>(args.out) + row * 8;
+        uint4 ov[8];
+        #pragma unroll
+        for (int c = 0; c < 8; ++c) ov[c] = osrc[c];
+        #pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t dw[4] = {dv[c].x, dv[c].y, dv[c].z, dv[c].w};
+          const uint32_t ow[4] = {ov[c].x, ov[c].y, ov[c].z, ov[c].w};
+          #pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 d2 = unpack_in(dw[e], fmt), o2 = unpack_in(ow[e], fmt);
+            Dn = fmaf(d2.x, o2.x, Dn);
+            Dn = fmaf(d2.y, o2.y, Dn);
+          }
+        }
       }
       args.D[row] = Dn;
     }
