@@ -36,7 +36,11 @@
 
 namespace dera {
 
-constexpr int kBwdColsThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 softmax (two per TMEM lane quarter)
+// cols kernel: warp 0 TMA, warp 1 MMA, then kColsParts softmax warps per TMEM
+// lane quarter, which split each query tile's 128 columns into 16-column
+// blocks, 3 + 3 + 2
+constexpr int kColsParts = 3;
+constexpr int kBwdColsThreads = 64 + 128 * kColsParts;
 constexpr int kBwdStages = 3;      // K/V (rows kernel) or Q/dO (cols kernel) ring depth
 
 
@@ -561,7 +565,7 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
   constexpr int fmt = BF16 ? kBF16 : kF16;
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const BwdCta cta = bwd_setup<SM>(smem_raw, warp, 2 * kBlockM);
+  const BwdCta cta = bwd_setup<SM>(smem_raw, warp, kColsParts * kBlockM);
   uint8_t* smem = cta.smem;
   uint64_t* bars = cta.bars;
   volatile int* abort_flag = cta.abort_flag;
@@ -640,8 +644,10 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     // ---------------------------------------------------------------- softmax threads
     const int wq = warp & 3;
     const int m = wq * 32 + lane;          // key slot of the tile
-    const int half = (warp - 2) >> 2;      // query columns [64 half, 64 half + 64) of every tile
-    const int t = threadIdx.x - 64;        // index among the 256 staging threads
+    const int part = (warp - 2) >> 2;      // query-column blocks [3 part, 3 part + nb) of every tile
+    const int nb = part < 2 ? 3 : 2;       // 16-column blocks of this part
+    constexpr int kStg = kColsParts * kBlockM;
+    const int t = threadIdx.x - 64;        // index among the kStg staging threads
     const int g = m / WP, kw = m % WP;
     const int kh = j * KHT + g;
     const bool key_valid = m < BN && kw < W && kh < H;
@@ -667,13 +673,13 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         // the tile's rel_w rows are one contiguous, 16-byte aligned block
         // (WP is a multiple of 4) copied as it lies
         const float4* src = reinterpret_cast<const float4*>(args.rel_w + base * W);
-        for (int e = t; e < rows * (WP / 4); e += 2 * kBlockM) cp_async16(buf + 4 * e, src + e);
+        for (int e = t; e < rows * (WP / 4); e += kStg) cp_async16(buf + 4 * e, src + e);
       } else {
         // element e = rr W + c of the block goes to row rr, column c; (rr, c)
         // advanced without a division per element
-        const int step_r = (2 * kBlockM) / W, step_c = (2 * kBlockM) - step_r * W;
+        const int step_r = kStg / W, step_c = kStg - step_r * W;
         int rr = t / W, c = t - (t / W) * W;
-        for (int e = t; e < rows * W; e += 2 * kBlockM) {
+        for (int e = t; e < rows * W; e += kStg) {
           cp_async4(buf + rr * WP + c, args.rel_w + base * W + e, 4u);
           rr += step_r;
           c += step_c;
@@ -683,14 +689,14 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
           }
         }
       }
-      for (int e = t; e < kBlockM * KHT; e += 2 * kBlockM) {
+      for (int e = t; e < kBlockM * KHT; e += kStg) {
         const int rr = e / KHT, gg = e - rr * KHT, khh = j * KHT + gg;
         const bool v = rr < rows && khh < H;
         cp_async4(buf + (64 + gg) * RS + rr, args.rel_h + (v ? (base + rr) * H + khh : 0), v ? 4u : 0u);
       }
       if (t < kBlockM) {
         cp_async4(buf + 72 * RS + t, args.lse + (t < rows ? base + t : 0), t < rows ? 4u : 0u);
-      } else {
+      } else if (t < 2 * kBlockM) {
         const int u = t - kBlockM;
         cp_async4(buf + 73 * RS + u, args.D + (u < rows ? base + u : 0), u < rows ? 4u : 0u);
       }
@@ -712,7 +718,7 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
       if (!ok) break;
       if (i + 1 < n_qt) stage(i + 1, (i + 1) & 1);
       const float* buf = stage_base + (i & 1) * kBufFloats;
-      const float* rw = buf + 64 * half * WP + kw;   // rel_w of this half's first query column
+      const float* rw = buf + 48 * part * WP + kw;   // rel_w of this part's first query column
       const float* rhT = buf + (64 + g) * RS;     // g < 8 for every key slot
       const float* lseT = buf + 72 * RS;
       const float* DT = buf + 73 * RS;
@@ -721,18 +727,19 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
       ok = warp_all(mbar_wait(&bars[kBwSFull], i & 1, abort_flag, status));
       if (!ok) break;
       tc_fence_after();
-      // this half's four 16-column blocks; the next block's S^T and dP^T
-      // loads are in flight while the current one is computed
-      const int c_first = 64 * half;
+      // this part's 16-column blocks; the next block's S^T and dP^T loads are
+      // in flight while the current one is computed
+      const int c_first = 48 * part;
       const float2 sl2v = make_float2(sl2, sl2), l2ev = make_float2(kLog2e, kLog2e);
       uint32_t us[2][16], up[2][16];
       tmem_ld16(tS + c_first, us[0]);
       tmem_ld16(tdP + c_first, up[0]);
       #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 3; ++q) {
+        if (q == nb) break;
         const int cb = c_first + 16 * q;
         tmem_wait_ld();
-        if (q < 3) {
+        if (q + 1 < nb) {
           tmem_ld16(tS + cb + 16, us[(q + 1) & 1]);
           tmem_ld16(tdP + cb + 16, up[(q + 1) & 1]);
         }
@@ -740,7 +747,7 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         #pragma unroll
         for (int k4 = 0; k4 < 16; k4 += 4) {
           const int c4 = cb + k4;
-          const int cr = 16 * q + k4;   // query column c4, counted from this half's first
+          const int cr = 16 * q + k4;   // query column c4, counted from this part's first
           const float4 w4 = make_float4(rw[cr * WP], rw[(cr + 1) * WP], rw[(cr + 2) * WP], rw[(cr + 3) * WP]);
           const float4 h4 = *reinterpret_cast<const float4*>(rhT + c4);
           const float4 l4 = *reinterpret_cast<const float4*>(lseT + c4);
@@ -788,16 +795,16 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     }
     cp_async_wait_all();
     if (ok) ok = warp_all(mbar_wait(&bars[kBwMmaDone], (n_qt - 1) & 1, abort_flag, status));
-    if (ok) {
+    if (ok && part < 2) {
       tc_fence_after();
       uint32_t a[32];
       const size_t tok = static_cast<size_t>(bh) * N + static_cast<size_t>(kh) * W + kw;
       const float sc = args.scale;
       // tcgen05.ld is warp-collective: every lane loads, lanes with a key store;
-      // the first half of the warps writes dv, the second dk
-      const uint32_t tacc = half == 0 ? tdV : tdK;
-      void* dst = half == 0 ? args.dv : args.dk;
-      const float mul = half == 0 ? 1.0f : sc;
+      // the warps of part 0 write dv, those of part 1 dk
+      const uint32_t tacc = part == 0 ? tdV : tdK;
+      void* dst = part == 0 ? args.dv : args.dk;
+      const float mul = part == 0 ? 1.0f : sc;
       #pragma unroll
       for (int h = 0; h < 2; ++h) {
         tmem_ld32(tacc + 32 * h, a);
