@@ -97,7 +97,8 @@ enum : int {
   kBwTFull = kBwAllDone + 1,               // rows kernel: both tables landed
   kBwGFull = kBwTFull + 1,                 // rows kernel: the softmax threads wrote dG and dG^T (count 128)
   kBwBDone = kBwGFull + 1,                 // rows kernel: the bias products of one table are complete
-  kBwCount = kBwBDone + 1
+  kBwSFree = kBwBDone + 1,                 // softmax threads hold this tile's S and dP in registers
+  kBwCount = kBwSFree + 1
 };
 // rows kernel: a three-stage K/V ring; staging holds each thread's rel_h row
 // (later its drel_h row) and its drel_w row, 2 x 128 rows of 65 floats
@@ -142,6 +143,7 @@ __device__ __forceinline__ BwdCta bwd_setup(uint8_t* smem_raw, int warp, int n_c
     mbar_init(&c.bars[kBwTFull], 1);
     mbar_init(&c.bars[kBwGFull], n_compute);
     mbar_init(&c.bars[kBwBDone], 1);
+    mbar_init(&c.bars[kBwSFree], n_compute);
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -250,13 +252,14 @@ relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
       ok = warp_all(mbar_wait(&bars[kBwRingFull + s], (j / KS) & 1, abort_flag, status));
       if (!ok) break;
       if (j > 0) {
-        // the softmax threads have read S(j-1), dP(j-1) and written dZ(j-1)
-        ok = warp_all(mbar_wait(&bars[kBwPFull], (j - 1) & 1, abort_flag, status));
+        // the softmax threads hold S(j-1) and dP(j-1) in registers
+        ok = warp_all(mbar_wait(&bars[kBwSFree], (j - 1) & 1, abort_flag, status));
         if (!ok) break;
       }
       tc_fence_after();
-      // S(j) and dP(j) first, so the softmax threads start on tile j while
-      // dZ(j-1) k runs; they store dZ(j) only once that product has read dZ(j-1)
+      // S(j) and dP(j) first, so that they run while the softmax threads finish
+      // tile j - 1 and start on tile j while dZ(j-1) k runs; they store dZ(j)
+      // only once that product has read dZ(j-1)
       #pragma unroll
       for (int k = 0; k < 4; ++k)
         umma_ss_w(tbase + 0, d_q + 2 * k, d_ring + s * kStageStep + 2 * k, id_s, k > 0);
@@ -264,7 +267,13 @@ relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
       for (int k = 0; k < 4; ++k)
         umma_ss_w(tbase + 128, d_do + 2 * k, d_ring + s * kStageStep + kVOfs + 2 * k, id_s, k > 0);
       umma_commit_w(&bars[kBwSFull]);
-      if (j > 0) issue_dq(j - 1);
+      if (j > 0) {
+        // dZ(j-1) is written
+        ok = warp_all(mbar_wait(&bars[kBwPFull], (j - 1) & 1, abort_flag, status));
+        if (!ok) break;
+        tc_fence_after();
+        issue_dq(j - 1);
+      }
     }
     if (ok) ok = warp_all(mbar_wait(&bars[kBwPFull], (n_kv - 1) & 1, abort_flag, status));
     if (ok) {
@@ -427,6 +436,10 @@ relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         if (bb + 1 < BN / 16) {
           tmem_ld16(tS + cb + 16, us[cur ^ 1]);
           tmem_ld16(tdP + cb + 16, up[cur ^ 1]);
+        } else {
+          // all of S(j) and dP(j) is in registers: S(j+1) and dP(j+1) may go ahead
+          tc_fence_before();
+          mbar_arrive(&bars[kBwSFree]);
         }
         uint32_t pk[8];
         #pragma unroll
@@ -618,12 +631,13 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
       ok = warp_all(mbar_wait(&bars[kBwRingFull + s], (i / KS) & 1, abort_flag, status));
       if (!ok) break;
       if (i > 0) {
-        ok = warp_all(mbar_wait(&bars[kBwPFull], (i - 1) & 1, abort_flag, status));
+        // the softmax threads hold S^T(i-1) and dP^T(i-1) in registers
+        ok = warp_all(mbar_wait(&bars[kBwSFree], (i - 1) & 1, abort_flag, status));
         if (!ok) break;
       }
       tc_fence_after();
-      // S^T(i) and dP^T(i) first, so the softmax threads start on query tile i
-      // while dv and dk take tile i - 1
+      // S^T(i) and dP^T(i) first, so that they run while the softmax threads
+      // finish tile i - 1 and start on query tile i while dv and dk take tile i - 1
       #pragma unroll
       for (int k = 0; k < 4; ++k)
         umma_ss_w(tbase + 0, d_k + 2 * k, d_ring + s * kStageStep + 2 * k, id_s, k > 0);
@@ -631,7 +645,13 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
       for (int k = 0; k < 4; ++k)
         umma_ss_w(tbase + 128, d_v + 2 * k, d_ring + s * kStageStep + kDoOfs + 2 * k, id_s, k > 0);
       umma_commit_w(&bars[kBwSFull]);
-      if (i > 0) issue_acc(i - 1);
+      if (i > 0) {
+        // P^T(i-1) and dZ^T(i-1) are written
+        ok = warp_all(mbar_wait(&bars[kBwPFull], (i - 1) & 1, abort_flag, status));
+        if (!ok) break;
+        tc_fence_after();
+        issue_acc(i - 1);
+      }
     }
     if (ok && warp_all(mbar_wait(&bars[kBwPFull], (n_qt - 1) & 1, abort_flag, status))) {
       tc_fence_after();
@@ -742,6 +762,10 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         if (q + 1 < nb) {
           tmem_ld16(tS + cb + 16, us[(q + 1) & 1]);
           tmem_ld16(tdP + cb + 16, up[(q + 1) & 1]);
+        } else {
+          // all of this thread's S^T(i) and dP^T(i) is in registers
+          tc_fence_before();
+          mbar_arrive(&bars[kBwSFree]);
         }
         uint32_t pp[8], pz[8];
         #pragma unroll
