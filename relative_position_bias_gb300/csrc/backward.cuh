@@ -364,7 +364,9 @@ relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
       for (int kw = 0; kw < WP; ++kw)
         bw[kw] = (kw < W) ? (row_valid ? kLog2e * args.rel_w[row * W + kw] : 0.f) : NEG_INF;
     }
-    const float lse2 = row_valid ? args.lse[row] : 0.f;
+    // a row past N takes lse = +inf, so that its P is exactly 0 (its S and dP
+    // are 0: the TMA fills its q and dO rows with zeros)
+    const float lse2 = row_valid ? args.lse[row] : __int_as_float(0x7f800000);
     // D = dO . out for this row (out in fp32 or in the input dtype), summed in
     // column order
     float Dn = 0.f;
@@ -421,9 +423,9 @@ relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
       ok = warp_all(mbar_wait(&bars[kBwSFull], j & 1, abort_flag, status));
       if (!ok) break;
       tc_fence_after();
-      float dRH[KHT];
+      float2 dRH[KHT];   // even and odd columns apart
       #pragma unroll
-      for (int g = 0; g < KHT; ++g) dRH[g] = 0.f;
+      for (int g = 0; g < KHT; ++g) dRH[g] = make_float2(0.f, 0.f);
       // 16-column blocks, the next block's S and dP loads in flight while the
       // current one is computed
       uint32_t us[2][16], up[2][16];
@@ -451,12 +453,11 @@ relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
           const float2 dp2 = make_float2(__uint_as_float(up[cur][k]), __uint_as_float(up[cur][k + 1]));
           const float2 b2 = fadd2(make_float2(bw[kw], bw[kw + 1]), make_float2(bhv[g], bhv[g]));
           const float2 x = fadd2(ffma2(s2, sl2v, b2), nlse2);
-          float2 d = __fmul2_rn(make_float2(ex2_approx(x.x), ex2_approx(x.y)), fadd2(dp2, nD2));
-          if (!row_valid) d = make_float2(0.f, 0.f);
+          const float2 d = __fmul2_rn(make_float2(ex2_approx(x.x), ex2_approx(x.y)), fadd2(dp2, nD2));
           const float2 acc = fadd2(make_float2(dRW[kw], dRW[kw + 1]), d);
           dRW[kw] = acc.x;
           dRW[kw + 1] = acc.y;
-          dRH[g] += d.x + d.y;
+          dRH[g] = fadd2(dRH[g], d);
           pk[k / 2] = pack_in(d.x, d.y, fmt);
         }
         if (bb == 0 && j > 0) {
@@ -476,7 +477,7 @@ relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
       mbar_arrive(&bars[kBwPFull]);
       #pragma unroll
       for (int g = 0; g < KHT; ++g)
-        if (j * KHT + g < H) bh_row[j * KHT + g] = dRH[g];
+        if (j * KHT + g < H) bh_row[j * KHT + g] = dRH[g].x + dRH[g].y;
     }
     #pragma unroll
     for (int kw = 0; kw < WP; ++kw)
