@@ -173,9 +173,10 @@ DERA_API dera_status dera_relpos_fused_lse(const void* q, const void* k, const v
 
 /*
  * Scratch needed by dera_relpos_fused_backward (bytes, written to *bytes):
- * 4 * (BH N (H + W + 1) + BH ceil(N / 128) 64 (2H - 1 + 2W - 1)) plus
- * alignment: the compact bias, one term per row and per-query-tile
- * table-gradient partials, all fp32.  head_dim must be 64.
+ * 4 * (BH N (H + W + 1) + BH ceil(N / 128) (128 H + 64 (2H - 1 + 2W - 1)))
+ * plus alignment: the compact bias, one term per row, the rel_h term of the
+ * exponent laid out by key grid row, and per-query-tile table-gradient
+ * partials, all fp32.  head_dim must be 64.
  */
 DERA_API dera_status dera_relpos_backward_workspace_size(int BH, int H, int W, int head_dim, size_t* bytes);
 

@@ -104,10 +104,11 @@ enum : int {
 // (later its drel_h row) and its drel_w row, 2 x 128 rows of 65 floats
 using BwdRowsSmem = BwdSmem<3, 2 * 128 * 65 * 4>;
 // cols kernel: a three-stage Q/dO ring; staging holds two buffers of one query
-// tile's rel_w (query rows of WP floats, at most 128 x 64 floats) and, transposed
-// into rows of 132 floats, its rel_h entries, lse and D (74 such rows in all)
+// tile's rel_w (query rows of WP floats, at most 128 x 64 floats) and, in rows
+// of 132 floats, its log2(e) rel_h - lse for the key tile's grid rows and D
+// (73 such rows in all)
 constexpr int kColsStageRow = 132;
-constexpr int kColsStageFloats = 74 * kColsStageRow;
+constexpr int kColsStageFloats = 73 * kColsStageRow;
 using BwdColsSmem = BwdSmem<3, 2 * kColsStageFloats * 4>;
 static_assert(kBwCount <= BwdRowsSmem::kNumBars, "barrier slots");
 
@@ -328,6 +329,9 @@ relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     float* bh_row = stg + r * 65;             // rel_h (base 2); each entry becomes drel_h once read
     float* dw_row = stg + 128 * 65 + r * 65;  // drel_w
     const int Hpad = n_kv * KHT;
+    // a row past N takes lse = +inf, so that its P is exactly 0 (its S and dP
+    // are 0: the TMA fills its q and dO rows with zeros)
+    const float lse2 = row_valid ? args.lse[row] : __int_as_float(0x7f800000);
     // The row loads below are independent 16-byte loads where the row allows
     // (rows of the 16-byte aligned workspace whose length is a multiple of 4;
     // dO and out rows of 64 elements), so that they are all in flight at once.
@@ -364,9 +368,13 @@ relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
       for (int kw = 0; kw < WP; ++kw)
         bw[kw] = (kw < W) ? (row_valid ? kLog2e * args.rel_w[row * W + kw] : 0.f) : NEG_INF;
     }
-    // a row past N takes lse = +inf, so that its P is exactly 0 (its S and dP
-    // are 0: the TMA fills its q and dO rows with zeros)
-    const float lse2 = row_valid ? args.lse[row] : __int_as_float(0x7f800000);
+    if (row_valid) {
+      // the exponent's rel_h term, log2(e) rel_h - lse, by key grid row for
+      // the cols kernel (coalesced over the warp's rows)
+      const size_t np = static_cast<size_t>(args.n_qtiles) * kBlockM;
+      float* hl = args.hl + static_cast<size_t>(bh) * H * np + n;
+      for (int kh = 0; kh < H; ++kh) hl[kh * np] = bh_row[kh] - lse2;
+    }
     // D = dO . out for this row (out in fp32 or in the input dtype), summed in
     // column order
     float Dn = 0.f;
@@ -566,8 +574,8 @@ __device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
 // columns: S^T [0, 128), dP^T [128, 256), P^T and dZ^T in the input dtype as
 // packed pairs [256, 320) and [320, 384), dv [384, 448), dk [448, 512).
 // Per query tile the softmax threads stage (cp.async, one tile ahead) the
-// tile's rel_w rows [128][WP], its rel_h entries for this key tile's grid rows
-// [KHT][128], lse and D.
+// tile's rel_w rows [128][WP], log2(e) rel_h - lse for this key tile's grid
+// rows [KHT][128] (which the rows kernel wrote in that layout) and D.
 template <int WP, bool BF16>
 __global__ void __launch_bounds__(kBwdColsThreads, 1)
 relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -678,11 +686,11 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     const float sl2 = args.scale_log2;
     float* stage_base = reinterpret_cast<float*>(smem + SM::kStaging);
     // buffer b: rel_w [n][kw] in query rows of WP floats (the first 128 WP
-    // floats), then, transposed so that a thread reads four query columns at
-    // once, rel_h [g][n] in rows 64..71, lse in row 72 and D in row 73 (rows of
-    // kColsStageRow floats; lse and D hold zeros past N).  rel_w entries past
-    // N or past W are never written: they reach only masked query columns or
-    // key slots without a key.
+    // floats), then, by query column so that a thread reads four at once,
+    // log2(e) rel_h - lse [g][n] in rows 64..71 and D in row 72 (rows of
+    // kColsStageRow floats; D holds zeros past N).  rel_w and rel_h entries
+    // past N, past W or past H are never written: they reach only masked query
+    // columns or key slots without a key.
     constexpr int kBufFloats = kColsStageFloats, RS = kColsStageRow;
     static_assert(kBlockM * WP <= 64 * RS, "rel_w rows fit below the transposed rows");
     auto stage = [&](int i, int b) {
@@ -710,17 +718,14 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
           }
         }
       }
-      for (int e = t; e < kBlockM * KHT; e += kStg) {
-        const int rr = e / KHT, gg = e - rr * KHT, khh = j * KHT + gg;
-        const bool v = rr < rows && khh < H;
-        cp_async4(buf + (64 + gg) * RS + rr, args.rel_h + (v ? (base + rr) * H + khh : 0), v ? 4u : 0u);
+      // whole 128-column rows of the rel_h term (16-byte chunks), one per grid row
+      const size_t np = static_cast<size_t>(n_qt) * kBlockM;
+      const float* hl = args.hl + (static_cast<size_t>(bh) * H + j * KHT) * np + n0;
+      for (int e = t; e < KHT * (kBlockM / 4); e += kStg) {
+        const int gg = e / (kBlockM / 4), c = e - gg * (kBlockM / 4);
+        if (j * KHT + gg < H) cp_async16(buf + (64 + gg) * RS + 4 * c, hl + gg * np + 4 * c);
       }
-      if (t < kBlockM) {
-        cp_async4(buf + 72 * RS + t, args.lse + (t < rows ? base + t : 0), t < rows ? 4u : 0u);
-      } else if (t < 2 * kBlockM) {
-        const int u = t - kBlockM;
-        cp_async4(buf + 73 * RS + u, args.D + (u < rows ? base + u : 0), u < rows ? 4u : 0u);
-      }
+      if (t < kBlockM) cp_async4(buf + 72 * RS + t, args.D + (t < rows ? base + t : 0), t < rows ? 4u : 0u);
     };
     uint32_t stg_phase = 0;
     auto group_sync = [&]() -> bool {
@@ -741,8 +746,7 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
       const float* buf = stage_base + (i & 1) * kBufFloats;
       const float* rw = buf + 48 * part * WP + kw;   // rel_w of this part's first query column
       const float* rhT = buf + (64 + g) * RS;     // g < 8 for every key slot
-      const float* lseT = buf + 72 * RS;
-      const float* DT = buf + 73 * RS;
+      const float* DT = buf + 72 * RS;
       const int rows = min(kBlockM, N - i * kBlockM);
       const bool full = rows == kBlockM;
       ok = warp_all(mbar_wait(&bars[kBwSFull], i & 1, abort_flag, status));
@@ -775,7 +779,6 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
           const int cr = 16 * q + k4;   // query column c4, counted from this part's first
           const float4 w4 = make_float4(rw[cr * WP], rw[(cr + 1) * WP], rw[(cr + 2) * WP], rw[(cr + 3) * WP]);
           const float4 h4 = *reinterpret_cast<const float4*>(rhT + c4);
-          const float4 l4 = *reinterpret_cast<const float4*>(lseT + c4);
           const float4 d4 = *reinterpret_cast<const float4*>(DT + c4);
           // Query columns past N must not reach dv or dk; key slots without a key
           // need no mask, since their P^T and dZ^T rows only reach their own
@@ -785,12 +788,11 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
           for (int hp = 0; hp < 4; hp += 2) {
             const float2 w2 = hp == 0 ? make_float2(w4.x, w4.y) : make_float2(w4.z, w4.w);
             const float2 h2 = hp == 0 ? make_float2(h4.x, h4.y) : make_float2(h4.z, h4.w);
-            const float2 nl2 = hp == 0 ? make_float2(-l4.x, -l4.y) : make_float2(-l4.z, -l4.w);
             const float2 nd2 = hp == 0 ? make_float2(-d4.x, -d4.y) : make_float2(-d4.z, -d4.w);
             const float2 s2 = make_float2(__uint_as_float(us[q & 1][k4 + hp]), __uint_as_float(us[q & 1][k4 + hp + 1]));
             const float2 dp2 =
                 make_float2(__uint_as_float(up[q & 1][k4 + hp]), __uint_as_float(up[q & 1][k4 + hp + 1]));
-            const float2 x = ffma2(s2, sl2v, ffma2(fadd2(w2, h2), l2ev, nl2));
+            const float2 x = ffma2(s2, sl2v, ffma2(w2, l2ev, h2));
             float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
             if (!full) {
               if (c4 + hp >= rows) p.x = 0.f;

@@ -270,7 +270,7 @@ dera_status current_device(int* dev) {
 
 // Workspace of the backward: fp32 regions, each 256-byte aligned.
 struct BwdLayout {
-  size_t rel_h, rel_w, D, parts, total;
+  size_t rel_h, rel_w, D, hl, parts, total;
   int n_qtiles;
   BwdLayout(int BH, int H, int W) {
     const size_t rows = static_cast<size_t>(BH) * H * W;
@@ -284,6 +284,7 @@ struct BwdLayout {
     rel_h = take(rows * H);
     rel_w = take(rows * W);
     D = take(rows);
+    hl = take(static_cast<size_t>(BH) * H * n_qtiles * kBlockM);
     parts = take(static_cast<size_t>(BH) * n_qtiles * (2 * H - 1 + 2 * W - 1) * 64);
     total = o;
   }
@@ -577,6 +578,7 @@ dera_status dera_relpos_fused_backward(const void* q, const void* k, const void*
   a.out = out;
   a.dout = dout;
   a.D = reinterpret_cast<float*>(ws + L.D);
+  a.hl = reinterpret_cast<float*>(ws + L.hl);
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;

@@ -140,12 +140,13 @@ def test_backward_rejects_before_any_cuda_work(lib):
 
 
 def test_backward_workspace_size_formula(lib):
-    """fp32 regions, each 256-byte aligned: rel_h, rel_w, D, per-query-tile table-gradient partials."""
+    """fp32 regions, each 256-byte aligned: rel_h, rel_w, D, the exponent's rel_h term by key grid
+    row over whole query tiles, per-query-tile table-gradient partials."""
     def a256(x):
         return (x + 255) // 256 * 256
     for BH, H, W in [(1, 4, 4), (12, 64, 64), (3, 40, 40), (2, 14, 14), (5, 7, 30)]:
         rows, nq = BH * H * W, -(-(H * W) // 128)
-        want = (a256(4 * rows * H) + a256(4 * rows * W) + a256(4 * rows)
+        want = (a256(4 * rows * H) + a256(4 * rows * W) + a256(4 * rows) + a256(4 * BH * H * nq * 128)
                 + a256(4 * BH * nq * (2 * H - 1 + 2 * W - 1) * 64))
         assert rpb.backward_workspace_size(BH, H, W, 64) == want
     with pytest.raises(rpb.DeraError):
