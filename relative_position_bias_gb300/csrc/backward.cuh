@@ -105,7 +105,7 @@ enum : int {
 using BwdRowsSmem = BwdSmem<3, 2 * 128 * 65 * 4>;
 // cols kernel: a three-stage Q/dO ring; staging holds two buffers of one query
 // tile's rel_w (query rows of WP floats, at most 128 x 64 floats) and, in rows
-// of 132 floats, its log2(e) rel_h - lse for the key tile's grid rows and D
+// of 132 floats, its log2(e) rel_h - lse for the key tile's grid rows and -D
 // (73 such rows in all)
 constexpr int kColsStageRow = 132;
 constexpr int kColsStageFloats = 73 * kColsStageRow;
@@ -417,17 +417,17 @@ relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
           }
         }
       }
-      args.D[row] = Dn;
+      args.D[row] = -Dn;   // negated, as the cols kernel adds it
     }
     float dRW[WP];
     #pragma unroll
     for (int kw = 0; kw < WP; ++kw) dRW[kw] = 0.f;
-    const float2 sl2v = make_float2(sl2, sl2), nlse2 = make_float2(-lse2, -lse2), nD2 = make_float2(-Dn, -Dn);
+    const float2 sl2v = make_float2(sl2, sl2), nD2 = make_float2(-Dn, -Dn);
     bool ok = true;
     for (int j = 0; ok && j < n_kv; ++j) {
       float bhv[KHT];
       #pragma unroll
-      for (int g = 0; g < KHT; ++g) bhv[g] = bh_row[j * KHT + g];
+      for (int g = 0; g < KHT; ++g) bhv[g] = bh_row[j * KHT + g] - lse2;   // the exponent's rel_h and lse terms
       ok = warp_all(mbar_wait(&bars[kBwSFull], j & 1, abort_flag, status));
       if (!ok) break;
       tc_fence_after();
@@ -460,7 +460,7 @@ relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
           const float2 s2 = make_float2(__uint_as_float(us[cur][k]), __uint_as_float(us[cur][k + 1]));
           const float2 dp2 = make_float2(__uint_as_float(up[cur][k]), __uint_as_float(up[cur][k + 1]));
           const float2 b2 = fadd2(make_float2(bw[kw], bw[kw + 1]), make_float2(bhv[g], bhv[g]));
-          const float2 x = fadd2(ffma2(s2, sl2v, b2), nlse2);
+          const float2 x = ffma2(s2, sl2v, b2);
           const float2 d = __fmul2_rn(make_float2(ex2_approx(x.x), ex2_approx(x.y)), fadd2(dp2, nD2));
           const float2 acc = fadd2(make_float2(dRW[kw], dRW[kw + 1]), d);
           dRW[kw] = acc.x;
@@ -575,7 +575,7 @@ __device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
 // packed pairs [256, 320) and [320, 384), dv [384, 448), dk [448, 512).
 // Per query tile the softmax threads stage (cp.async, one tile ahead) the
 // tile's rel_w rows [128][WP], log2(e) rel_h - lse for this key tile's grid
-// rows [KHT][128] (which the rows kernel wrote in that layout) and D.
+// rows [KHT][128] (which the rows kernel wrote in that layout) and -D.
 template <int WP, bool BF16>
 __global__ void __launch_bounds__(kBwdColsThreads, 1)
 relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -687,8 +687,8 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     float* stage_base = reinterpret_cast<float*>(smem + SM::kStaging);
     // buffer b: rel_w [n][kw] in query rows of WP floats (the first 128 WP
     // floats), then, by query column so that a thread reads four at once,
-    // log2(e) rel_h - lse [g][n] in rows 64..71 and D in row 72 (rows of
-    // kColsStageRow floats; D holds zeros past N).  rel_w and rel_h entries
+    // log2(e) rel_h - lse [g][n] in rows 64..71 and -D in row 72 (rows of
+    // kColsStageRow floats; -D holds zeros past N).  rel_w and rel_h entries
     // past N, past W or past H are never written: they reach only masked query
     // columns or key slots without a key.
     constexpr int kBufFloats = kColsStageFloats, RS = kColsStageRow;
@@ -788,7 +788,7 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
           for (int hp = 0; hp < 4; hp += 2) {
             const float2 w2 = hp == 0 ? make_float2(w4.x, w4.y) : make_float2(w4.z, w4.w);
             const float2 h2 = hp == 0 ? make_float2(h4.x, h4.y) : make_float2(h4.z, h4.w);
-            const float2 nd2 = hp == 0 ? make_float2(-d4.x, -d4.y) : make_float2(-d4.z, -d4.w);
+            const float2 nd2 = hp == 0 ? make_float2(d4.x, d4.y) : make_float2(d4.z, d4.w);   // -D
             const float2 s2 = make_float2(__uint_as_float(us[q & 1][k4 + hp]), __uint_as_float(us[q & 1][k4 + hp + 1]));
             const float2 dp2 =
                 make_float2(__uint_as_float(up[q & 1][k4 + hp]), __uint_as_float(up[q & 1][k4 + hp + 1]));

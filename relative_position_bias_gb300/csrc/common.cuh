@@ -78,7 +78,7 @@ struct BwdArgs {
   const float* lse;     // [BH, N] base-2 log-sum-exp of each row's logits (forward)
   const void* out;      // [BH, N, 64] forward output (input dtype)
   const void* dout;     // [BH, N, 64] upstream gradient (input dtype)
-  float* D;             // [BH, N] dO . out per row (rows kernel writes, cols kernel reads)
+  float* D;             // [BH, N] -(dO . out) per row (rows kernel writes, cols kernel reads)
   float* hl;            // [BH, H, n_qtiles * 128] log2(e) rel_h - lse, key grid row major
                         // (rows kernel writes, cols kernel reads)
   void* dq;             // [BH, N, 64] grad dtype (rows kernel)
