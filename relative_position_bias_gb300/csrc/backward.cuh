@@ -504,6 +504,7 @@ relpos_bwd_rows_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         ok = warp_all(mbar_wait(&bars[kBwBDone], 0, abort_flag, status));
         if (!ok) break;
       }
+      #pragma unroll 8
       for (int i = 0; i < 128; i += 2) {
         const int k0 = coord - i + L - 1, k1 = k0 - 1;
         const float v0 = (row_valid && k0 >= 0 && k0 < L) ? drow[k0] : 0.f;
