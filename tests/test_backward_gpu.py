@@ -136,3 +136,43 @@ def test_backward_empty_batch():
     torch.cuda.synchronize()
     assert dq.shape == (0, H * W, 64) and dk.shape == dq.shape and dv.shape == dq.shape
     assert torch.count_nonzero(dth) == 0 and torch.count_nonzero(dtw) == 0
+
+
+def _bench_case(name):
+    """A workload exactly as `bench.py --entry backward` times it: the seeded inputs, dout from
+    seed 1000, the training forward's out and lse in the input dtype, gradients in the input
+    dtype."""
+    w = I.WORKLOADS[name]
+    x = I.make_inputs(w, seed=0)
+    d = {n: t.cuda() for n, t in x.items()}
+    g = torch.Generator().manual_seed(1000)
+    dout = torch.randn(w.BH, w.N, w.d, generator=g).to(w.torch_dtype)
+    out, lse = rpb.fused_lse(d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], w.H, w.W, w.scale)
+    grads = rpb.fused_backward(d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], out, lse, dout.cuda(), w.H,
+                               w.W, w.scale, grad_dtype=w.torch_dtype)
+    torch.cuda.synchronize()
+    return w, x, d, dout, out, lse, grads
+
+
+def _check(label, got, ref, dtype):
+    rl2_tol, max_tol = TOL[dtype]
+    g = got.double().cpu().numpy() if isinstance(got, torch.Tensor) else got
+    assert np.isfinite(g).all(), label
+    err = np.abs(g - ref).max()
+    scale_ref = max(np.abs(ref).max(), 1e-2)
+    rl2 = np.linalg.norm(g - ref) / max(np.linalg.norm(ref), 1e-2 * math.sqrt(ref.size))
+    record_margin(f"backward {label} (max-abs / max|ref|)", err / scale_ref, rl2, f"{max_tol:g} / {rl2_tol:g}")
+    assert rl2 <= rl2_tol, f"{label}: rel-L2 {rl2:.3e}"
+    assert err <= max_tol * scale_ref, f"{label}: max-abs {err:.3e} of max {scale_ref:.3e}"
+
+
+@pytest.mark.parametrize("name", ["global64", "batched64", "wide64", "ragged40", "window14"])
+def test_backward_full_size(name):
+    """The bench's call on each workload at its full size (input-dtype out and gradients), every
+    gradient element against the oracle, which takes the heads one at a time."""
+    w, x, _, dout, _, _, grads = _bench_case(name)
+    f = {n: I.to_f64(t) for n, t in x.items()}
+    want = oracle.fused_backward(f["q"], f["k"], f["v"], f["rel_pos_h"], f["rel_pos_w"], w.H, w.W, w.scale,
+                                 I.to_f64(dout))
+    for gname, got, ref in zip(["dq", "dk", "dv", "drel_pos_h", "drel_pos_w"], grads, want):
+        _check(f"{name} full {gname}", got, ref, w.torch_dtype)
