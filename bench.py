@@ -437,8 +437,8 @@ def backward_flops(BH: int, N: int, d: int = 64) -> float:
 
 
 def run_backward(args, w, rank: int, world: int) -> dict | None:
-    """`--entry backward`: one step = dera_relpos_fused_backward (projection, rows, cols, bias and
-    table kernels) on the workload, with the training forward's out and lse and a random dout
+    """`--entry backward`: one step = dera_relpos_fused_backward (projection, rows, cols and table
+    kernels) on the workload, with the training forward's out and lse and a random dout
     already in HBM; gradients in the input dtype."""
     import torch
     import relative_position_bias_gb300 as rpb
@@ -500,12 +500,12 @@ def run_backward(args, w, rank: int, world: int) -> dict | None:
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": cfg,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                     "traffic": None, "kernel": "the whole backward call (5 kernels)",
+                     "traffic": None, "kernel": "the whole backward call (4 kernels)",
                      "peak_source": f"bf16_tflops (burst) of {peak_src}", "flops_per_launch": flops,
                      "flops_executed": 14.0 * w.BH * w.N * w.N * w.d},
         "training_forward": {"ms": statistics.median(fwd_ms),
                              "tflops": attention_flops(w.BH, w.N, w.d) / (statistics.median(fwd_ms) * 1e-3) / 1e12},
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": 4 * args.steps,
         "clocks": clocks.summary(),
     }
 

@@ -861,8 +861,18 @@ __global__ void relpos_bwd_tables_kernel(const BwdArgs args, int n_blocks) {
   const int ol = threadIdx.x & 31, chunk = threadIdx.x >> 5;
   const int o = blockIdx.x * 32 + ol;
   float acc = 0.f;
-  if (o < total)
-    for (int b = chunk; b < n_blocks; b += 8) acc += args.parts[static_cast<size_t>(b) * total + o];
+  if (o < total) {
+    // eight loads in flight, then added in the same order as one at a time
+    int b = chunk;
+    for (; b + 56 < n_blocks; b += 64) {
+      float v[8];
+      #pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = args.parts[static_cast<size_t>(b + 8 * u) * total + o];
+      #pragma unroll
+      for (int u = 0; u < 8; ++u) acc += v[u];
+    }
+    for (; b < n_blocks; b += 8) acc += args.parts[static_cast<size_t>(b) * total + o];
+  }
   red[chunk][ol] = acc;
   __syncthreads();
   if (chunk == 0 && o < total) {
