@@ -21,11 +21,13 @@
 //                     the softmax threads (one per query row), dZ k accumulated
 //                     on the tensor core; then, also on the tensor core, dq's
 //                     part through the projection and the tile's partial table
-//                     gradients from the on-chip bias gradients; writes D, dq
-//                     and the partials.
+//                     gradients from the on-chip bias gradients; writes dq, the
+//                     partials, and for the cols kernel -D and the exponent's
+//                     rel_h term log2(e) rel_h - lse by key grid row.
 //   relpos_bwd_cols   one CTA per (head, key tile), query tiles streamed:
 //                     S^T = k q^T and dP^T = v dO^T, P^T and dZ^T per key row,
-//                     dv += P^T dO and dk += dZ^T q accumulated in TMEM.
+//                     dv += P^T dO and dk += dZ^T q accumulated in TMEM; runs
+//                     after the rows kernel, whose -D and rel_h term it reads.
 //   relpos_bwd_tables sums the per-tile partials in a fixed order.
 // Nothing is accumulated with atomics, so the result does not depend on the
 // order in which CTAs run.
@@ -569,9 +571,12 @@ __device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
 }
 
 // ---------------------------------------------------------------------------
-// Cols kernel: one CTA per (head, key tile of KHT grid rows); thread m of warps
-// 2-5 owns key slot m of the tile (TMEM lane m; slots past the tile's BN keys,
-// padded columns and padded grid rows compute nothing that is stored).  TMEM
+// Cols kernel: one CTA per (head, key tile of KHT grid rows); key slot m of the
+// tile is TMEM lane m, which the kColsParts softmax warps of lane quarter m / 32
+// share, each taking some of every query tile's 16-column blocks (slots past
+// the tile's BN keys, padded columns and padded grid rows compute nothing that
+// is stored).  The next query tile's S^T and dP^T go ahead once every softmax
+// thread holds the current ones in registers.  TMEM
 // columns: S^T [0, 128), dP^T [128, 256), P^T and dZ^T in the input dtype as
 // packed pairs [256, 320) and [320, 384), dv [384, 448), dk [448, 512).
 // Per query tile the softmax threads stage (cp.async, one tile ahead) the
@@ -693,7 +698,7 @@ relpos_bwd_cols_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     // past N, past W or past H are never written: they reach only masked query
     // columns or key slots without a key.
     constexpr int kBufFloats = kColsStageFloats, RS = kColsStageRow;
-    static_assert(kBlockM * WP <= 64 * RS, "rel_w rows fit below the transposed rows");
+    static_assert(kBlockM * WP <= 64 * RS, "rel_w rows fit below the rows by query column");
     auto stage = [&](int i, int b) {
       float* buf = stage_base + b * kBufFloats;
       const int n0 = i * kBlockM;
