@@ -282,6 +282,10 @@ def fused_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, rel_pos_h:
         with torch.cuda.device(q.device):
             need = backward_workspace_size(BH, H, W, d)
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+        if int(st or 0) != torch.cuda.current_stream(q.device).cuda_stream:
+            # freed when this call returns: the allocator must not hand it out again before
+            # the kernels on that stream are done with it
+            workspace.record_stream(torch.cuda.ExternalStream(int(st or 0), device=q.device))
     _check(lib.dera_relpos_fused_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(rel_pos_h), _ptr(rel_pos_w), _ptr(out),
                                           _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dth), _ptr(dtw),
                                           BH, H, W, d, float(scale), _code(q.dtype), _code(out.dtype), _code(gd),

@@ -125,6 +125,25 @@ def test_backward_is_deterministic():
         assert torch.equal(x16, x32.to(torch.bfloat16))
 
 
+def test_backward_on_another_stream():
+    """A call on a stream other than the current one (its scratch is recorded on that stream)
+    gives the same gradients, bit for bit."""
+    BH, H, W, dtype, sq, sk = CASES["grid16-bf16"]
+    x = make_case(BH, H, W, dtype, sq=sq, sk=sk, seed=7)
+    d = {n: t.cuda() for n, t in x.items()}
+    out, lse = rpb.fused_lse(d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], H, W, 0.125)
+    args = (d["q"], d["k"], d["v"], d["rel_pos_h"], d["rel_pos_w"], out, lse, d["dout"], H, W, 0.125)
+    a = rpb.fused_backward(*args)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    b = rpb.fused_backward(*args, stream=side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    for x1, x2 in zip(a, b):
+        assert torch.equal(x1, x2)
+
+
 def test_backward_empty_batch():
     """BH = 0: nothing to compute; the table gradients are zero."""
     H, W = 4, 4
