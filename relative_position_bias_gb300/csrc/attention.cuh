@@ -257,17 +257,31 @@ struct ReplayRecord {
   Segment sg;
 };
 
+// Key tiles of the forward: KeyTile's grid rows, except that a grid padded to
+// 40 columns (head_dim 64) takes three grid rows, 120 keys, into S and PV
+// products 128 keys wide.  Its last 8 columns are padding: their P is 0 and
+// their K and V rows are never loaded (V's are kept finite, see the kernel's
+// set-up).  Fewer, fuller key tiles than two grid rows of 80 keys.
+template <int WP, int D>
+struct FwdKeyTile {
+  static constexpr int KHT = (D == 64 && WP == 40) ? 3 : KeyTile<WP, D>::KHT;
+  static constexpr int BN = KHT * WP;               // keys loaded per tile
+  static constexpr int BNP = (BN + 15) / 16 * 16;   // width of the S and PV products
+  static_assert(BNP <= 128 && (BNP == BN || D == 64), "padded key tiles need head_dim 64");
+};
+
 template <int WP, bool FUSED, bool BF16, int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     relpos_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_th,
                        const __grid_constant__ CUtensorMap tm_tw, const AttnArgs args) {
-  using KT = KeyTile<WP, D>;
+  using KT = FwdKeyTile<WP, D>;
   using Dm = AttnDims<D, KT::BN>;
   using SM = AttnSmem<D, KT::BN>;
   constexpr int kBiasStride = Dm::kBiasStride;
   constexpr int KHT = KT::KHT;
-  constexpr int BN = KT::BN;
+  constexpr int BN = KT::BN;     // keys of a tile
+  constexpr int BNP = KT::BNP;   // columns of its S and PV products (BN, or BN padded to 16)
   constexpr int KS = Dm::kStages;
 
   extern __shared__ uint8_t smem_raw[];
@@ -328,6 +342,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (warp == 2) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
+  }
+  if constexpr (BNP > BN) {
+    // Rows BN..BNP-1 of every K and V stage are read by the products but never
+    // loaded by TMA (the fused prologue's tables, whose rows there are past the
+    // tables' ends for these widths, load zeros).  Their P is 0, and 0 times a
+    // finite V is 0, so V (and K, for tidiness) start as zeros.
+    constexpr int kPadChunks = (BNP - BN) * 128 / 16;   // 16-byte chunks per region (head_dim 64)
+    for (int i = threadIdx.x; i < KS * 2 * kPadChunks; i += kAttnThreads) {
+      const int s = i / (2 * kPadChunks), c = i - s * (2 * kPadChunks);
+      uint8_t* region = c < kPadChunks ? sK(s) : sV(s);
+      *reinterpret_cast<uint4*>(region + BN * 128 + 16 * (c % kPadChunks)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
@@ -436,7 +463,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // warp-uniform); one elected lane issues each tcgen05 instruction.
     {
       constexpr uint32_t fmt = BF16 ? kBF16 : kF16;
-      constexpr uint32_t id_qk = idesc_f16(kBlockM, BN, fmt, fmt, 0, 0);
+      constexpr uint32_t id_qk = idesc_f16(kBlockM, BNP, fmt, fmt, 0, 0);
       // PV in 64-column halves of O (one V atom each)
       constexpr uint32_t id_pv = idesc_f16(kBlockM, 64, kF16, kF16, 0, 1);
       // G: [T_h ; T_w] as one N = 256 product (head_dim 64), or T_h and T_w
@@ -464,7 +491,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int h = 0; h < Dm::kAtoms; ++h) {
           const uint64_t b = d_v + s * kStageStep + h * kKVAtom;
           #pragma unroll
-          for (int k = 0; k < BN / 16; ++k)
+          for (int k = 0; k < BNP / 16; ++k)
             umma_ts_w(tbase + Dm::tmO(i) + 64 * h, tbase + Dm::tmP(i) + 8 * k, b + 128 * k, id_pv,
                       (acc || k > 0) ? 1u : 0u);
         }
@@ -593,8 +620,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t tP = tbase + lane_off + Dm::tmP(wg);
     const uint32_t tO = tbase + lane_off + Dm::tmO(wg);
     float* area = reinterpret_cast<float*>(smem + SM::kBias) + wg * kBlockM * kBiasStride;
-    const int Hpad = n_kv * KHT;
-    const int HS = kBiasStride;  // >= Hpad + 1; a thread's rel_h row is its staging row
+    // a thread's rel_h row is its staging row; it holds the H grid rows only (a
+    // tile's grid rows past H, up to n_kv KHT, read as -inf)
+    const int HS = kBiasStride;
     float* bh_row = area + r * HS;
     const float NEG_INF = -__int_as_float(0x7f800000);
     const float sl2 = args.scale_log2;
@@ -639,7 +667,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // kBiasStride both), read and written by that thread alone
         if (ok) {
           skew_row_to_smem(tbase + lane_off + 256 * wg, qh, H, bh_row, kLog2e);
-          for (int kh = H; kh < Hpad; ++kh) bh_row[kh] = NEG_INF;
         }
         tc_fence_before();
         mbar_arrive(&bars[kBarGFree]);
@@ -715,7 +742,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         ok = wg_sync() && ok;
         if (raw)
           for (int kh = 0; kh < H; ++kh) bh_row[kh] *= kLog2e;   // this thread's own row
-        for (int kh = H; kh < Hpad; ++kh) bh_row[kh] = NEG_INF;
         if (!ok) return false;
       }
       ++seg;
@@ -723,9 +749,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // S is processed in blocks of kBlk columns (one TMEM load and one wait
       // each); narrow grids, with more grid rows per tile, use 16 to keep
       // their per-row bias terms in registers.
-      constexpr int kBlk = WP <= 16 ? 16 : 32;
+      constexpr int kBlk = (WP <= 16 || BNP != BN) ? 16 : 32;
       auto load_block = [&](int cb, uint32_t (&u)[kBlk]) {
-        if (kBlk == 32 && BN - cb >= 32) tmem_ld32(tS + cb, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+        if (kBlk == 32 && BNP - cb >= 32) tmem_ld32(tS + cb, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
         else tmem_ld16(tS + cb, *reinterpret_cast<uint32_t(*)[16]>(&u[0]));
         tmem_wait_ld();
       };
@@ -785,26 +811,30 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           #pragma unroll
           for (int k = 0; k < 16; k += 2) {
             const int col = cb + k;
-            const int g = col / WP, kw = col % WP;
-            float2 t = ffma2(make_float2(__uint_as_float(u[k]), __uint_as_float(u[k + 1])), sl2v,
-                             make_float2(bw[kw], bw[kw + 1]));
-            t = fadd2(t, off[g]);
-            const float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
-            ts[(k / 2) & 3] = fadd2(ts[(k / 2) & 3], p);
-            pk[k / 2] = pack_f16x2(p.x, p.y);
+            if (col < BN) {
+              const int g = col / WP, kw = col % WP;
+              float2 t = ffma2(make_float2(__uint_as_float(u[k]), __uint_as_float(u[k + 1])), sl2v,
+                               make_float2(bw[kw], bw[kw + 1]));
+              t = fadd2(t, off[g]);
+              const float2 p = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+              ts[(k / 2) & 3] = fadd2(ts[(k / 2) & 3], p);
+              pk[k / 2] = pack_f16x2(p.x, p.y);
+            } else {
+              pk[k / 2] = 0u;   // padding columns of the product: P = 0
+            }
           }
           if (cb == 0) wait_pv();
           tmem_st8(tP + cb / 2, pk);
         };
         tmem_ld16(tS, ua);
         #pragma unroll
-        for (int cb = 0; cb < BN; cb += 32) {
+        for (int cb = 0; cb < BNP; cb += 32) {
           tmem_wait_ld();
-          if (cb + 16 < BN) tmem_ld16(tS + cb + 16, ub);
+          if (cb + 16 < BNP) tmem_ld16(tS + cb + 16, ub);
           block(cb, ua);
-          if (cb + 16 < BN) {
+          if (cb + 16 < BNP) {
             tmem_wait_ld();
-            if (cb + 32 < BN) tmem_ld16(tS + cb + 32, ua);
+            if (cb + 32 < BNP) tmem_ld16(tS + cb + 32, ua);
             block(cb + 16, ub);
           }
         }
@@ -831,7 +861,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int kh0 = j * KHT;
         float bhv[KHT];
         #pragma unroll
-        for (int g = 0; g < KHT; ++g) bhv[g] = bh_row[kh0 + g];
+        for (int g = 0; g < KHT; ++g) bhv[g] = kh0 + g < H ? bh_row[kh0 + g] : NEG_INF;
         bool exact = j == sg.j0;
         if (!exact) {
           float hb = bhv[0];

@@ -12,7 +12,7 @@ namespace dera {
 template <int WP, int D>
 cudaError_t launch_attention_d(const AttnMaps& maps, const AttnArgs& args, int ctas, bool fused,
                                cudaStream_t stream) {
-  using SM = AttnSmem<D, KeyTile<WP, D>::BN>;
+  using SM = AttnSmem<D, FwdKeyTile<WP, D>::BN>;
   const bool bf16 = args.in_fmt == kBF16;
   auto kern = fused ? (bf16 ? relpos_attn_kernel<WP, true, true, D> : relpos_attn_kernel<WP, true, false, D>)
                     : (bf16 ? relpos_attn_kernel<WP, false, true, D> : relpos_attn_kernel<WP, false, false, D>);

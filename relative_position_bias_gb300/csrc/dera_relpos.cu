@@ -175,11 +175,13 @@ bool map_table(CUtensorMap* m, const void* p, dera_dtype t, int L, int d) {
 }
 
 int padded_width(int W) { return W <= 16 ? 16 : (W <= 32 ? 32 : (W <= 40 ? 40 : 64)); }
-// grid rows per key tile (KeyTile<WP, d>::KHT)
+// grid rows per key tile (KeyTile<WP, d>::KHT), and the forward's
+// (FwdKeyTile<WP, d>::KHT: three for a 40-column grid with head_dim 64)
 int rows_per_tile(int WP, int d) {
   if (d == 64) return WP <= 16 ? 8 : (WP <= 32 ? 4 : 2);
   return WP <= 16 ? 4 : (WP <= 40 ? 2 : 1);
 }
+int fwd_rows_per_tile(int WP, int d) { return (d == 64 && WP == 40) ? 3 : rows_per_tile(WP, d); }
 
 // Streaming-multiprocessor count of a device (cached; 0 if the query fails).
 int sm_count(int dev) {
@@ -234,7 +236,7 @@ int uncut_ctas(int n_units, int sms) { return sms > 0 && n_units > sms ? sms : n
 Plan make_plan(int BH, int H, int W, int d, int sms) {
   Plan p;
   const int N = H * W;
-  const int KHT = rows_per_tile(padded_width(W), d);
+  const int KHT = fwd_rows_per_tile(padded_width(W), d);
   p.n_qtiles = (N + kBlockM - 1) / kBlockM;
   p.n_pairs = (p.n_qtiles + 1) / 2;
   p.n_units = BH * p.n_pairs;
@@ -302,7 +304,7 @@ dera_status run_attention(const void* q, const void* k, const void* v, const voi
     plan.split = false;  // no (or too small a) workspace: whole units, round-robin
     plan.ctas = uncut_ctas(plan.n_units, sm_count(dev));
   }
-  const int WP = padded_width(W), KHT = rows_per_tile(WP, d);
+  const int WP = padded_width(W), KHT = fwd_rows_per_tile(WP, d);
   AttnMaps maps;
   if (!map_rows(&maps.q, q, in_dtype, BH, N, d) || !map_keys(&maps.k, k, in_dtype, BH, H, W, d, WP, KHT) ||
       !map_keys(&maps.v, v, in_dtype, BH, H, W, d, WP, KHT))

@@ -96,7 +96,7 @@ def default_plan(w: I.Workload) -> tuple[bool, int, int]:
     units_per_head = (-(-w.N // 128) + per - 1) // per
     U = w.BH * units_per_head
     wp = next(x for x in (16, 32, 40, 64) if x >= w.W)
-    kht = {16: 8, 32: 4, 40: 2, 64: 2}[wp] if w.d == 64 else {16: 4, 32: 2, 40: 2, 64: 1}[wp]
+    kht = {16: 8, 32: 4, 40: 3, 64: 2}[wp] if w.d == 64 else {16: 4, 32: 2, 40: 2, 64: 1}[wp]
     n_kv = -(-w.H // kht)
     return (n_kv >= 4 and U > sms and U % sms != 0), U, units_per_head
 
