@@ -620,8 +620,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t tP = tbase + lane_off + Dm::tmP(wg);
     const uint32_t tO = tbase + lane_off + Dm::tmO(wg);
     float* area = reinterpret_cast<float*>(smem + SM::kBias) + wg * kBlockM * kBiasStride;
-    // a thread's rel_h row is its staging row; it holds the H grid rows only (a
-    // tile's grid rows past H, up to n_kv KHT, read as -inf)
+    // A thread's rel_h row is its staging row.  Where n_kv KHT grid rows always
+    // fit in it, those past H hold -inf; with three grid rows per tile (up to
+    // 66 > kBiasStride) the row holds the H grid rows only and a tile's grid
+    // rows past H read as -inf.
+    constexpr bool kPadRows = (64 + KHT - 1) / KHT * KHT < kBiasStride;
+    const int Hpad = n_kv * KHT;
     const int HS = kBiasStride;
     float* bh_row = area + r * HS;
     const float NEG_INF = -__int_as_float(0x7f800000);
@@ -667,6 +671,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // kBiasStride both), read and written by that thread alone
         if (ok) {
           skew_row_to_smem(tbase + lane_off + 256 * wg, qh, H, bh_row, kLog2e);
+          if (kPadRows)
+            for (int kh = H; kh < Hpad; ++kh) bh_row[kh] = NEG_INF;
         }
         tc_fence_before();
         mbar_arrive(&bars[kBarGFree]);
@@ -742,6 +748,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         ok = wg_sync() && ok;
         if (raw)
           for (int kh = 0; kh < H; ++kh) bh_row[kh] *= kLog2e;   // this thread's own row
+        if (kPadRows)
+          for (int kh = H; kh < Hpad; ++kh) bh_row[kh] = NEG_INF;
         if (!ok) return false;
       }
       ++seg;
@@ -861,7 +869,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int kh0 = j * KHT;
         float bhv[KHT];
         #pragma unroll
-        for (int g = 0; g < KHT; ++g) bhv[g] = kh0 + g < H ? bh_row[kh0 + g] : NEG_INF;
+        for (int g = 0; g < KHT; ++g) bhv[g] = (kPadRows || kh0 + g < H) ? bh_row[kh0 + g] : NEG_INF;
         bool exact = j == sg.j0;
         if (!exact) {
           float hb = bhv[0];
