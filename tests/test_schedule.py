@@ -53,7 +53,7 @@ def partition(U: int, G: int, n_kv: int, seg: int):
     return dp, sk, begin, cta_of
 
 
-@pytest.mark.parametrize("n_kv", [1, 2, 3, 5, 8, 16, 20, 32, 64])
+@pytest.mark.parametrize("n_kv", [1, 2, 3, 5, 8, 14, 16, 20, 22, 32, 64])
 @pytest.mark.parametrize("G", [1, 2, 3, 7, 148, 152])
 def test_tail_partition(n_kv, G):
     seg = seg_cost()
